@@ -1,0 +1,281 @@
+"""CPU oracle for the Step-5 sparse-indexer attention (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may
+import this package.  The product path (the CUDA library and its binding) never does.
+
+The arithmetic lives in ``step5_oracle.c`` (plain C, fp64), which follows the
+definition in "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903), the commit
+that adds the CSA indexer.  This module only builds that file with gcc and marshals
+numpy arrays to it.  bf16 tensors travel as uint16 bit patterns and e4m3 tensors as
+uint8 codes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "step5_oracle.c")
+_HDR = os.path.join(_HERE, "step5_oracle.h")
+_LIB = os.path.join(_HERE, "liboracle_step5.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    with _lock:
+        stale = (not os.path.exists(_LIB)) or any(
+            os.path.getmtime(p) > os.path.getmtime(_LIB) for p in (_SRC, _HDR))
+        if force or stale:
+            tmp = _LIB + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-pthread",
+                   "-ffp-contract=off", "-fno-fast-math", "-D_GNU_SOURCE",
+                   _SRC, "-o", tmp, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        sigs = {
+            "orc_round_bf16": (f64, [f64]),
+            "orc_round_e4m3": (f64, [f64]),
+            "orc_bf16_code": (ctypes.c_uint16, [f64]),
+            "orc_bf16_value": (f64, [ctypes.c_uint16]),
+            "orc_e4m3_code": (ctypes.c_uint8, [f64]),
+            "orc_e4m3_value": (f64, [ctypes.c_uint8]),
+            "orc_bf16_codes_to_e4m3_codes": (None, [P, P, i64]),
+            "orc_round_bf16_array": (None, [P, P, i64]),
+            "orc_rotate_neox": (None, [P, i32, i32, P, P, P]),
+            "orc_summarize_region": (None, [P, P, i32, i32, i32, i32, P, P, P, P]),
+            "orc_score_group": (None, [P, P, i32, i32, i32, i32, P, P, P, i64, P]),
+            "orc_select_topk": (i32, [P, i64, i32, P]),
+            "orc_attend_group": (None, [P, i32, i32, P, P, P, i32, i32, i32, f64, P]),
+            "orc_summarize_batch": (i32, [i32, i32, i64, i64, i32, i32, i32, P, P, P, P,
+                                          P, P, P, P, i32]),
+            "orc_score_batch": (i32, [i32, i32, i32, i32, i32, i32, i64, P, P, P, P, P,
+                                      P, P, P, i32]),
+            "orc_select_batch": (i32, [i32, i32, i32, i32, i64, P, P, P, P, i32]),
+            "orc_attend_batch": (i32, [i32, i32, i32, i32, i32, i32, i64, f64, P, P, P,
+                                       P, P, P, P, P, i32]),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+# ----------------------------------------------------------------------------------
+# Codecs
+# ----------------------------------------------------------------------------------
+
+def round_bf16(x: float) -> float:
+    return _load().orc_round_bf16(float(x))
+
+
+def round_e4m3(x: float) -> float:
+    return _load().orc_round_e4m3(float(x))
+
+
+def bf16_value(code: int) -> float:
+    return _load().orc_bf16_value(int(code))
+
+
+def e4m3_value(code: int) -> float:
+    return _load().orc_e4m3_value(int(code))
+
+
+def e4m3_code(v: float) -> int:
+    return int(_load().orc_e4m3_code(float(v)))
+
+
+def bf16_code(v: float) -> int:
+    return int(_load().orc_bf16_code(float(v)))
+
+
+def bf16_codes_to_e4m3_codes(codes: np.ndarray) -> np.ndarray:
+    codes = _c(codes, np.uint16)
+    out = np.empty(codes.shape, dtype=np.uint8)
+    _load().orc_bf16_codes_to_e4m3_codes(_p(codes), _p(out), codes.size)
+    return out
+
+
+def e4m3_values(codes: np.ndarray) -> np.ndarray:
+    """fp64 values of an array of e4m3 codes (table of the 256 codes)."""
+    lib = _load()
+    table = np.array([lib.orc_e4m3_value(c) for c in range(256)], dtype=np.float64)
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def bf16_values(codes: np.ndarray) -> np.ndarray:
+    codes = np.asarray(codes, dtype=np.uint16).astype(np.uint32) << 16
+    with np.errstate(invalid="ignore"):
+        return codes.view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------------
+# Per-item steps
+# ----------------------------------------------------------------------------------
+
+def rotate_neox(x_codes, rope_dims, cos_row=None, sin_row=None) -> np.ndarray:
+    x = _c(x_codes, np.uint16)
+    out = np.empty(x.shape[-1], dtype=np.float64)
+    cs = None if cos_row is None else _c(cos_row, np.uint16)
+    sn = None if sin_row is None else _c(sin_row, np.uint16)
+    _load().orc_rotate_neox(_p(x), x.shape[-1], rope_dims, _p(cs), _p(sn), _p(out))
+    return out
+
+
+def summarize_region(k_codes, z_codes, t0, rope_dims, cos_tab=None, sin_tab=None):
+    """(s fp64 [dim], codes uint8 [dim]) for one region; k, z: [region_tokens][dim]."""
+    k = _c(k_codes, np.uint16)
+    z = _c(z_codes, np.uint16)
+    rt, dim = k.shape
+    s = np.empty(dim, dtype=np.float64)
+    code = np.empty(dim, dtype=np.uint8)
+    cs = None if cos_tab is None else _c(cos_tab, np.uint16)
+    sn = None if sin_tab is None else _c(sin_tab, np.uint16)
+    _load().orc_summarize_region(_p(k), _p(z), rt, dim, int(t0), rope_dims, _p(cs), _p(sn),
+                                 _p(s), _p(code))
+    return s, code
+
+
+def score_group(q_codes, w, pos, rope_dims, summ_codes, cos_tab=None, sin_tab=None):
+    """fp64 scores [R] of one (row, group); q: [hpg][dim] codes, w: [hpg] fp32."""
+    q = _c(q_codes, np.uint16)
+    w = _c(w, np.float32)
+    s = _c(summ_codes, np.uint8)
+    hpg, dim = q.shape
+    R = s.shape[0]
+    out = np.empty(R, dtype=np.float64)
+    cs = None if cos_tab is None else _c(cos_tab, np.uint16)
+    sn = None if sin_tab is None else _c(sin_tab, np.uint16)
+    _load().orc_score_group(_p(q), _p(w), hpg, dim, int(pos), rope_dims, _p(cs), _p(sn),
+                            _p(s), R, _p(out))
+    return out
+
+
+def select_topk(scores, K) -> np.ndarray:
+    sc = _c(scores, np.float64)
+    ids = np.full(max(K, 1), -1, dtype=np.int32)
+    cnt = _load().orc_select_topk(_p(sc), sc.size, K, _p(ids))
+    return ids[:cnt]
+
+
+def attend_group(q_codes, k_cache, v_cache, sel, pos, region_tokens, scale) -> np.ndarray:
+    """fp64 [hq_g][head_dim]; k/v cache: [t_cap][head_dim] codes of one (seq, group)."""
+    q = _c(q_codes, np.uint16)
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    sel = _c(sel, np.int32)
+    hq, D = q.shape
+    out = np.empty((hq, D), dtype=np.float64)
+    _load().orc_attend_group(_p(q), hq, D, _p(kc), _p(vc), _p(sel), sel.size, int(pos),
+                             region_tokens, float(scale), _p(out))
+    return out
+
+
+# ----------------------------------------------------------------------------------
+# Batched steps (same layouts as the CUDA library's entry points)
+# ----------------------------------------------------------------------------------
+
+def summarize_batch(idx_k, idx_z, cos_tab, sin_tab, region_begin, region_end, r_cap,
+                    rope_dims, region_tokens=8, summ=None, want_f64=False, nthreads=0):
+    """idx_k/idx_z: [B][G][t_cap][dim] uint16.  Writes into ``summ`` ([B][G][r_cap][dim]
+    uint8, created zero-filled if None).  Returns (summ, s_f64 or None, threads)."""
+    k = _c(idx_k, np.uint16)
+    z = _c(idx_z, np.uint16)
+    B, G, t_cap, dim = k.shape
+    if summ is None:
+        summ = np.zeros((B, G, r_cap, dim), dtype=np.uint8)
+    assert summ.flags.c_contiguous and summ.dtype == np.uint8
+    s64 = np.zeros((B, G, r_cap, dim), dtype=np.float64) if want_f64 else None
+    cs = None if cos_tab is None else _c(cos_tab, np.uint16)
+    sn = None if sin_tab is None else _c(sin_tab, np.uint16)
+    rb = _c(region_begin, np.int32)
+    re = _c(region_end, np.int32)
+    th = _load().orc_summarize_batch(B, G, t_cap, r_cap, dim, region_tokens, rope_dims,
+                                     _p(k), _p(z), _p(cs), _p(sn), _p(rb), _p(re),
+                                     _p(summ), _p(s64), nthreads)
+    return summ, s64, th
+
+
+def score_batch(idx_q, w, row_seq, row_pos, summ, G, rope_dims, cos_tab=None,
+                sin_tab=None, region_tokens=8, nthreads=0):
+    """Returns (scores fp64 [N][G][r_cap] (NaN past each row's R), threads)."""
+    q = _c(idx_q, np.uint16)
+    w = _c(w, np.float32)
+    s = _c(summ, np.uint8)
+    N, idx_heads, dim = q.shape
+    r_cap = s.shape[2]
+    scores = np.full((N, G, r_cap), np.nan, dtype=np.float64)
+    cs = None if cos_tab is None else _c(cos_tab, np.uint16)
+    sn = None if sin_tab is None else _c(sin_tab, np.uint16)
+    seq = _c(row_seq, np.int32)
+    pos = _c(row_pos, np.int32)
+    th = _load().orc_score_batch(N, G, idx_heads, dim, region_tokens, rope_dims, r_cap,
+                                 _p(q), _p(w), _p(seq), _p(pos), _p(cs), _p(sn), _p(s),
+                                 _p(scores), nthreads)
+    return scores, th
+
+
+def select_batch(scores, row_pos, K=512, region_tokens=8, nthreads=0):
+    """scores: [N][G][r_cap] (any float dtype; converted exactly to fp64).
+    Returns (sel_ids [N][G][K] padded with -1, sel_count [N][G], threads)."""
+    sc = _c(scores, np.float64)
+    N, G, r_cap = sc.shape
+    pos = _c(row_pos, np.int32)
+    ids = np.empty((N, G, K), dtype=np.int32)
+    cnt = np.empty((N, G), dtype=np.int32)
+    th = _load().orc_select_batch(N, G, K, region_tokens, r_cap, _p(pos), _p(sc), _p(ids),
+                                  _p(cnt), nthreads)
+    return ids, cnt, th
+
+
+def attend_batch(q, k_cache, v_cache, row_seq, row_pos, sel_ids, sel_count, scale,
+                 region_tokens=8, nthreads=0):
+    """q: [N][Hq][D], caches [B][G][t_cap][D] (uint16).  Returns (out fp64, threads)."""
+    qq = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    N, Hq, D = qq.shape
+    B, G, t_cap, _ = kc.shape
+    ids = _c(sel_ids, np.int32)
+    cnt = _c(sel_count, np.int32)
+    K = ids.shape[2]
+    out = np.empty((N, Hq, D), dtype=np.float64)
+    th = _load().orc_attend_batch(N, G, Hq, D, region_tokens, K, t_cap, float(scale),
+                                  _p(qq), _p(kc), _p(vc), _p(_c(row_seq, np.int32)),
+                                  _p(_c(row_pos, np.int32)), _p(ids), _p(cnt), _p(out),
+                                  nthreads)
+    return out, th
+
+
+def bf16_round_array(x: np.ndarray) -> np.ndarray:
+    """Round an fp64 array to bf16 codes with the oracle's own rounding."""
+    flat = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(flat.shape, dtype=np.uint16)
+    _load().orc_round_bf16_array(_p(flat), _p(out), flat.size)
+    return out

@@ -1,0 +1,126 @@
+/*
+ * step5_oracle.h -- plain, slow CPU oracle for the Step-5 sparse-indexer attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls this
+ * library; only the tests, the smoke check and the benchmark's CPU-baseline leg do.
+ * It shares no code, header, table or helper with the CUDA library.
+ *
+ * Source of the method: "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903),
+ * the commit that adds the CSA indexer "for contexts to 1M tokens": every completed
+ * 8-token region is summarised as a per-dim softmax over z of the indexer k, rounded
+ * through bf16 to e4m3; scores are sum_h relu(e4m3(q_h) . summary) * w_h per KV group;
+ * the top 512 regions by (-score, id), ascending, are kept; attention runs over those
+ * regions and the row's own region.  The indexer's q and k take NEOX rotation on their
+ * first 32 dims from bf16 cos/sin (same page, the commit on Step-5's glue).
+ *
+ * Arithmetic: fp64 everywhere except at the rounding points the page fixes
+ * (bf16 after rotation, bf16 then e4m3 for summaries, e4m3 for the indexer q).
+ * Codes: bf16 values travel as uint16 bit patterns, e4m3 values as uint8 codes
+ * (OCP FP8 E4M3 "fn": bias 7, 3 mantissa bits, no infinities, 0x7F/0xFF = NaN).
+ */
+#ifndef STEP5_ORACLE_H
+#define STEP5_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- codecs (format definitions: bfloat16 = IEEE binary32 with 7 stored mantissa
+ *      bits; OCP 8-bit floating point, E4M3 with saturation) ---------------------- */
+double   orc_round_bf16(double x);      /* nearest bf16 value, ties to even; overflow -> inf */
+double   orc_round_e4m3(double x);      /* nearest e4m3 value, ties to even; |x|>448 -> 448 */
+uint16_t orc_bf16_code(double v);       /* bit pattern of a bf16-representable value        */
+double   orc_bf16_value(uint16_t code);
+uint8_t  orc_e4m3_code(double v);       /* code of an e4m3-representable value (or NaN)      */
+double   orc_e4m3_value(uint8_t code);
+void     orc_bf16_codes_to_e4m3_codes(const uint16_t* in, uint8_t* out, int64_t n);
+void     orc_round_bf16_array(const double* in, uint16_t* out_codes, int64_t n);
+
+/* ---- NEOX partial rotation (the page's glue commit: "q/k norm and NEOX rotation from
+ *      bf16 cos/sin"; the indexer commit: "NEOX on their first 32 dims") -----------
+ * x: dim bf16 codes.  Pairs (i, i + rope_dims/2) for i < rope_dims/2 rotate by the
+ * angle whose bf16 cosine/sine are cos_row[i]/sin_row[i].  Each rotated element is
+ * x1*c - x2*s (first half) or x2*c + x1*s (second half), rounded once to bf16.
+ * cos_row == NULL means "already rotated": out = x.  out: dim doubles (bf16 values). */
+void orc_rotate_neox(const uint16_t* x, int dim, int rope_dims,
+                     const uint16_t* cos_row, const uint16_t* sin_row, double* out);
+
+/* ---- step 1: region summary -------------------------------------------------------
+ * k, z: region_tokens rows of dim bf16 codes (row stride dim).  Token j sits at
+ * position t0 + j; its rotation row is cos_tab[(t0 + j) * (rope_dims/2)].
+ * s_out[d] = sum_j softmax_j(z[., d]) * rot(k)[j][d]   (fp64)
+ * code_out[d] = e4m3(bf16(s_out[d])).                                                */
+void orc_summarize_region(const uint16_t* k, const uint16_t* z, int region_tokens,
+                          int dim, int t0, int rope_dims,
+                          const uint16_t* cos_tab, const uint16_t* sin_tab,
+                          double* s_out, uint8_t* code_out);
+
+/* ---- step 2: index scores for one (row, KV group) ---------------------------------
+ * q: hpg indexer heads x dim bf16 codes (the group's heads), w: hpg floats, row at
+ * position pos.  summ: R regions x dim e4m3 codes.
+ * out[r] = sum_h relu( sum_d e4m3(bf16(rot(q_h)))[d] * summ[r][d] ) * w_h  (fp64;
+ * the inner sum is exact in fp64).  -0 is returned as +0.                           */
+void orc_score_group(const uint16_t* q, const float* w, int hpg, int dim, int pos,
+                     int rope_dims, const uint16_t* cos_tab, const uint16_t* sin_tab,
+                     const uint8_t* summ, int64_t R, double* out);
+
+/* ---- step 3: selection for one (row, KV group) ------------------------------------
+ * Sorts the R keys (-score, id) ascending and writes the first min(K, R) ids in that
+ * order.  Returns the count.  scores are fp64 (an fp32 score converts exactly).      */
+int orc_select_topk(const double* scores, int64_t R, int K, int32_t* ids_out);
+
+/* ---- step 4: attention for one (row, KV group) -------------------------------------
+ * q: hq_g query heads x head_dim bf16 codes.  kc, vc: this (sequence, group)'s cache,
+ * t_cap rows x head_dim bf16 codes.  Keys: every token of the cnt regions in sel, then
+ * the tokens rt*o .. pos of the row's own region o = pos / rt.
+ * out[h][d] = sum_t softmax_t(scale * q_h . k_t) v_t[d]   (fp64, max-subtracted).     */
+void orc_attend_group(const uint16_t* q, int hq_g, int head_dim,
+                      const uint16_t* kc, const uint16_t* vc,
+                      const int32_t* sel, int cnt, int pos, int region_tokens,
+                      double scale, double* out);
+
+/* ---- batched drivers: plain loops over independent items, spread over nthreads
+ *      host threads (0 = all online cores).  They add no arithmetic of their own. ---- */
+
+/* Summaries for b in [0,B), g in [0,G), r in [region_begin[b], region_end[b]).
+ * k, z: [B][G][t_cap][dim].  summ: [B][G][r_cap][dim] codes; s_f64 (nullable) same
+ * shape in fp64.  Returns the threads used.                                          */
+int orc_summarize_batch(int B, int G, int64_t t_cap, int64_t r_cap, int dim,
+                        int region_tokens, int rope_dims,
+                        const uint16_t* k, const uint16_t* z,
+                        const uint16_t* cos_tab, const uint16_t* sin_tab,
+                        const int32_t* region_begin, const int32_t* region_end,
+                        uint8_t* summ, double* s_f64, int nthreads);
+
+/* Scores for n in [0,N), g in [0,G), r < row_pos[n] / region_tokens.
+ * q: [N][idx_heads][dim], w: [N][idx_heads]; group g owns heads [g*hpg, (g+1)*hpg).
+ * summ: [B][G][r_cap][dim].  scores: [N][G][r_cap] fp64 (entries past R untouched). */
+int orc_score_batch(int N, int G, int idx_heads, int dim, int region_tokens,
+                    int rope_dims, int64_t r_cap,
+                    const uint16_t* q, const float* w,
+                    const int32_t* row_seq, const int32_t* row_pos,
+                    const uint16_t* cos_tab, const uint16_t* sin_tab,
+                    const uint8_t* summ, double* scores, int nthreads);
+
+/* Selections for every (n, g) from scores [N][G][r_cap] (fp64), R = row_pos/rt.
+ * sel_ids: [N][G][K], padded with -1; sel_count: [N][G].                             */
+int orc_select_batch(int N, int G, int K, int region_tokens, int64_t r_cap,
+                     const int32_t* row_pos, const double* scores,
+                     int32_t* sel_ids, int32_t* sel_count, int nthreads);
+
+/* Attention for every (n, g).  q: [N][num_q_heads][head_dim]; kc, vc:
+ * [B][G][t_cap][head_dim]; sel_ids [N][G][K], sel_count [N][G];
+ * out: [N][num_q_heads][head_dim] fp64.                                              */
+int orc_attend_batch(int N, int G, int num_q_heads, int head_dim, int region_tokens,
+                     int K, int64_t t_cap, double scale,
+                     const uint16_t* q, const uint16_t* kc, const uint16_t* vc,
+                     const int32_t* row_seq, const int32_t* row_pos,
+                     const int32_t* sel_ids, const int32_t* sel_count,
+                     double* out, int nthreads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
