@@ -1,0 +1,227 @@
+"""Python binding of libstep5sa: the Step-5 sparse-indexer attention on GB300 (sm_103a).
+
+Thin ctypes marshalling over the C ABI declared in ``include/step5_sparse_attn.h``:
+each function takes torch tensors that already live on the GPU, passes their device
+pointers and the current CUDA stream, and raises ``Step5Error`` on a non-OK status.
+Every step of the computation runs in the library's kernels; there is no other path.
+If the library has not been built, the first call raises.
+
+Steps (TensorFold PR #903, "Step-5-Preview on one 256 GB Mac", CSA-indexer commit):
+  step5_region_summarize  -- e4m3 summary of each completed 8-token region
+  step5_index_score_topk  -- sum_h relu(e4m3(q_h) . summary) * w_h, top-k by (-score, id)
+  step5_sparse_attn       -- attention over the picked regions plus the row's own region
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from ._build import LIB, build  # noqa: F401
+
+__all__ = [
+    "Step5Error", "Geometry", "STEP5_GEOMETRY", "library_path", "load",
+    "step5_region_summarize", "step5_index_score_topk", "step5_sparse_attn",
+    "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
+    "step5_set_select_path", "step5_status_string", "step5_convert_bf16_to_e4m3",
+    "Workspace", "decode_step",
+]
+
+STATUS = {0: "STEP5_OK", 1: "STEP5_ERR_INVALID_ARGUMENT", 2: "STEP5_ERR_UNSUPPORTED",
+          3: "STEP5_ERR_WORKSPACE", 4: "STEP5_ERR_CUDA", 5: "STEP5_ERR_TIMEOUT"}
+DEV_RANGE, DEV_TIMEOUT = 1, 2
+
+
+class Step5Error(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)}" + (f" ({detail})" if detail else ""))
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_groups", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("idx_heads", ctypes.c_int32),
+                ("idx_dim", ctypes.c_int32), ("rope_dims", ctypes.c_int32),
+                ("region_tokens", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float)]
+
+    @classmethod
+    def step5(cls, **over) -> "Geometry":
+        vals = dict(num_q_heads=32, num_kv_groups=4, head_dim=128, idx_heads=16, idx_dim=64,
+                    rope_dims=32, region_tokens=8, top_k=512, softmax_scale=1.0 / math.sqrt(128.0))
+        vals.update(over)
+        return cls(**vals)
+
+    @classmethod
+    def of(cls, g) -> "Geometry":
+        if isinstance(g, Geometry):
+            return g
+        return cls(g.num_q_heads, g.num_kv_groups, g.head_dim, g.idx_heads, g.idx_dim,
+                   g.rope_dims, g.region_tokens, g.top_k, g.softmax_scale)
+
+
+STEP5_GEOMETRY = Geometry.step5()
+
+_lib = None
+
+
+def library_path() -> str:
+    return LIB
+
+
+def load():
+    """Loads libstep5sa.so (raises if it is missing: build it with ``build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB):
+        raise RuntimeError(f"{LIB} is not built; run block_sparse_attention_step5_gb300.build() "
+                           "(nvcc, sm_103a) first")
+    lib = ctypes.CDLL(LIB)
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    G = ctypes.POINTER(Geometry)
+    sigs = {
+        "step5_region_summarize": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]),
+        "step5_index_score_topk": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P,
+                                         P, sz, P]),
+        "step5_sparse_attn": (i32, [G, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]),
+        "step5_workspace_bytes": (sz, [G, i32, i32]),
+        "step5_workspace_init": (i32, [P, sz, P]),
+        "step5_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32), P]),
+        "step5_set_select_path": (i32, [i32]),
+        "step5_status_string": (ctypes.c_char_p, [i32]),
+        "step5_convert_bf16_to_e4m3": (i32, [P, P, i64, P]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libstep5sa must be on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libstep5sa must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise Step5Error(fn, status)
+
+
+def step5_status_string(status: int) -> str:
+    return load().step5_status_string(status).decode()
+
+
+def step5_set_select_path(mode: int) -> int:
+    """0 = automatic, 1 = one block per (row, group), 2 = histogram split path."""
+    return load().step5_set_select_path(mode)
+
+
+def step5_workspace_bytes(geom, N: int, r_cap: int) -> int:
+    return load().step5_workspace_bytes(ctypes.byref(Geometry.of(geom)), N, r_cap)
+
+
+def step5_workspace_init(workspace: torch.Tensor, stream=None):
+    _check("step5_workspace_init", load().step5_workspace_init(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def step5_device_status(stream=None) -> int:
+    """Reads and clears the device status word (synchronises the stream)."""
+    v = ctypes.c_uint32(0)
+    st = load().step5_device_status(ctypes.byref(v), _stream(stream))
+    if st not in (0, 5):
+        _check("step5_device_status", st)
+    return v.value
+
+
+def step5_convert_bf16_to_e4m3(x: torch.Tensor, out: torch.Tensor, stream=None):
+    assert x.dtype == torch.bfloat16 and out.dtype == torch.uint8 and out.numel() == x.numel()
+    _check("step5_convert_bf16_to_e4m3", load().step5_convert_bf16_to_e4m3(
+        _ptr(x), _ptr(out), x.numel(), _stream(stream)))
+
+
+def step5_region_summarize(geom, idx_k, idx_z, cos, sin, region_begin, region_end,
+                           summaries, summaries_f32=None, max_regions_per_seq=None, stream=None):
+    """idx_k/idx_z [B][G][t_cap][64] bf16, cos/sin [t_cap][rope/2] bf16 (or None),
+    region_begin/end [B] int32, summaries [B][G][r_cap][64] uint8 (written)."""
+    B, G, t_cap, _ = idx_k.shape
+    r_cap = summaries.shape[2]
+    if max_regions_per_seq is None:
+        max_regions_per_seq = r_cap
+    _check("step5_region_summarize", load().step5_region_summarize(
+        ctypes.byref(Geometry.of(geom)), B, t_cap, r_cap, int(max_regions_per_seq),
+        _ptr(idx_k), _ptr(idx_z), _ptr(cos), _ptr(sin), _ptr(region_begin), _ptr(region_end),
+        _ptr(summaries), _ptr(summaries_f32), _stream(stream)))
+
+
+def step5_index_score_topk(geom, idx_q, w, row_seq, row_pos, cos, sin, summaries, sel_ids,
+                           sel_count, workspace, t_cap, scores=None, sel_scores=None, stream=None):
+    """idx_q [N][idx_heads][64] bf16, w [N][idx_heads] fp32, row_seq/row_pos [N] int32,
+    summaries [B][G][r_cap][64] uint8; writes sel_ids [N][G][top_k], sel_count [N][G]."""
+    N = idx_q.shape[0]
+    B, _, r_cap, _ = summaries.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("step5_index_score_topk", load().step5_index_score_topk(
+        ctypes.byref(Geometry.of(geom)), N, B, int(t_cap), r_cap, _ptr(idx_q), _ptr(w),
+        _ptr(row_seq), _ptr(row_pos), _ptr(cos), _ptr(sin), _ptr(summaries), _ptr(sel_ids),
+        _ptr(sel_count), _ptr(scores), _ptr(sel_scores), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def step5_sparse_attn(geom, q, k_cache, v_cache, row_seq, row_pos, sel_ids, sel_count, out,
+                      workspace, stream=None):
+    """q [N][Hq][128] bf16, k/v cache [B][G][t_cap][128] bf16 -> out [N][Hq][128] bf16."""
+    N = q.shape[0]
+    B, _, t_cap, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("step5_sparse_attn", load().step5_sparse_attn(
+        ctypes.byref(Geometry.of(geom)), N, B, t_cap, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(row_seq), _ptr(row_pos), _ptr(sel_ids), _ptr(sel_count), _ptr(out), _ptr(workspace),
+        ws_bytes, _stream(stream)))
+
+
+@dataclass
+class Workspace:
+    """Device workspace for N rows and r_cap summary slots, zeroed once on creation."""
+    tensor: torch.Tensor
+
+    @classmethod
+    def create(cls, geom, N: int, r_cap: int, device="cuda") -> "Workspace":
+        nbytes = step5_workspace_bytes(geom, N, r_cap)
+        if nbytes == 0:
+            raise Step5Error("step5_workspace_bytes", 2, "unsupported geometry")
+        t = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        step5_workspace_init(t)
+        return cls(t)
+
+
+def decode_step(geom, t: dict, ws: Workspace, sel_ids, sel_count, out, max_regions_per_seq,
+                summarize: bool = True, stream=None):
+    """One pass of the whole path over the tensors of ``t`` (keys as produced by the
+    synthetic workload module): summarise [sum_begin, sum_end), score + select, attend."""
+    if summarize:
+        step5_region_summarize(geom, t["idx_k"], t["idx_z"], t["cos"], t["sin"], t["sum_begin"],
+                               t["sum_end"], t["summaries"],
+                               max_regions_per_seq=max_regions_per_seq, stream=stream)
+    step5_index_score_topk(geom, t["idx_q"], t["w"], t["row_seq"], t["row_pos"], t["cos"],
+                           t["sin"], t["summaries"], sel_ids, sel_count, ws.tensor,
+                           t_cap=t["idx_k"].shape[2], stream=stream)
+    step5_sparse_attn(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
+                      sel_ids, sel_count, out, ws.tensor, stream=stream)

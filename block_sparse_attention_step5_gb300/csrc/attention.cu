@@ -1,0 +1,379 @@
+// attention.cu -- step (4): attention over the picked regions plus the row's own region.
+//
+// "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903), CSA-indexer commit:
+// "attention over those regions and the row's own"; below 512 regions every region is
+// read, which is the dense attention it replaces.  The same page's decode kernel splits
+// a row's keys over many workers and merges their online-softmax states in a fixed
+// order ("one simdgroup walking every key alone left decode waiting on loads").
+//
+// Design (sm_103a):
+//  * work item = (row, KV group, split); a split is a run of entries of the row's key
+//    list (picked regions in selection order, then the own region); 4 warps per block,
+//    each warp takes pairs of entries (16 tokens) with its own 2-stage pipeline.
+//  * a region is a contiguous 2 KB tile of the [B][G][t_cap][128] cache; it is fetched
+//    with two 2-D TMA boxes (64 dims x 8 rows each) into 128-byte-swizzled shared
+//    memory, so the ldmatrix reads below hit 8 distinct bank groups.
+//  * S = Q K^T and O += P V run on bf16 mma.sync (m16n8k16, fp32 accumulate) with the
+//    group's query heads as the 16-row left operand (4, 8 or 16 heads; unused rows are
+//    zero); P is rounded to bf16 for the PV product, the softmax state is fp32.
+//  * the 4 warps merge through shared memory; splits of one (row, group) write fp32
+//    partial states and the block that finishes last (atomic ticket, no waiting) merges
+//    them in split order, so the result does not depend on timing.
+#include "kernels.cuh"
+
+namespace step5 {
+
+namespace {
+
+constexpr int kThreads = kAttnWarps * 32;
+constexpr int kRegionBytes = 2048;                    // 8 tokens x 128 dims x bf16
+constexpr int kPairBytes = 4 * kRegionBytes;          // K (2 regions) + V (2 regions)
+constexpr int kStageBytes = kAttnWarps * kAttnStages * kPairBytes;
+constexpr int kMergeFloatsPerWarp = 16 * 128 + 32;    // O[16][128], m[16], l[16]
+constexpr size_t kSmemBytes = kStageBytes + kAttnWarps * kAttnStages * 8 + 1024;
+static_assert(kAttnWarps * kMergeFloatsPerWarp * 4 <= kStageBytes, "merge area must fit");
+
+// Shared-memory byte offset of (token row t, 16-byte chunk c16 of the 256-byte row) in a
+// region tile written by two 64-dim TMA boxes with 128-byte swizzle.
+__device__ __forceinline__ uint32_t tile_off(int t, int c16) {
+    const int half = c16 >> 3, c = c16 & 7;
+    return (uint32_t)(half * 1024 + t * 128 + ((c ^ t) << 4));
+}
+
+__global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                const __grid_constant__ CUtensorMap vmap,
+                                                                AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageBytes);
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x, g = blockIdx.y, n = blockIdx.z;
+    const int64_t ng = (int64_t)n * p.G + g;
+    const int hq_g = p.hq_g;
+
+    if (tid == 0) {
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&vmap);
+    }
+    pdl_wait();
+
+    const int b = p.row_seq[n];
+    const int pos = p.row_pos[n];
+    if (b < 0 || b >= p.B || pos < 0 || pos >= p.t_cap) {
+        if (split == 0) {
+            if (tid == 0) raise_status(p.status, kDevRange);
+            for (int i = tid; i < hq_g * 128; i += kThreads)
+                p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g) * 128 + i] = 0;
+        }
+        return;
+    }
+    int cnt = p.sel_count[ng];
+    if (cnt < 0 || cnt > p.top_k) {
+        if (split == 0 && tid == 0) raise_status(p.status, kDevRange);
+        cnt = cnt < 0 ? 0 : p.top_k;
+    }
+    const int own = pos >> 3;
+    const int own_tokens = pos - own * 8 + 1;
+    const int E = cnt + 1;
+    const int e0 = split * p.entries_per_split;
+    const int e1 = min(E, e0 + p.entries_per_split);
+    const int npairs = e1 > e0 ? (e1 - e0 + 1) >> 1 : 0;
+    const int nmy = npairs > warp ? (npairs - warp + kAttnWarps - 1) / kAttnWarps : 0;
+    const int32_t* ids = p.sel_ids + ng * p.top_k;
+    const int64_t row_base = ((int64_t)b * p.G + g) * p.t_cap;
+
+    uint8_t* wstage = smem + warp * kAttnStages * kPairBytes;
+    uint64_t* wbar = bars + warp * kAttnStages;
+    if (lane == 0) {
+        for (int st = 0; st < kAttnStages; ++st) mbar_init(&wbar[st], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    // entry e -> (region id, valid tokens); invalid ids are masked out entirely
+    auto entry = [&](int e, int& rid) -> int {
+        if (e >= e1) {
+            rid = -1;
+            return 0;
+        }
+        if (e == cnt) {
+            rid = own;
+            return own_tokens;
+        }
+        rid = ids[e];
+        if (rid < 0 || rid >= own) {
+            raise_status(p.status, kDevRange);
+            rid = -1;
+            return 0;
+        }
+        return 8;
+    };
+
+    auto issue = [&](int li) {
+        if (lane != 0) return;
+        const int pi = warp + li * kAttnWarps;
+        const int st = li % kAttnStages;
+        uint8_t* kt = wstage + st * kPairBytes;
+        uint8_t* vt = kt + 2 * kRegionBytes;
+        int ra, rb;
+        const int na = entry(e0 + 2 * pi, ra);
+        const int nb = entry(e0 + 2 * pi + 1, rb);
+        const uint32_t bytes = (uint32_t)(((na > 0) + (nb > 0)) * 2 * kRegionBytes);
+        mbar_arrive_expect_tx(&wbar[st], bytes);
+        if (na > 0) {
+            const int y = (int)(row_base + (int64_t)ra * 8);
+            tma_load_2d(kt, &kmap, &wbar[st], 0, y);
+            tma_load_2d(kt + 1024, &kmap, &wbar[st], 64, y);
+            tma_load_2d(vt, &vmap, &wbar[st], 0, y);
+            tma_load_2d(vt + 1024, &vmap, &wbar[st], 64, y);
+        }
+        if (nb > 0) {
+            const int y = (int)(row_base + (int64_t)rb * 8);
+            tma_load_2d(kt + kRegionBytes, &kmap, &wbar[st], 0, y);
+            tma_load_2d(kt + kRegionBytes + 1024, &kmap, &wbar[st], 64, y);
+            tma_load_2d(vt + kRegionBytes, &vmap, &wbar[st], 0, y);
+            tma_load_2d(vt + kRegionBytes + 1024, &vmap, &wbar[st], 64, y);
+        }
+    };
+
+    for (int li = 0; li < kAttnStages && li < nmy; ++li) issue(li);
+
+    // query heads of the group as the A operand (rows >= hq_g are zero)
+    const int qr = lane >> 2, qc = (lane & 3) * 2;
+    uint32_t qa[8][4];
+    {
+        const uint16_t* qb = p.q + ((int64_t)n * p.Hq + (int64_t)g * hq_g) * 128;
+        const bool v0 = qr < hq_g, v1 = qr + 8 < hq_g;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int c = kk * 16 + qc;
+            qa[kk][0] = v0 ? *reinterpret_cast<const uint32_t*>(qb + qr * 128 + c) : 0u;
+            qa[kk][1] = v1 ? *reinterpret_cast<const uint32_t*>(qb + (qr + 8) * 128 + c) : 0u;
+            qa[kk][2] = v0 ? *reinterpret_cast<const uint32_t*>(qb + qr * 128 + c + 8) : 0u;
+            qa[kk][3] = v1 ? *reinterpret_cast<const uint32_t*>(qb + (qr + 8) * 128 + c + 8) : 0u;
+        }
+    }
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    float o[16][4];
+#pragma unroll
+    for (int nn = 0; nn < 16; ++nn) o[nn][0] = o[nn][1] = o[nn][2] = o[nn][3] = 0.0f;
+
+    int li_fail = -1;
+    for (int li = 0; li < nmy; ++li) {
+        const int pi = warp + li * kAttnWarps;
+        const int st = li % kAttnStages;
+        uint8_t* kt = wstage + st * kPairBytes;
+        uint8_t* vt = kt + 2 * kRegionBytes;
+        int ra, rb;
+        const int na = entry(e0 + 2 * pi, ra);
+        const int nb = entry(e0 + 2 * pi + 1, rb);
+        if (!mbar_wait(&wbar[st], (uint32_t)((li / kAttnStages) & 1))) {
+            li_fail = li;
+            break;
+        }
+        // zero the V rows of masked tokens so that 0-weight rows stay finite
+        if (na < 8 || nb < 8) {
+            for (int i = lane; i < 2 * 8 * 16; i += 32) {
+                const int slot = i >> 7, t = (i >> 4) & 7, c16 = i & 15;
+                const int valid = slot ? nb : na;
+                if (t >= valid)
+                    *reinterpret_cast<uint4*>(vt + slot * kRegionBytes + tile_off(t, c16)) =
+                        make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+        }
+        const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+
+        // S = Q K^T over the 16 tokens (slot 0: tokens 0-7, slot 1: tokens 8-15)
+        float s[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
+            const int mat = lane >> 3, t = lane & 7;
+#pragma unroll
+            for (int kk = 0; kk < 8; kk += 2) {
+                const int c16 = 2 * (kk + (mat >> 1)) + (mat & 1);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(b0, b1, b2, b3, kbase + j * kRegionBytes + tile_off(t, c16));
+                mma_bf16_16816(s[j], qa[kk], b0, b1);
+                mma_bf16_16816(s[j], qa[kk + 1], b2, b3);
+            }
+        }
+        // scale, mask, online softmax (rows qr and qr + 8)
+        const int tq = (lane & 3) * 2;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int valid = j ? nb : na;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = tq + (e & 1);
+                s[j][e] = (t < valid) ? s[j][e] * p.scale_log2 : -INFINITY;
+            }
+            mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
+            mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float base0 = (mn0 == -INFINITY) ? 0.0f : mn0;
+        const float base1 = (mn1 == -INFINITY) ? 0.0f : mn1;
+        const float a0 = exp2f(m0 - base0), a1 = exp2f(m1 - base1);
+        m0 = mn0;
+        m1 = mn1;
+        float pr[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            pr[j][0] = exp2f(s[j][0] - base0);
+            pr[j][1] = exp2f(s[j][1] - base0);
+            pr[j][2] = exp2f(s[j][2] - base1);
+            pr[j][3] = exp2f(s[j][3] - base1);
+        }
+        l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+        l1 = l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+#pragma unroll
+        for (int nn = 0; nn < 16; ++nn) {
+            o[nn][0] *= a0;
+            o[nn][1] *= a0;
+            o[nn][2] *= a1;
+            o[nn][3] *= a1;
+        }
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+        pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+        pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+        pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+        // O += P V
+        {
+            const int mat = lane >> 3, t = lane & 7;
+            const int slot = mat & 1;
+#pragma unroll
+            for (int nn = 0; nn < 16; nn += 2) {
+                const int c16 = nn + (mat >> 1);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4_trans(b0, b1, b2, b3, vbase + slot * kRegionBytes + tile_off(t, c16));
+                mma_bf16_16816(o[nn], pa, b0, b1);
+                mma_bf16_16816(o[nn + 1], pa, b2, b3);
+            }
+        }
+        __syncwarp();
+        fence_proxy_async();
+        if (li + kAttnStages < nmy) issue(li + kAttnStages);
+    }
+    if (li_fail >= 0) {
+        if (lane == 0) raise_status(p.status, kDevTimeout);
+        // give the copies this warp issued and did not consume a bounded chance to land
+        // before the block's shared memory goes away
+        for (int li = li_fail + 1; li < nmy && li < li_fail + kAttnStages; ++li)
+            mbar_wait(&wbar[li % kAttnStages], (uint32_t)((li / kAttnStages) & 1));
+    }
+
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+    // ---- merge the 4 warps through shared memory (reuses the stage buffers)
+    __syncthreads();
+    float* mw = reinterpret_cast<float*>(smem) + warp * kMergeFloatsPerWarp;
+#pragma unroll
+    for (int nn = 0; nn < 16; ++nn) {
+        const int d = nn * 8 + qc;
+        mw[qr * 128 + d] = o[nn][0];
+        mw[qr * 128 + d + 1] = o[nn][1];
+        mw[(qr + 8) * 128 + d] = o[nn][2];
+        mw[(qr + 8) * 128 + d + 1] = o[nn][3];
+    }
+    if ((lane & 3) == 0) {
+        mw[2048 + qr] = m0;
+        mw[2048 + qr + 8] = m1;
+        mw[2048 + 16 + qr] = l0;
+        mw[2048 + 16 + qr + 8] = l1;
+    }
+    __syncthreads();
+
+    const float* mall = reinterpret_cast<const float*>(smem);
+    const int d = tid;  // 128 threads = 128 dims
+    float* part = p.partial + (ng * p.splits + split) * (int64_t)hq_g * 130;
+    for (int r = 0; r < hq_g; ++r) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mall[w * kMergeFloatsPerWarp + 2048 + r]);
+        const float base = (M == -INFINITY) ? 0.0f : M;
+        float L = 0.0f, O = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) {
+            const float sc = exp2f(mall[w * kMergeFloatsPerWarp + 2048 + r] - base);
+            L += mall[w * kMergeFloatsPerWarp + 2048 + 16 + r] * sc;
+            O += mall[w * kMergeFloatsPerWarp + r * 128 + d] * sc;
+        }
+        if (p.splits == 1) {
+            p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / L);
+        } else {
+            if (d == 0) {
+                part[r * 130 + 0] = M;
+                part[r * 130 + 1] = L;
+            }
+            part[r * 130 + 2 + d] = O;
+        }
+    }
+    if (p.splits == 1) return;
+
+    // ---- the last split of (row, group) to finish merges all of them in order
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t ticket = atomicAdd(p.counter + ng, 1u);
+        s_last = (ticket == (uint32_t)(p.splits - 1));
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const float* pall = p.partial + ng * p.splits * (int64_t)hq_g * 130;
+    for (int r = 0; r < hq_g; ++r) {
+        float M = -INFINITY;
+        for (int sidx = 0; sidx < p.splits; ++sidx)
+            M = fmaxf(M, __ldcg(pall + ((int64_t)sidx * hq_g + r) * 130));
+        const float base = (M == -INFINITY) ? 0.0f : M;
+        float L = 0.0f, O = 0.0f;
+        for (int sidx = 0; sidx < p.splits; ++sidx) {
+            const float* ps = pall + ((int64_t)sidx * hq_g + r) * 130;
+            const float sc = exp2f(__ldcg(ps) - base);
+            L += __ldcg(ps + 1) * sc;
+            O += __ldcg(ps + 2 + d) * sc;
+        }
+        p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / L);
+    }
+    if (tid == 0) p.counter[ng] = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             cudaStream_t stream, bool pdl) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.splits, p.G, p.N);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, sparse_attn_kernel, kmap, vmap, p);
+}
+
+}  // namespace step5

@@ -1,0 +1,191 @@
+// common.cuh -- device helpers shared by the sm_103a kernels of libstep5sa.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace step5 {
+
+constexpr uint32_t kDevRange = 1u;
+constexpr uint32_t kDevTimeout = 2u;
+
+// Bounded spin for mbarrier waits: ~2^26 polls (seconds), far beyond any copy latency.
+constexpr uint32_t kSpinLimit = 1u << 26;
+
+__device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
+    atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------------------------
+// bf16 / e4m3 conversions
+// ---------------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
+
+// fp32 -> bf16 bits, round to nearest even.
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+    __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// bf16(exact a + b) for fp32 a, b whose sum is not representable in fp32: rounds the
+// exact sum once.  The fp32 sum s is off by the TwoSum residual e; the only case where
+// rounding s to bf16 differs from rounding a + b is s sitting exactly on a bf16 halfway
+// point, and there the residual's sign says which way the exact sum lies.
+__device__ __forceinline__ uint16_t bf16_of_exact_sum(float a, float b) {
+    float s = __fadd_rn(a, b);
+    float bb = __fsub_rn(s, a);
+    float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    uint32_t u = __float_as_uint(s);
+    if ((u & 0xffffu) == 0x8000u && e != 0.0f) {
+        // move s off the halfway point toward the exact value
+        bool away = (e > 0.0f) == (s > 0.0f);
+        u = away ? u + 1u : u - 1u;
+        s = __uint_as_float(u);
+    }
+    return f32_to_bf16_bits(s);
+}
+
+// NEOX pair rotation of bf16 values with bf16 cos/sin: returns bf16 bits of
+// x1*c - x2*s (first = true) or x2*c + x1*s (first = false), rounded once.
+// Products of two bf16 values are exact in fp32.
+__device__ __forceinline__ uint16_t neox_rotate(float x_self, float x_partner, float c, float s,
+                                                bool first) {
+    float p_self = __fmul_rn(x_self, c);
+    float p_part = __fmul_rn(x_partner, s);
+    return first ? bf16_of_exact_sum(p_self, -p_part) : bf16_of_exact_sum(p_self, p_part);
+}
+
+// e4m3 code of an fp32 value (round to nearest even, saturate to +-448).
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+    return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Two e4m3 codes (low byte first) -> two floats (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t two) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+    __half2 hh = *reinterpret_cast<__half2*>(&h);
+    return __half22float2(hh);
+}
+
+// Order-preserving map of a float score to a key that sorts DEScending by score:
+// smaller key = larger score.  -0 is mapped like +0.
+__device__ __forceinline__ uint32_t desc_key(float score) {
+    uint32_t u = __float_as_uint(score);
+    if (u == 0x80000000u) u = 0u;
+    uint32_t ordered = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ~ordered;
+}
+
+__device__ __forceinline__ float score_of_desc_key(uint32_t key) {
+    uint32_t ordered = ~key;
+    uint32_t u = (ordered & 0x80000000u) ? (ordered & 0x7fffffffu) : ~ordered;
+    return __uint_as_float(u);
+}
+
+// ---------------------------------------------------------------------------------
+// mbarrier / TMA (inline PTX)
+// ---------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Waits for phase `parity` of the barrier; gives up after kSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t addr = smem_u32(bar);
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_t* bar, int32_t x,
+                                            int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// ---------------------------------------------------------------------------------
+// Warp-level tensor-core helpers (bf16 m16n8k16, fp32 accumulate)
+// ---------------------------------------------------------------------------------
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                            uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------------
+
+// Waits until the grids this launch depends on have completed and flushed memory.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next grid on the stream begin launching (its pdl_wait still waits for us).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace step5

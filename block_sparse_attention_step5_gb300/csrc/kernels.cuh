@@ -1,0 +1,78 @@
+// kernels.cuh -- parameter blocks and launchers of the libstep5sa kernels.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace step5 {
+
+// ----------------------------------------------------------------- step (1)
+struct SummarizeParams {
+    const uint16_t* idx_k;   // [B][G][t_cap][64]
+    const uint16_t* idx_z;   // [B][G][t_cap][64]
+    const uint16_t* cos;     // [t_cap][rope_dims/2] or null
+    const uint16_t* sin;
+    const int32_t* region_begin;  // [B]
+    const int32_t* region_end;    // [B]
+    uint8_t* summ;           // [B][G][r_cap][64]
+    float* summ_f32;         // [B][G][r_cap][64] or null
+    uint32_t* status;
+    int G, t_cap, r_cap, max_span, rope_dims;
+};
+cudaError_t launch_summarize(const SummarizeParams& p, int B, cudaStream_t stream);
+cudaError_t launch_convert(const uint16_t* in, uint8_t* out, int64_t n, cudaStream_t stream);
+
+// ----------------------------------------------------------------- steps (2) + (3)
+constexpr int kHistBits = 12;
+constexpr int kHistBins = 1 << kHistBits;
+constexpr int kCandCap = 2048;          // candidates per (row, group) on the split path
+constexpr int kFusedMaxRegions = 16384; // regions a fused block keeps in shared memory
+constexpr int kMaxTopK = 2048;
+
+struct ScoreParams {
+    const uint16_t* idx_q;   // [N][idx_heads][64]
+    const float* w;          // [N][idx_heads]
+    const int32_t* row_seq;  // [N]
+    const int32_t* row_pos;  // [N]
+    const uint16_t* cos;     // [t_cap][rope_dims/2] or null
+    const uint16_t* sin;
+    const uint8_t* summ;     // [B][G][r_cap][64]
+    int32_t* sel_ids;        // [N][G][top_k]
+    int32_t* sel_count;      // [N][G]
+    float* sel_scores;       // [N][G][top_k] or null
+    float* scores;           // [N][G][r_cap]: caller's export or workspace (split path)
+    uint32_t* hist;          // [N][G][kHistBins]   (split path, zero between calls)
+    uint32_t* cand_count;    // [N][G]              (split path, zero between calls)
+    uint64_t* cand;          // [N][G][kCandCap]    (split path)
+    uint32_t* status;
+    int N, B, G, idx_heads, hpg, t_cap, r_cap, rope_dims, top_k;
+    int regions_per_cta;     // split path: regions scored by one block
+};
+cudaError_t launch_score_fused(const ScoreParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_score_split(const ScoreParams& p, cudaStream_t stream, bool pdl);
+
+// ----------------------------------------------------------------- step (4)
+constexpr int kAttnWarps = 4;
+constexpr int kAttnStages = 2;          // pair buffers per warp
+constexpr int kMaxSplits = 128;
+
+struct AttnParams {
+    const uint16_t* q;       // [N][Hq][128]
+    const int32_t* row_seq;
+    const int32_t* row_pos;
+    const int32_t* sel_ids;  // [N][G][top_k]
+    const int32_t* sel_count;
+    uint16_t* out;           // [N][Hq][128]
+    float* partial;          // [N][G][splits][hq_g][130]  (m, l, o[128])
+    uint32_t* counter;       // [N][G]  (zero between calls)
+    uint32_t* status;
+    int N, B, G, Hq, hq_g, t_cap, top_k;
+    int splits, entries_per_split;
+    float scale_log2;        // softmax_scale * log2(e)
+};
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             cudaStream_t stream, bool pdl);
+
+}  // namespace step5

@@ -1,0 +1,381 @@
+// step5_api.cu -- the C ABI of libstep5sa: host-side validation, workspace layout,
+// TMA descriptors and kernel launches.  Declared in include/step5_sparse_attn.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "kernels.cuh"
+#include "step5_sparse_attn.h"
+
+namespace step5 {
+namespace {
+
+__device__ uint32_t g_status_word;
+
+int32_t g_select_path = 0;  // 0 auto, 1 fused, 2 split
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Geometry check after the vLLM Step5 DSA validation (provider groups = KV groups,
+// indexer heads divisible into them, 4/8/16 query heads per KV group) plus the shapes
+// the kernels implement.
+step5_status check_geometry(const step5_geometry* g) {
+    if (g == nullptr) return STEP5_ERR_INVALID_ARGUMENT;
+    if (g->num_q_heads <= 0 || g->num_kv_groups <= 0 || g->idx_heads <= 0) return STEP5_ERR_INVALID_ARGUMENT;
+    if (g->num_kv_groups > 16) return STEP5_ERR_UNSUPPORTED;
+    if (g->idx_heads % g->num_kv_groups) return STEP5_ERR_UNSUPPORTED;
+    const int hpg = g->idx_heads / g->num_kv_groups;
+    if (hpg != 1 && hpg != 2 && hpg != 4 && hpg != 8) return STEP5_ERR_UNSUPPORTED;
+    if (g->num_q_heads % g->num_kv_groups) return STEP5_ERR_UNSUPPORTED;
+    const int hq = g->num_q_heads / g->num_kv_groups;
+    if (hq != 4 && hq != 8 && hq != 16) return STEP5_ERR_UNSUPPORTED;
+    if (g->head_dim != 128 || g->idx_dim != 64 || g->region_tokens != 8) return STEP5_ERR_UNSUPPORTED;
+    if (g->rope_dims < 0 || g->rope_dims > g->idx_dim || (g->rope_dims % 16) != 0) return STEP5_ERR_UNSUPPORTED;
+    if (g->top_k < 1 || g->top_k > kMaxTopK) return STEP5_ERR_UNSUPPORTED;
+    if (!(g->softmax_scale > 0.0f) || !isfinite(g->softmax_scale)) return STEP5_ERR_INVALID_ARGUMENT;
+    return STEP5_OK;
+}
+
+uint32_t* status_ptr() {
+    static uint32_t* ptr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        ptr[dev] = static_cast<uint32_t*>(p);
+    }
+    return ptr[dev];
+}
+
+// ------------------------------------------------------------------ workspace layout
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// How step (4) splits a row's (top_k + 1)-entry key list: enough blocks to cover the
+// GPU twice, each split a whole number of 16-token pairs for each of the 4 warps.
+void attn_splits(const step5_geometry* g, int N, int* splits_out, int* eps_out) {
+    const int emax = g->top_k + 1;
+    const int64_t items = (int64_t)N * g->num_kv_groups;
+    int64_t splits = (2 * 152 + items - 1) / items;
+    if (splits < 1) splits = 1;
+    int64_t eps = (emax + splits - 1) / splits;
+    eps = (eps + 7) / 8 * 8;
+    if (eps < 8) eps = 8;
+    splits = (emax + eps - 1) / eps;
+    if (splits > kMaxSplits) {
+        splits = kMaxSplits;
+        eps = (emax + splits - 1) / splits;
+        eps = (eps + 7) / 8 * 8;
+        splits = (emax + eps - 1) / eps;
+    }
+    *splits_out = (int)splits;
+    *eps_out = (int)eps;
+}
+
+// One workspace serves both calls.  Everything that does not depend on r_cap comes
+// first (the zero-maintained histogram and counters, then the attention partials), so
+// step (4), which does not know r_cap, finds its part at the same offsets.
+struct Layout {
+    size_t hist, cand_count, attn_counter, partial, scores, cand, end;
+};
+
+Layout layout(const step5_geometry* g, int N, int r_cap) {
+    Layout L;
+    const int G = g->num_kv_groups;
+    const size_t ng = (size_t)N * G;
+    int splits, eps;
+    attn_splits(g, N, &splits, &eps);
+    const size_t partial_bytes = splits > 1 ? ng * (size_t)splits * (g->num_q_heads / G) * 130 * 4 : 0;
+    L.hist = 0;
+    L.cand_count = align256(L.hist + ng * kHistBins * 4);
+    L.attn_counter = align256(L.cand_count + ng * 4);
+    L.partial = align256(L.attn_counter + ng * 4);
+    L.scores = align256(L.partial + partial_bytes);
+    L.cand = align256(L.scores + ng * (size_t)(r_cap > 0 ? r_cap : 0) * 4);
+    L.end = align256(L.cand + ng * kCandCap * 8);
+    return L;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D view [rows][128] bf16 of a [B][G][t_cap][128] cache; box 64 dims x 8 rows,
+// 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* base, uint64_t rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {64, 8};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct MapCache {
+    std::mutex mu;
+    const void* kptr = nullptr;
+    const void* vptr = nullptr;
+    uint64_t rows = 0;
+    CUtensorMap k, v;
+};
+MapCache g_maps;
+
+bool cache_maps(const void* kptr, const void* vptr, uint64_t rows, CUtensorMap* k, CUtensorMap* v) {
+    std::lock_guard<std::mutex> lock(g_maps.mu);
+    if (g_maps.kptr != kptr || g_maps.vptr != vptr || g_maps.rows != rows) {
+        if (!encode_cache_map(&g_maps.k, kptr, rows) || !encode_cache_map(&g_maps.v, vptr, rows)) {
+            g_maps.kptr = g_maps.vptr = nullptr;
+            return false;
+        }
+        g_maps.kptr = kptr;
+        g_maps.vptr = vptr;
+        g_maps.rows = rows;
+    }
+    *k = g_maps.k;
+    *v = g_maps.v;
+    return true;
+}
+
+bool use_pdl() { return true; }
+
+}  // namespace
+}  // namespace step5
+
+using namespace step5;
+
+extern "C" {
+
+const char* step5_status_string(step5_status s) {
+    switch (s) {
+        case STEP5_OK: return "ok";
+        case STEP5_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case STEP5_ERR_UNSUPPORTED: return "unsupported geometry";
+        case STEP5_ERR_WORKSPACE: return "workspace missing or too small";
+        case STEP5_ERR_CUDA: return "CUDA error";
+        case STEP5_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int32_t step5_set_select_path(int32_t mode) {
+    const int32_t prev = g_select_path;
+    if (mode >= 0 && mode <= 2) g_select_path = mode;
+    return prev;
+}
+
+size_t step5_workspace_bytes(const step5_geometry* geom, int32_t N, int32_t r_cap) {
+    if (check_geometry(geom) != STEP5_OK || N <= 0 || r_cap <= 0) return 0;
+    return layout(geom, N, r_cap).end;
+}
+
+step5_status step5_workspace_init(void* workspace, size_t workspace_bytes, step5_stream_t stream) {
+    if (workspace == nullptr || workspace_bytes == 0) return STEP5_ERR_INVALID_ARGUMENT;
+    if (cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream) != cudaSuccess) return STEP5_ERR_CUDA;
+    return STEP5_OK;
+}
+
+step5_status step5_device_status(uint32_t* flags_out, step5_stream_t stream) {
+    if (flags_out == nullptr) return STEP5_ERR_INVALID_ARGUMENT;
+    uint32_t* st = status_ptr();
+    if (!st) return STEP5_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, st, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess) return STEP5_ERR_CUDA;
+    if (cudaMemsetAsync(st, 0, 4, (cudaStream_t)stream) != cudaSuccess) return STEP5_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return STEP5_ERR_CUDA;
+    *flags_out = v;
+    return (v & STEP5_DEV_TIMEOUT) ? STEP5_ERR_TIMEOUT : STEP5_OK;
+}
+
+step5_status step5_convert_bf16_to_e4m3(const void* in_bf16, uint8_t* out_e4m3, int64_t n, step5_stream_t stream) {
+    if (n < 0 || (n > 0 && (in_bf16 == nullptr || out_e4m3 == nullptr))) return STEP5_ERR_INVALID_ARGUMENT;
+    if (n == 0) return STEP5_OK;
+    if (launch_convert(static_cast<const uint16_t*>(in_bf16), out_e4m3, n, (cudaStream_t)stream) != cudaSuccess)
+        return STEP5_ERR_CUDA;
+    return STEP5_OK;
+}
+
+step5_status step5_region_summarize(const step5_geometry* geom, int32_t B, int32_t t_cap, int32_t r_cap,
+                                    int32_t max_regions_per_seq, const void* idx_k_bf16, const void* idx_z_bf16,
+                                    const void* rope_cos_bf16, const void* rope_sin_bf16,
+                                    const int32_t* region_begin, const int32_t* region_end,
+                                    uint8_t* summaries_e4m3, float* summaries_f32_or_null, step5_stream_t stream) {
+    step5_status s = check_geometry(geom);
+    if (s != STEP5_OK) return s;
+    if (B <= 0 || t_cap <= 0 || r_cap <= 0 || max_regions_per_seq < 0) return STEP5_ERR_INVALID_ARGUMENT;
+    if (t_cap % geom->region_tokens) return STEP5_ERR_INVALID_ARGUMENT;
+    if (!idx_k_bf16 || !idx_z_bf16 || !region_begin || !region_end || !summaries_e4m3)
+        return STEP5_ERR_INVALID_ARGUMENT;
+    if ((rope_cos_bf16 == nullptr) != (rope_sin_bf16 == nullptr)) return STEP5_ERR_INVALID_ARGUMENT;
+    if (!aligned16(idx_k_bf16) || !aligned16(idx_z_bf16) || !aligned16(summaries_e4m3) ||
+        !aligned16(summaries_f32_or_null) || !aligned16(rope_cos_bf16) || !aligned16(rope_sin_bf16))
+        return STEP5_ERR_INVALID_ARGUMENT;
+    if ((int64_t)B * geom->num_kv_groups * t_cap > INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
+    if (max_regions_per_seq == 0) return STEP5_OK;
+    uint32_t* st = status_ptr();
+    if (!st) return STEP5_ERR_CUDA;
+    SummarizeParams p;
+    p.idx_k = static_cast<const uint16_t*>(idx_k_bf16);
+    p.idx_z = static_cast<const uint16_t*>(idx_z_bf16);
+    p.cos = static_cast<const uint16_t*>(rope_cos_bf16);
+    p.sin = static_cast<const uint16_t*>(rope_sin_bf16);
+    p.region_begin = region_begin;
+    p.region_end = region_end;
+    p.summ = summaries_e4m3;
+    p.summ_f32 = summaries_f32_or_null;
+    p.status = st;
+    p.G = geom->num_kv_groups;
+    p.t_cap = t_cap;
+    p.r_cap = r_cap;
+    p.max_span = max_regions_per_seq;
+    p.rope_dims = rope_cos_bf16 ? geom->rope_dims : 0;
+    if (launch_summarize(p, B, (cudaStream_t)stream) != cudaSuccess) return STEP5_ERR_CUDA;
+    return STEP5_OK;
+}
+
+step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
+                                    const void* idx_q_bf16, const float* w, const int32_t* row_seq,
+                                    const int32_t* row_pos, const void* rope_cos_bf16, const void* rope_sin_bf16,
+                                    const uint8_t* summaries_e4m3, int32_t* sel_ids, int32_t* sel_count,
+                                    float* scores_or_null, float* sel_scores_or_null, void* workspace,
+                                    size_t workspace_bytes, step5_stream_t stream) {
+    step5_status s = check_geometry(geom);
+    if (s != STEP5_OK) return s;
+    if (N <= 0 || B <= 0 || t_cap <= 0 || r_cap <= 0) return STEP5_ERR_INVALID_ARGUMENT;
+    if (N > 65535) return STEP5_ERR_UNSUPPORTED;
+    if (!idx_q_bf16 || !w || !row_seq || !row_pos || !summaries_e4m3 || !sel_ids || !sel_count)
+        return STEP5_ERR_INVALID_ARGUMENT;
+    if ((rope_cos_bf16 == nullptr) != (rope_sin_bf16 == nullptr)) return STEP5_ERR_INVALID_ARGUMENT;
+    if (!aligned16(summaries_e4m3) || !aligned16(idx_q_bf16)) return STEP5_ERR_INVALID_ARGUMENT;
+    const int G = geom->num_kv_groups;
+    const int hpg = geom->idx_heads / G;
+    const int P2 = [&] { int x = 1; while (x < geom->top_k) x <<= 1; return x; }();
+    const int fused_need = P2 * 8 + ((r_cap + 3) & ~3) * 4 + hpg * 64 * 4;
+    bool fused;
+    if (g_select_path == 1)
+        fused = true;
+    else if (g_select_path == 2)
+        fused = false;
+    else
+        fused = (int64_t)N * G >= 128 || r_cap <= 2048;
+    if (r_cap > kFusedMaxRegions || fused_need > 200 * 1024) fused = false;
+    const Layout L = layout(geom, N, r_cap);
+    if (!fused) {
+        if (workspace == nullptr) return STEP5_ERR_WORKSPACE;
+        if (workspace_bytes < L.end) return STEP5_ERR_WORKSPACE;
+    }
+    uint32_t* st = status_ptr();
+    if (!st) return STEP5_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    ScoreParams p;
+    p.idx_q = static_cast<const uint16_t*>(idx_q_bf16);
+    p.w = w;
+    p.row_seq = row_seq;
+    p.row_pos = row_pos;
+    p.cos = static_cast<const uint16_t*>(rope_cos_bf16);
+    p.sin = static_cast<const uint16_t*>(rope_sin_bf16);
+    p.summ = summaries_e4m3;
+    p.sel_ids = sel_ids;
+    p.sel_count = sel_count;
+    p.sel_scores = sel_scores_or_null;
+    p.scores = scores_or_null ? scores_or_null : (fused ? nullptr : reinterpret_cast<float*>(ws + L.scores));
+    p.hist = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.hist);
+    p.cand_count = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.cand_count);
+    p.cand = fused ? nullptr : reinterpret_cast<uint64_t*>(ws + L.cand);
+    p.status = st;
+    p.N = N;
+    p.B = B;
+    p.G = G;
+    p.idx_heads = geom->idx_heads;
+    p.hpg = hpg;
+    p.t_cap = t_cap;
+    p.r_cap = r_cap;
+    p.rope_dims = rope_cos_bf16 ? geom->rope_dims : 0;
+    p.top_k = geom->top_k;
+    // split path: enough blocks per (row, group) to cover the GPU about four times over
+    {
+        const int64_t want_ctas = 4 * 152;
+        int64_t per = (int64_t)N * G;
+        int64_t chunks = (want_ctas + per - 1) / per;
+        int64_t rpc = (r_cap + chunks - 1) / chunks;
+        rpc = (rpc + 255) / 256 * 256;
+        if (rpc < 256) rpc = 256;
+        p.regions_per_cta = (int)rpc;
+    }
+    cudaError_t e = fused ? launch_score_fused(p, (cudaStream_t)stream, use_pdl())
+                          : launch_score_split(p, (cudaStream_t)stream, use_pdl());
+    return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
+}
+
+step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, const void* q_bf16,
+                               const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
+                               const int32_t* row_pos, const int32_t* sel_ids, const int32_t* sel_count,
+                               void* out_bf16, void* workspace, size_t workspace_bytes, step5_stream_t stream) {
+    step5_status s = check_geometry(geom);
+    if (s != STEP5_OK) return s;
+    if (N <= 0 || B <= 0 || t_cap <= 0 || (t_cap % geom->region_tokens)) return STEP5_ERR_INVALID_ARGUMENT;
+    if (N > 65535) return STEP5_ERR_UNSUPPORTED;
+    if (!q_bf16 || !k_cache_bf16 || !v_cache_bf16 || !row_seq || !row_pos || !sel_ids || !sel_count || !out_bf16)
+        return STEP5_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q_bf16) || !aligned16(k_cache_bf16) || !aligned16(v_cache_bf16) || !aligned16(out_bf16))
+        return STEP5_ERR_INVALID_ARGUMENT;
+    const int G = geom->num_kv_groups;
+    const uint64_t rows = (uint64_t)B * G * t_cap;
+    if (rows > (uint64_t)INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
+    const int hq_g = geom->num_q_heads / G;
+
+    int splits, eps;
+    attn_splits(geom, N, &splits, &eps);
+    const Layout L = layout(geom, N, 0);
+    if (splits > 1) {
+        if (workspace == nullptr) return STEP5_ERR_WORKSPACE;
+        if (workspace_bytes < L.scores) return STEP5_ERR_WORKSPACE;
+    }
+    uint32_t* st = status_ptr();
+    if (!st) return STEP5_ERR_CUDA;
+    CUtensorMap kmap, vmap;
+    if (!cache_maps(k_cache_bf16, v_cache_bf16, rows, &kmap, &vmap)) return STEP5_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    AttnParams p;
+    p.q = static_cast<const uint16_t*>(q_bf16);
+    p.row_seq = row_seq;
+    p.row_pos = row_pos;
+    p.sel_ids = sel_ids;
+    p.sel_count = sel_count;
+    p.out = static_cast<uint16_t*>(out_bf16);
+    p.partial = splits > 1 ? reinterpret_cast<float*>(ws + L.partial) : nullptr;
+    p.counter = splits > 1 ? reinterpret_cast<uint32_t*>(ws + L.attn_counter) : nullptr;
+    p.status = st;
+    p.N = N;
+    p.B = B;
+    p.G = G;
+    p.Hq = geom->num_q_heads;
+    p.hq_g = hq_g;
+    p.t_cap = t_cap;
+    p.top_k = geom->top_k;
+    p.splits = splits;
+    p.entries_per_split = eps;
+    p.scale_log2 = geom->softmax_scale * 1.4426950408889634f;
+    cudaError_t e = launch_attention(p, kmap, vmap, (cudaStream_t)stream, use_pdl());
+    return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,178 @@
+/*
+ * step5_sparse_attn.h -- C ABI of libstep5sa.so, the GB300 (sm_103a) implementation of
+ * the Step-5 full-attention layer's sparse-indexer attention (DSA/CSA).
+ *
+ * The method is stated in "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903), in
+ * the commit that runs StepFun's CSA indexer "for contexts to 1M tokens":
+ *   (1) every completed 8-token region is summarised, per KV group, as a per-dim
+ *       softmax over z of the indexer k, rounded through bf16 to e4m3;
+ *   (2) each region is scored as sum_h relu(e4m3(q_h) . summary) * w_h per KV group;
+ *   (3) the top 512 regions by (-score, id), ascending, are kept;
+ *   (4) attention runs over those regions and the row's own region; below 512 regions
+ *       every region is read, which is the dense attention it replaces.
+ * The indexer q and k take NEOX rotation on their first 32 dims from bf16 cos/sin (same
+ * page, commit on Step-5's glue).  Geometry rules follow the vLLM Step5 model's DSA
+ * validation (`_validate_step5_dsa_parallel_geometry`): indexer provider groups equal
+ * the attention KV groups, indexer heads divide into them, and each KV group serves
+ * 4, 8 or 16 query heads.
+ *
+ * Conventions shared by every call
+ *  - All pointers named *_bf16, *_e4m3, *_f32, sel_*, row_*, region_*, out and
+ *    workspace are DEVICE pointers on the current CUDA device.  bf16 data are raw
+ *    16-bit patterns, e4m3 data are OCP FP8 E4M3 ("fn") byte codes.  Every buffer is
+ *    dense, row-major, in the layout written beside it.  The caller owns all memory;
+ *    the library allocates nothing and never synchronises `stream`: every call only
+ *    enqueues kernels on `stream` and returns.
+ *  - Arguments are checked on the host before anything is enqueued; a call that
+ *    returns anything but STEP5_OK has enqueued nothing.  Values that live in device
+ *    memory (positions, ids, ranges) are caller preconditions; the kernels check them
+ *    anyway, skip the offending item instead of touching memory out of range, and set
+ *    a bit in the device status word (step5_device_status).
+ *  - Positions: a query row at position p (0-based) sees keys 0..p.  Its own region is
+ *    o = p / region_tokens (tokens region_tokens*o .. p); its candidate regions are
+ *    0 .. o-1, so it has R(p) = p / region_tokens of them.
+ */
+#ifndef STEP5_SPARSE_ATTN_H
+#define STEP5_SPARSE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st* step5_stream_t;
+
+typedef enum {
+    STEP5_OK = 0,
+    STEP5_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, misaligned pointer     */
+    STEP5_ERR_UNSUPPORTED = 2,      /* geometry outside what the kernels implement    */
+    STEP5_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required     */
+    STEP5_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed           */
+    STEP5_ERR_TIMEOUT = 5           /* a bounded device wait gave up (device status)  */
+} step5_status;
+
+/* Layer geometry.  Supported: num_kv_groups in [1, 16]; idx_heads a multiple of
+ * num_kv_groups with idx_heads / num_kv_groups in {1, 2, 4, 8}; num_q_heads a multiple
+ * of num_kv_groups with num_q_heads / num_kv_groups in {4, 8, 16}; head_dim 128;
+ * idx_dim 64; rope_dims in {0, 16, 32, 48, 64}; region_tokens 8; 1 <= top_k <= 2048;
+ * softmax_scale finite and > 0.  Step-5: {32, 4, 128, 16, 64, 32, 8, 512, 1/sqrt(128)}. */
+typedef struct {
+    int32_t num_q_heads;    /* attention query heads of the layer (all KV groups)     */
+    int32_t num_kv_groups;  /* KV groups = indexer provider groups                    */
+    int32_t head_dim;       /* attention head dim                                     */
+    int32_t idx_heads;      /* indexer query heads; group g owns a contiguous block   */
+    int32_t idx_dim;        /* indexer proxy dim                                      */
+    int32_t rope_dims;      /* leading indexer dims rotated NEOX-style                */
+    int32_t region_tokens;  /* tokens per region                                      */
+    int32_t top_k;          /* regions kept per (row, KV group)                       */
+    float softmax_scale;    /* attention logit scale                                  */
+} step5_geometry;
+
+/* Step (1): region summaries.
+ * For every sequence b < B, KV group g and region r in [region_begin[b], region_end[b]):
+ *   kr[t][d] = bf16(NEOX-rotated idx_k at position 8r+t) for d < rope_dims, else idx_k;
+ *   s[d]     = sum_t softmax_t(idx_z[.][d]) * kr[t][d]        (fp32, t = 8r .. 8r+7)
+ *   summaries_e4m3[b][g][r][d] = e4m3(bf16(s[d]))              (round to nearest even,
+ *                                                                saturate at +-448)
+ *   summaries_f32_or_null[b][g][r][d] = s[d]                   (if not NULL)
+ * idx_k_bf16, idx_z_bf16: [B][G][t_cap][idx_dim].  rope_cos_bf16, rope_sin_bf16:
+ * [t_cap][rope_dims/2], the cosine/sine of pair i at each position; both NULL means the
+ * indexer k is already rotated.  region_begin, region_end: device int32 [B].
+ * max_regions_per_seq: host upper bound on region_end[b] - region_begin[b] (sizes the
+ * grid; regions beyond it are not summarised and set the status range bit).
+ * Preconditions: 0 <= region_begin[b] <= region_end[b], region_end[b] <= r_cap,
+ * 8 * region_end[b] <= t_cap.  t_cap must be a multiple of region_tokens.
+ * Pointers must be 16-byte aligned. */
+step5_status step5_region_summarize(const step5_geometry* geom, int32_t B, int32_t t_cap,
+                                    int32_t r_cap, int32_t max_regions_per_seq,
+                                    const void* idx_k_bf16, const void* idx_z_bf16,
+                                    const void* rope_cos_bf16, const void* rope_sin_bf16,
+                                    const int32_t* region_begin, const int32_t* region_end,
+                                    uint8_t* summaries_e4m3, float* summaries_f32_or_null,
+                                    step5_stream_t stream);
+
+/* Steps (2) and (3): index scores and top-k selection, fused.
+ * For every row n < N (sequence b = row_seq[n], position p = row_pos[n]) and KV group g,
+ * with H = idx_heads / G heads h = g*H .. g*H+H-1:
+ *   qe[h]   = e4m3(bf16(NEOX-rotated idx_q[n][h] at position p))
+ *   score_r = sum_h relu( sum_d qe[h][d] * summaries[b][g][r][d] ) * w[n][h]
+ *             (fp32; r < R(p); -0 is stored as +0)
+ *   sel_ids[n][g][0..k) = the k = min(top_k, R(p)) region ids with the smallest keys
+ *             (-score, id), in ascending key order; entries k..top_k-1 are -1.
+ *   sel_count[n][g] = k.
+ * idx_q_bf16: [N][idx_heads][idx_dim]; w: [N][idx_heads] fp32; row_seq, row_pos: [N].
+ * rope_cos/sin: [t_cap][rope_dims/2] or both NULL (idx_q already rotated); t_cap is the
+ * table length (positions must be < t_cap).  summaries_e4m3: [B][G][r_cap][idx_dim].
+ * sel_ids: [N][G][top_k]; sel_count: [N][G].
+ * scores_or_null: [N][G][r_cap] fp32, receives every score (entries past R(p) are not
+ * written).  sel_scores_or_null: [N][G][top_k] fp32, the picked scores (-inf padding).
+ * workspace: see step5_workspace_bytes / step5_workspace_init. */
+step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32_t B,
+                                    int32_t t_cap, int32_t r_cap,
+                                    const void* idx_q_bf16, const float* w,
+                                    const int32_t* row_seq, const int32_t* row_pos,
+                                    const void* rope_cos_bf16, const void* rope_sin_bf16,
+                                    const uint8_t* summaries_e4m3,
+                                    int32_t* sel_ids, int32_t* sel_count,
+                                    float* scores_or_null, float* sel_scores_or_null,
+                                    void* workspace, size_t workspace_bytes,
+                                    step5_stream_t stream);
+
+/* Step (4): attention over the picked regions plus the row's own region.
+ * For every row n, query head h of KV group g = h / (num_q_heads / G):
+ *   keys  = tokens 8r .. 8r+7 of every r in sel_ids[n][g][0 .. sel_count[n][g]),
+ *           then the own-region tokens 8o .. p (o = p / 8)
+ *   out[n][h] = softmax(softmax_scale * q[n][h] . K^T) V   (bf16 products, fp32
+ *           accumulation, rounded once to bf16)
+ * q_bf16: [N][num_q_heads][head_dim]; k_cache_bf16, v_cache_bf16: [B][G][t_cap][head_dim]
+ * (post-rotation keys); sel_ids [N][G][top_k], sel_count [N][G] as written by
+ * step5_index_score_topk (ids must be distinct candidates of the row, < o);
+ * out_bf16: [N][num_q_heads][head_dim].  Cache rows past p are never read into the
+ * result (they may hold anything).  t_cap must be a multiple of region_tokens; pointers
+ * 16-byte aligned. */
+step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
+                               int32_t t_cap, const void* q_bf16,
+                               const void* k_cache_bf16, const void* v_cache_bf16,
+                               const int32_t* row_seq, const int32_t* row_pos,
+                               const int32_t* sel_ids, const int32_t* sel_count,
+                               void* out_bf16, void* workspace, size_t workspace_bytes,
+                               step5_stream_t stream);
+
+/* Bytes of device workspace that step5_index_score_topk and step5_sparse_attn need for
+ * N rows and r_cap summary slots (one workspace serves both calls on one stream).
+ * Returns 0 for an unsupported geometry. */
+size_t step5_workspace_bytes(const step5_geometry* geom, int32_t N, int32_t r_cap);
+
+/* Zero-fills a workspace (enqueued on stream).  The workspace must be zero when a call
+ * begins; every call that completes leaves it zero again.  Zero it once after
+ * allocating it, again whenever N, the geometry or r_cap change between calls on it,
+ * and after any call whose device status reported an error. */
+step5_status step5_workspace_init(void* workspace, size_t workspace_bytes, step5_stream_t stream);
+
+/* Reads and clears the device status word of the current device: a bit mask of
+ * STEP5_DEV_* flags raised by kernels since the last read.  Synchronises `stream`. */
+#define STEP5_DEV_RANGE   1u  /* a position, id, range or sequence index out of bounds */
+#define STEP5_DEV_TIMEOUT 2u  /* a bounded wait on an in-flight copy gave up           */
+step5_status step5_device_status(uint32_t* flags_out, step5_stream_t stream);
+
+/* Selection path of step5_index_score_topk: 0 = automatic, 1 = one block per
+ * (row, group) scoring and selecting in shared memory, 2 = many blocks per
+ * (row, group) with a histogram threshold pass.  Both give identical results; this is a
+ * tuning and testing switch.  Returns the previous value. */
+int32_t step5_set_select_path(int32_t mode);
+
+/* Human-readable name of a status code (static string). */
+const char* step5_status_string(step5_status status);
+
+/* e4m3(bf16 value) for n bf16 inputs with the same device conversion the summaries use
+ * (round to nearest even, saturate at +-448); in_bf16 [n] -> out_e4m3 [n]. */
+step5_status step5_convert_bf16_to_e4m3(const void* in_bf16, uint8_t* out_e4m3, int64_t n,
+                                        step5_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* STEP5_SPARSE_ATTN_H */

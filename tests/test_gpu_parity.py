@@ -1,0 +1,285 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same
+seeded inputs.  See tests/parity.py for the comparison rules.
+
+Cases cover several tiles and ragged tails: rows with no candidate region (p < 8), a
+complete own region (p = 7 mod 8), just under / at / over 512 regions, several rows per
+sequence, both selection paths, the geometry variants the boundary accepts, degenerate
+all-equal scores (pure id order, including more tied candidates than the split path's
+candidate list holds), injected exact ties, and repeated calls on one workspace.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as S
+from parity import (check_out, check_scores, check_selection_near_ties, check_summaries,
+                    run_path, score_term_bound)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def s5():
+    import block_sparse_attention_step5_gb300 as s5
+    s5.build()
+    s5.load()
+    torch.cuda.init()
+    return s5
+
+
+def host_inputs(t):
+    out = {}
+    for k, v in t.items():
+        if v is None:
+            out[k] = None
+        elif v.dtype == torch.bfloat16:
+            out[k] = S.codes16(v)
+        else:
+            out[k] = v.cpu().numpy()
+    return out
+
+
+def oracle_chain(geom, w, h, summaries=None):
+    """Oracle steps 1-4 from scratch on host inputs h."""
+    if summaries is None:
+        summ = h["summaries"].copy()
+        summ, s64, _ = oracle.summarize_batch(h["idx_k"], h["idx_z"], h["cos"], h["sin"], w.sum_begin,
+                                              w.sum_end, w.r_cap, geom.rope_dims, summ=summ,
+                                              want_f64=True)
+    else:
+        summ, s64 = summaries, None
+    scores, _ = oracle.score_batch(h["idx_q"], h["w"], w.row_seq, w.row_pos, summ,
+                                   geom.num_kv_groups, geom.rope_dims, h["cos"], h["sin"])
+    ids, cnt, _ = oracle.select_batch(scores, w.row_pos, K=geom.top_k)
+    out, _ = oracle.attend_batch(h["q"], h["k_cache"], h["v_cache"], w.row_seq, w.row_pos, ids, cnt,
+                                 geom.softmax_scale)
+    return dict(summaries=summ, s64=s64, scores=scores, ids=ids, cnt=cnt, out=out)
+
+
+def full_check(s5, geom, w, t, path=0, chain=True):
+    """Every comparison of tests/parity.py on one workload; returns the GPU results."""
+    h = host_inputs(t)
+    g = run_path(s5, geom, w, t, path=path)
+    assert g["status"] == 0, f"device status {g['status']}"
+    G = geom.num_kv_groups
+    hpg = geom.idx_heads // G
+    # (1) summaries over the regions the step summarised
+    ref_summ, ref_s64, _ = oracle.summarize_batch(h["idx_k"], h["idx_z"], h["cos"], h["sin"],
+                                                  w.sum_begin, w.sum_end, w.r_cap, geom.rope_dims,
+                                                  summ=h["summaries"].copy(), want_f64=True)
+    for b in range(w.B):
+        r0, r1 = int(w.sum_begin[b]), int(w.sum_end[b])
+        if r1 <= r0:
+            continue
+        kreg = h["idx_k"][b, :, 8 * r0:8 * r1].reshape(G, r1 - r0, 8, 64)
+        check_summaries(g["summaries"][b, :, r0:r1], g["summ_f32"][b, :, r0:r1],
+                        ref_s64[b, :, r0:r1], kreg, geom.rope_dims if h["cos"] is not None else 0,
+                        where=f"seq {b}")
+    # (2) scores from the GPU's summaries (teacher forced)
+    tf_scores, _ = oracle.score_batch(h["idx_q"], h["w"], w.row_seq, w.row_pos, g["summaries"], G,
+                                      geom.rope_dims, h["cos"], h["sin"])
+    for n in range(w.N):
+        R = int(w.row_pos[n]) // 8
+        b = int(w.row_seq[n])
+        for gg in range(G):
+            if R == 0:
+                continue
+            bound = score_term_bound(h["idx_q"][n, gg * hpg:(gg + 1) * hpg], h["w"][n, gg * hpg:(gg + 1) * hpg],
+                                     int(w.row_pos[n]), geom.rope_dims, g["summaries"][b, gg, :R],
+                                     h["cos"], h["sin"])
+            check_scores(g["scores"][n, gg, :R], tf_scores[n, gg, :R], bound, where=f"row {n} group {gg}")
+    # (3) selection from the GPU's scores (teacher forced): exact ids in order
+    tf_ids, tf_cnt, _ = oracle.select_batch(g["scores"], w.row_pos, K=geom.top_k)
+    assert np.array_equal(tf_cnt, g["sel_count"])
+    assert np.array_equal(tf_ids, g["sel_ids"])
+    # picked scores export
+    for n in range(w.N):
+        for gg in range(G):
+            c = int(g["sel_count"][n, gg])
+            assert np.array_equal(g["sel_scores"][n, gg, :c], g["scores"][n, gg, g["sel_ids"][n, gg, :c]])
+            assert np.all(np.isneginf(g["sel_scores"][n, gg, c:]))
+    # (4) attention on the GPU's selection (teacher forced)
+    ref_out, _ = oracle.attend_batch(h["q"], h["k_cache"], h["v_cache"], w.row_seq, w.row_pos,
+                                     g["sel_ids"], g["sel_count"], geom.softmax_scale)
+    check_out(g["out"], ref_out, where="teacher-forced")
+    if chain:
+        ref = oracle_chain(geom, w, h)
+        for n in range(w.N):
+            for gg in range(G):
+                R = int(w.row_pos[n]) // 8
+                assert np.all((g["sel_ids"][n, gg, :g["sel_count"][n, gg]] >= 0) &
+                              (g["sel_ids"][n, gg, :g["sel_count"][n, gg]] < R))
+                check_selection_near_ties(g["sel_ids"][n, gg], int(g["sel_count"][n, gg]),
+                                          ref["ids"][n, gg], int(ref["cnt"][n, gg]), ref["scores"][n, gg],
+                                          where=f"row {n} group {gg}")
+        check_out(g["out"], ref["out"], where="oracle chain")
+    return g
+
+
+SMALL_POS = [0, 1, 7, 8, 9, 15, 16, 17, 129, 4095, 4096, 4097, 4103, 4104, 4600]
+
+
+@pytest.mark.parametrize("seed", [17, 41])
+@pytest.mark.parametrize("path", [1, 2])
+def test_small_cases_both_paths(s5, seed, path):
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": SMALL_POS, "B": 3}, seed=seed)
+    t = S.materialize(w, device="cuda")
+    full_check(s5, geom, w, t, path=path)
+
+
+def test_paths_agree_bit_for_bit(s5):
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [5000, 9000, 12001, 700, 3], "B": 2}, seed=17)
+    t = S.materialize(w, device="cuda")
+    a = run_path(s5, geom, w, t, path=1)
+    b = run_path(s5, geom, w, t, path=2)
+    for k in ("sel_ids", "sel_count", "sel_scores", "out"):
+        assert np.array_equal(a[k], b[k]), k
+    R = w.row_pos // 8
+    for n in range(w.N):
+        assert np.array_equal(a["scores"][n, :, :R[n]], b["scores"][n, :, :R[n]])
+
+
+@pytest.mark.parametrize("over", [
+    dict(num_q_heads=16), dict(num_q_heads=64), dict(idx_heads=4), dict(idx_heads=8),
+    dict(idx_heads=32), dict(rope_dims=0), dict(rope_dims=16), dict(rope_dims=48),
+    dict(rope_dims=64), dict(top_k=64), dict(top_k=2048), dict(num_kv_groups=2, idx_heads=16),
+    dict(num_kv_groups=8, num_q_heads=64, idx_heads=16),
+])
+def test_geometry_variants(s5, over):
+    base = s5.STEP5_GEOMETRY
+    geom = s5.Geometry.step5(**over)
+    sg = S.Geometry(num_q_heads=geom.num_q_heads, num_kv_groups=geom.num_kv_groups, head_dim=128,
+                    idx_heads=geom.idx_heads, idx_dim=64, rope_dims=geom.rope_dims, region_tokens=8,
+                    top_k=geom.top_k, softmax_scale=base.softmax_scale)
+    w = S.workload({"positions": [17, 600, 4100, 20000], "B": 2}, seed=41, geom=sg)
+    t = S.materialize(w, device="cuda")
+    for path in (1, 2):
+        full_check(s5, geom, w, t, path=path, chain=(path == 1))
+
+
+def test_no_rotation_tables(s5):
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [4200, 33], "B": 2}, seed=17)
+    t = S.materialize(w, device="cuda")
+    t["cos"] = None
+    t["sin"] = None
+    full_check(s5, geom, w, t, path=0)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_all_equal_scores_pick_ids_in_order(s5, path):
+    """w = 0 makes every score +0: the picks are regions 0..K-1 in id order.  The row
+    with 24,000 regions puts more tied keys in the threshold bin than the split path's
+    candidate list holds, which takes its exact full-scan route."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [4500, 192003, 30], "B": 3}, seed=17)
+    t = S.materialize(w, device="cuda", with_kv=True)
+    t["w"].zero_()
+    g = run_path(s5, geom, w, t, path=path)
+    assert g["status"] == 0
+    for n in range(w.N):
+        R = int(w.row_pos[n]) // 8
+        k = min(R, geom.top_k)
+        for gg in range(4):
+            assert g["sel_count"][n, gg] == k
+            assert np.array_equal(g["sel_ids"][n, gg, :k], np.arange(k))
+            assert np.all(g["scores"][n, gg, :R] == 0) and not np.signbit(g["scores"][n, gg, :R]).any()
+
+
+def test_injected_ties_order_by_id(s5):
+    """Summaries built by the oracle on the CPU, 10% of each (sequence, group)'s regions
+    overwritten with copies of others (exact score ties), uploaded; the step then only
+    scores, selects and attends."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [40000, 24000], "B": 2}, seed=41)
+    t = S.materialize(w, device="cuda")
+    h = host_inputs(t)
+    summ, _, _ = oracle.summarize_batch(h["idx_k"], h["idx_z"], h["cos"], h["sin"], w.sum_begin,
+                                        w.sum_end, w.r_cap, geom.rope_dims)
+    rng = np.random.default_rng(3)
+    for b in range(w.B):
+        R = int(w.row_pos[b]) // 8
+        for gg in range(4):
+            src = rng.integers(0, R, R // 10)
+            dst = rng.integers(0, R, R // 10)
+            summ[b, gg, dst] = summ[b, gg, src]
+    t["summaries"].copy_(torch.from_numpy(summ))
+    w.sum_end[:] = w.sum_begin
+    t["sum_end"].copy_(t["sum_begin"])
+    for path in (1, 2):
+        full_check(s5, geom, w, t, path=path)
+
+
+def test_repeat_calls_reuse_workspace(s5):
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [30000, 4100, 70], "B": 3}, seed=17)
+    t = S.materialize(w, device="cuda")
+    dev = t["q"].device
+    ws = s5.Workspace.create(geom, w.N, w.r_cap, device=dev)
+    outs = []
+    for path in (2, 2, 1, 2):
+        prev = s5.step5_set_select_path(path)
+        sel_ids = torch.empty((w.N, 4, 512), dtype=torch.int32, device=dev)
+        sel_count = torch.empty((w.N, 4), dtype=torch.int32, device=dev)
+        out = torch.empty((w.N, 32, 128), dtype=torch.bfloat16, device=dev)
+        s5.decode_step(geom, t, ws, sel_ids, sel_count, out, max_regions_per_seq=w.max_span)
+        s5.step5_set_select_path(prev)
+        torch.cuda.synchronize()
+        outs.append((sel_ids.cpu(), sel_count.cpu(), out.cpu()))
+    assert s5.step5_device_status() == 0
+    # the workspace is left zero where it must be
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert torch.equal(a, b)
+
+
+def test_dense_equivalence_on_gpu(s5):
+    """At most 512 regions: every region is picked and the output is dense causal
+    attention over tokens 0..p (torch SDPA in fp64 on the CPU)."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [4095, 2000, 8, 0], "B": 4}, seed=41)
+    t = S.materialize(w, device="cuda")
+    g = run_path(s5, geom, w, t, path=0)
+    h = host_inputs(t)
+    for n in range(w.N):
+        p, b = int(w.row_pos[n]), int(w.row_seq[n])
+        assert np.all(g["sel_count"][n] == p // 8)
+        for gg in range(4):
+            assert sorted(g["sel_ids"][n, gg, :p // 8].tolist()) == list(range(p // 8))
+            q = torch.from_numpy(oracle.bf16_values(h["q"][n, 8 * gg:8 * gg + 8]))
+            k = torch.from_numpy(oracle.bf16_values(h["k_cache"][b, gg, :p + 1]))
+            v = torch.from_numpy(oracle.bf16_values(h["v_cache"][b, gg, :p + 1]))
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                q[:, None], k[None].expand(8, -1, -1), v[None].expand(8, -1, -1),
+                scale=geom.softmax_scale)[:, 0].numpy()
+            check_out(g["out"][n, 8 * gg:8 * gg + 8], ref, where=f"dense row {n}")
+
+
+def test_cache_rows_past_position_are_ignored(s5):
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [4101, 4099], "B": 2}, seed=17)
+    t = S.materialize(w, device="cuda")
+    a = run_path(s5, geom, w, t, path=0)
+    for b, p in enumerate(w.row_pos):
+        t["k_cache"][b, :, p + 1:] = float("nan")
+        t["v_cache"][b, :, p + 1:] = float("inf")
+    bres = run_path(s5, geom, w, t, path=0)
+    assert np.array_equal(a["out"], bres["out"]) and np.array_equal(a["sel_ids"], bres["sel_ids"])
+
+
+def test_out_of_range_row_sets_status_and_touches_nothing_else(s5):
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [300, 5000], "B": 2}, seed=17)
+    t = S.materialize(w, device="cuda")
+    good = run_path(s5, geom, w, t, path=0)
+    t["row_pos"][0] = w.t_cap + 100     # violates row_pos < t_cap
+    bad = run_path(s5, geom, w, t, path=0)
+    assert bad["status"] & s5.DEV_RANGE
+    assert np.array_equal(good["out"][1], bad["out"][1])
+    assert np.array_equal(good["sel_ids"][1], bad["sel_ids"][1])
+    assert s5.step5_device_status() == 0
