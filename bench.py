@@ -1,0 +1,506 @@
+"""Benchmark of the Step-5 sparse-indexer attention step on GB300.
+
+A step is one pass of the whole path over one batch of rows: summarise the region the
+previous token completed (step 1), score every candidate region and select the top 512
+per KV group (steps 2-3), attend over the picks plus the own region (step 4).
+
+Headline workload: one decode row at 1,048,576 tokens (131,072 regions x 4 KV groups,
+e4m3 summaries, 2 GiB bf16 K/V); the 4-row 128K workload is reported beside it.  Inputs
+are seeded synthetic tensors already resident in HBM; L2 is flushed (a 256 MiB write)
+between timed steps, each step timed with CUDA events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+``--impl reference`` times the CPU oracle (the reference implementation of this path) on
+the host cores, on a bounded sample of the same workload, and prints the same line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn decode rows/sec at 128K and 1M ctx; achieved HBM GB/s vs peak"
+UNIT = "rows/s"
+FLUSH_BYTES = 256 << 20
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_hist_decode_1x1m.md")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=4, help="headline workload (2 or 4)")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_sha():
+    src = os.path.join(ROOT, "block_sparse_attention_step5_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("score_select.cu", "common.cuh", "kernels.cuh"):
+        h.update(open(os.path.join(src, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if
+    it was taken on the current source of that kernel (else None)."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != kernel_source_sha():
+        return None
+    return float(m_tr.group(1))
+
+
+def step_bytes(w, geom):
+    """Algorithmic bytes one step must move: summaries read by scoring, K/V of every
+    picked and own-region token, the rows' q / indexer q / w, the output, and step 1's
+    k/z/cos/sin of the summarised regions plus their summaries."""
+    G = geom.num_kv_groups
+    total = 0
+    score = 0
+    for n in range(w.N):
+        p = int(w.row_pos[n])
+        R = p // 8
+        k = min(R, geom.top_k)
+        own = p - 8 * R + 1
+        score += R * G * geom.idx_dim
+        total += G * (k * 8 + own) * geom.head_dim * 2 * 2
+        total += geom.num_q_heads * geom.head_dim * 2 * 2          # q in, out
+        total += geom.idx_heads * geom.idx_dim * 2 + geom.idx_heads * 4
+    span = int((w.sum_end - w.sum_begin).sum())
+    summ = span * G * (8 * geom.idx_dim * 2 * 2 + geom.idx_dim) + span * 8 * geom.rope_dims * 2
+    score_call = score + w.N * (geom.idx_heads * geom.idx_dim * 2 + geom.idx_heads * 4) \
+        + w.N * G * (geom.top_k * 4 + 4)
+    return total + score + summ, score_call
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import block_sparse_attention_step5_gb300 as s5
+    import synthetic as S
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    s5.build()
+    s5.load()
+    geom = s5.STEP5_GEOMETRY
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def measure(cfg, steps, warmup, clocks=False):
+        w = S.workload(cfg, seed=17)
+        t = S.materialize(w, device=dev)
+        N, G = w.N, geom.num_kv_groups
+        ws = s5.Workspace.create(geom, N, w.r_cap, device=dev)
+        sel_ids = torch.empty((N, G, geom.top_k), dtype=torch.int32, device=dev)
+        sel_count = torch.empty((N, G), dtype=torch.int32, device=dev)
+        out = torch.empty((N, geom.num_q_heads, geom.head_dim), dtype=torch.bfloat16, device=dev)
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream()
+        span = w.max_span
+        path = s5.step5_select_path_for(geom, N, w.r_cap)
+        launches_per_step = (1 if span > 0 else 0) + (1 if path == 1 else 3) + 1
+
+        def call_sum():
+            s5.step5_region_summarize(geom, t["idx_k"], t["idx_z"], t["cos"], t["sin"], t["sum_begin"],
+                                      t["sum_end"], t["summaries"], max_regions_per_seq=span)
+
+        def call_score():
+            s5.step5_index_score_topk(geom, t["idx_q"], t["w"], t["row_seq"], t["row_pos"], t["cos"],
+                                      t["sin"], t["summaries"], sel_ids, sel_count, ws.tensor, t_cap=w.t_cap)
+
+        def call_attn():
+            s5.step5_sparse_attn(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
+                                 sel_ids, sel_count, out, ws.tensor)
+
+        def step():
+            call_sum()
+            call_score()
+            call_attn()
+
+        # eager warm-up (sets kernel attributes, TMA descriptors), then the step and each
+        # call captured as CUDA graphs: a replay issues the whole step at once, so the
+        # device time is not bounded by the host's launch rate
+        for _ in range(warmup):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        assert s5.step5_device_status() == 0
+
+        def capture(fn):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                fn()
+            return g
+
+        g_step = capture(step)
+        g_parts = [capture(fn) for fn in (call_sum, call_score, call_attn)]
+        for _ in range(warmup):
+            flush.zero_()
+            g_step.replay()
+        torch.cuda.synchronize()
+        assert s5.step5_device_status() == 0
+
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        sampler = ClockSampler(local_rank) if clocks else None
+        if sampler:
+            sampler.__enter__()
+        barrier()
+        wall0 = time.perf_counter()
+        for i in range(steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            g_step.replay()
+            evs[i][1].record(stream)
+        barrier()
+        wall = time.perf_counter() - wall0
+        if sampler:
+            sampler.__exit__(None, None, None)
+        per_step = np.array([e[0].elapsed_time(e[1]) for e in evs])
+        assert s5.step5_device_status() == 0
+        ms = float(per_step.mean())
+        if dist is not None:
+            tt = torch.tensor([ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms = float(tt.item())
+
+        # per-call breakdown (each call its own graph, L2 flushed before each step)
+        evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        barrier()
+        for i in range(steps):
+            flush.zero_()
+            evb[i][0].record(stream)
+            for j, g in enumerate(g_parts):
+                g.replay()
+                evb[i][j + 1].record(stream)
+        barrier()
+        per_sum = np.array([e[0].elapsed_time(e[1]) for e in evb])
+        per_score = np.array([e[1].elapsed_time(e[2]) for e in evb])
+        per_attn = np.array([e[2].elapsed_time(e[3]) for e in evb])
+        bytes_step, bytes_score = step_bytes(w, geom)
+        res = dict(w=w, ms=ms, ms_min=float(per_step.min()), per_score=float(per_score.mean()),
+                   per_attn=float(per_attn.mean()), per_sum=float(per_sum.mean()), bytes_step=bytes_step,
+                   bytes_score=bytes_score, launches=launches_per_step * steps, path=path, wall=wall,
+                   clocks=sampler.summary() if sampler else None)
+
+        # end to end through the C ABI with host buffers: the rows' inputs copied in from
+        # pinned memory and the output copied back, every step
+        names = ("q", "idx_q", "w", "row_seq", "row_pos")
+        host = {k: torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True) for k in names}
+        for k in names:
+            host[k].copy_(t[k].cpu())
+        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+        d2h = out_host.numel() * out_host.element_size()
+        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        barrier()
+        for i in range(steps):
+            flush.zero_()
+            ev2[i][0].record(stream)
+            for k in names:
+                t[k].copy_(host[k], non_blocking=True)
+            step()
+            out_host.copy_(out, non_blocking=True)
+            ev2[i][1].record(stream)
+        barrier()
+        e2e_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev2]))
+        # the same with the step replayed from its CUDA graph
+        barrier()
+        for i in range(steps):
+            flush.zero_()
+            ev2[i][0].record(stream)
+            for k in names:
+                t[k].copy_(host[k], non_blocking=True)
+            g_step.replay()
+            out_host.copy_(out, non_blocking=True)
+            ev2[i][1].record(stream)
+        barrier()
+        e2e_graph_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev2]))
+        if dist is not None:
+            tt = torch.tensor([e2e_ms, e2e_graph_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms, e2e_graph_ms = float(tt[0].item()), float(tt[1].item())
+        res.update(e2e_ms=e2e_ms, e2e_graph_ms=e2e_graph_ms, h2d=h2d, d2h=d2h)
+        del t, flush
+        torch.cuda.empty_cache()
+        return res
+
+    peak, peak_kind = peaks()
+    head = measure(args.workload, args.steps, args.warmup, clocks=True)
+    w = head["w"]
+    rows = w.N * world
+    value = rows / (head["ms"] / 1e3)
+    score_gbs = head["bytes_score"] / (head["per_score"] / 1e3) / 1e9
+    step_gbs = head["bytes_step"] / (head["ms"] / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(head["ms"], 5), "ms_per_step_min": round(head["ms_min"], 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3+bf16 (fp32 accumulate)", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "rows_per_gpu": w.N, "context": int(w.row_pos.max()),
+                   "regions_per_group": int(w.row_pos.max()) // 8, "kv_groups": 4, "q_heads": 32,
+                   "idx_heads": 16, "top_k": 512, "select_path": "fused" if head["path"] == 1 else "split",
+                   "l2": "flushed between timed steps (256 MiB write, untimed)",
+                   "timing": "CUDA events around a CUDA-graph replay of the whole step",
+                   "parallelism": f"replicas x{world}"},
+        "step_hbm": {"bytes_per_step": head["bytes_step"], "achieved_gbs": round(step_gbs, 1),
+                     "peak_gbs": peak, "frac": round(step_gbs / peak, 4), "peak_kind": peak_kind},
+        "breakdown_us": {"summarize": round(head["per_sum"] * 1e3, 2),
+                         "score_select": round(head["per_score"] * 1e3, 2),
+                         "attention": round(head["per_attn"] * 1e3, 2)},
+        "roofline": {"kernel": "step5_index_score_topk (score + histogram, filter, select)",
+                     "bound": "hbm", "achieved": round(score_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(score_gbs / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "algorithmic_bytes_per_launch": head["bytes_score"],
+                     "traffic": profiled_traffic()},
+        "e2e": {"value": round(rows / (head["e2e_ms"] / 1e3), 2), "unit": UNIT,
+                "ms_per_step": round(head["e2e_ms"], 5), "h2d_bytes_per_step": head["h2d"],
+                "d2h_bytes_per_step": head["d2h"],
+                "how": "pinned host inputs copied in, the three C-ABI calls issued eagerly, output copied out",
+                "graph_value": round(rows / (head["e2e_graph_ms"] / 1e3), 2),
+                "graph_ms_per_step": round(head["e2e_graph_ms"], 5)},
+        "gpu_launches": head["launches"],
+        "clocks": head["clocks"],
+    }
+    if not args.no_secondary:
+        sec = measure(2 if args.workload == 4 else 4, max(20, args.steps // 2), args.warmup)
+        sgbs = sec["bytes_step"] / (sec["ms"] / 1e3) / 1e9
+        line["secondary"] = {"workload": sec["w"].name, "value": round(sec["w"].N * world / (sec["ms"] / 1e3), 2),
+                             "unit": UNIT, "ms_per_step": round(sec["ms"], 5),
+                             "achieved_gbs": round(sgbs, 1), "frac": round(sgbs / peak, 4),
+                             "select_path": "fused" if sec["path"] == 1 else "split",
+                             "breakdown_us": {"summarize": round(sec["per_sum"] * 1e3, 2),
+                                              "score_select": round(sec["per_score"] * 1e3, 2),
+                                              "attention": round(sec["per_attn"] * 1e3, 2)}}
+        line["gpu_launches"] += sec["launches"]
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = oracle_sample(args.workload, quarter=False)
+        line["cpu_baseline"] = cb
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- oracle arm
+
+def oracle_inputs(cfg):
+    """Host inputs of one workload for the oracle, drawn on the CPU from the same
+    generator (caches only at the rows the oracle reads)."""
+    import synthetic as S
+    w = S.workload(cfg, seed=17)
+    g = w.geom
+    G = g.num_kv_groups
+    h = {}
+    h["q"] = S.codes16(S.normal_bf16((w.N, g.num_q_heads, g.head_dim), w.seed, S.S_Q))
+    h["idx_q"] = S.codes16(S.normal_bf16((w.N, g.idx_heads, g.idx_dim), w.seed, S.S_IQ, scale=w.idx_q_scale))
+    h["w"] = S.uniform_f32((w.N, g.idx_heads), w.seed, S.S_W).numpy()
+    cos, sin = S.rope_tables(w.t_cap, g.rope_dims)
+    h["cos"], h["sin"] = S.codes16(cos), S.codes16(sin)
+    if w.random_summaries:
+        h["summaries"] = S.random_summaries(w).numpy()
+    else:
+        h["summaries"] = np.zeros((w.B, G, w.r_cap, g.idx_dim), np.uint8)
+    rows = []
+    for b in range(w.B):
+        for (r0, r1) in ((int(w.pre_begin[b]), int(w.pre_end[b])), (int(w.sum_begin[b]), int(w.sum_end[b]))):
+            if r1 > r0:
+                rows.append(((b * G + np.arange(G))[:, None] * w.t_cap + np.arange(8 * r0, 8 * r1)[None, :]).ravel())
+    rows = np.concatenate(rows) if rows else np.zeros(0, np.int64)
+    kshape = (w.B, G, w.t_cap, g.idx_dim)
+    h["idx_k"] = S.normal_bf16_rows(kshape, rows, w.seed, S.S_IK)
+    h["idx_z"] = S.normal_bf16_rows(kshape, rows, w.seed, S.S_IZ)
+    return w, h
+
+
+def oracle_kv(w, ids, cnt, rows_n):
+    import synthetic as S
+    g = w.geom
+    G = g.num_kv_groups
+    need = []
+    for i, n in enumerate(rows_n):
+        b, p = int(w.row_seq[n]), int(w.row_pos[n])
+        for gg in range(G):
+            regs = np.concatenate([ids[i, gg, :cnt[i, gg]], [p // 8]]).astype(np.int64)
+            need.append((b * G + gg) * w.t_cap + (regs[:, None] * 8 + np.arange(8)).ravel())
+    need = np.concatenate(need)
+    shape = (w.B, G, w.t_cap, g.head_dim)
+    return S.normal_bf16_rows(shape, need, w.seed, S.S_K), S.normal_bf16_rows(shape, need, w.seed, S.S_V)
+
+
+def oracle_step(w, h, groups=None, nthreads=0):
+    """The oracle's whole path for the workload's rows (optionally only some groups);
+    returns (seconds, threads used).  K/V drawing is outside the timed span."""
+    import oracle
+    g = w.geom
+    t0 = time.perf_counter()
+    summ = h["summaries"].copy()
+    _, _, th1 = oracle.summarize_batch(h["idx_k"], h["idx_z"], h["cos"], h["sin"], w.sum_begin, w.sum_end,
+                                       w.r_cap, g.rope_dims, summ=summ, nthreads=nthreads)
+    scores, th2 = oracle.score_batch(h["idx_q"], h["w"], w.row_seq, w.row_pos, summ, g.num_kv_groups,
+                                     g.rope_dims, h["cos"], h["sin"], nthreads=nthreads)
+    if groups is not None:
+        keep = np.zeros(g.num_kv_groups, bool)
+        keep[list(groups)] = True
+        scores[:, ~keep] = 0.0
+    ids, cnt, th3 = oracle.select_batch(scores, w.row_pos, K=g.top_k, nthreads=nthreads)
+    t1 = time.perf_counter()
+    kc, vc = oracle_kv(w, ids, cnt, range(w.N))
+    t2 = time.perf_counter()
+    out, th4 = oracle.attend_batch(h["q"], kc, vc, w.row_seq, w.row_pos, ids, cnt, g.softmax_scale,
+                                   nthreads=nthreads)
+    t3 = time.perf_counter()
+    return (t1 - t0) + (t3 - t2), max(th1, th2, th3, th4)
+
+
+def oracle_sample(cfg, quarter=False):
+    import oracle
+    oracle.build()
+    w, h = oracle_inputs(cfg)
+    sec, th = oracle_step(w, h)
+    return {"value": round(w.N / sec, 4), "unit": UNIT, "cores": int(th), "kind": "oracle",
+            "sample": f"one whole step of {w.name} ({w.N} row(s), all 4 KV groups) on the host cores; "
+                      f"{sec:.2f} s", "cpu_count": os.cpu_count()}
+
+
+def run_reference(args, rank, world):
+    """The oracle timed on the host cores: each step is the oracle's whole path for the
+    workload's row(s); rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w, h = oracle_inputs(args.workload)
+    for _ in range(min(args.warmup, 1)):
+        oracle_step(w, h)
+    times, th = [], 1
+    budget = 150.0
+    t_start = time.perf_counter()
+    for i in range(args.steps):
+        sec, th = oracle_step(w, h)
+        times.append(sec)
+        if time.perf_counter() - t_start > budget:
+            break
+    ms = float(np.mean(times)) * 1e3
+    value = w.N / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": len(times), "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "rows_per_gpu": w.N, "context": int(w.row_pos.max())},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": int(th), "kind": "oracle",
+                             "sample": f"{len(times)} whole oracle steps of {w.name} (the steps requested, "
+                                       f"cut at a {budget:.0f} s budget)"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

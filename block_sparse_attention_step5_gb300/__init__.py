@@ -27,7 +27,7 @@ __all__ = [
     "Step5Error", "Geometry", "STEP5_GEOMETRY", "library_path", "load",
     "step5_region_summarize", "step5_index_score_topk", "step5_sparse_attn",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
-    "step5_set_select_path", "step5_status_string", "step5_convert_bf16_to_e4m3",
+    "step5_set_select_path", "step5_select_path_for", "step5_status_string", "step5_convert_bf16_to_e4m3",
     "Workspace", "decode_step",
 ]
 
@@ -93,6 +93,7 @@ def load():
         "step5_workspace_init": (i32, [P, sz, P]),
         "step5_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32), P]),
         "step5_set_select_path": (i32, [i32]),
+        "step5_select_path_for": (i32, [G, i32, i32]),
         "step5_status_string": (ctypes.c_char_p, [i32]),
         "step5_convert_bf16_to_e4m3": (i32, [P, P, i64, P]),
     }
@@ -131,6 +132,11 @@ def step5_status_string(status: int) -> str:
 def step5_set_select_path(mode: int) -> int:
     """0 = automatic, 1 = one block per (row, group), 2 = histogram split path."""
     return load().step5_set_select_path(mode)
+
+
+def step5_select_path_for(geom, N: int, r_cap: int) -> int:
+    """1 (fused: one kernel) or 2 (split: three kernels) for this N and r_cap."""
+    return load().step5_select_path_for(ctypes.byref(Geometry.of(geom)), N, r_cap)
 
 
 def step5_workspace_bytes(geom, N: int, r_cap: int) -> int:

@@ -31,7 +31,7 @@ constexpr int kPairBytes = 4 * kRegionBytes;          // K (2 regions) + V (2 re
 constexpr int kStageBytes = kAttnWarps * kAttnStages * kPairBytes;
 constexpr int kMergeFloatsPerWarp = 16 * 128 + 32;    // O[16][128], m[16], l[16]
 constexpr size_t kSmemBytes = kStageBytes + kAttnWarps * kAttnStages * 8 + 1024;
-static_assert(kAttnWarps * kMergeFloatsPerWarp * 4 <= kStageBytes, "merge area must fit");
+static_assert((kAttnWarps * kMergeFloatsPerWarp + 2 * 16 * 130) * 4 <= kStageBytes, "merge area must fit");
 
 // Shared-memory byte offset of (token row t, 16-byte chunk c16 of the 256-byte row) in a
 // region tile written by two 64-dim TMA boxes with 128-byte swizzle.
@@ -297,9 +297,10 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     }
     __syncthreads();
 
+    // this block's state: merge of its warps, kept in shared memory (rows < hq_g)
+    float* mine = reinterpret_cast<float*>(smem) + kAttnWarps * kMergeFloatsPerWarp;
     const float* mall = reinterpret_cast<const float*>(smem);
     const int d = tid;  // 128 threads = 128 dims
-    float* part = p.partial + (ng * p.splits + split) * (int64_t)hq_g * 130;
     for (int r = 0; r < hq_g; ++r) {
         float M = -INFINITY;
 #pragma unroll
@@ -316,33 +317,89 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
             p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / L);
         } else {
             if (d == 0) {
-                part[r * 130 + 0] = M;
-                part[r * 130 + 1] = L;
+                mine[r * 130 + 0] = M;
+                mine[r * 130 + 1] = L;
             }
-            part[r * 130 + 2 + d] = O;
+            mine[r * 130 + 2 + d] = O;
         }
     }
     if (p.splits == 1) return;
 
-    // ---- the last split of (row, group) to finish merges all of them in order
+    // ---- the cluster's blocks (splits of one row and group) merge on chip: block 0 of
+    // the cluster reads the others' states through distributed shared memory, in rank
+    // order
+    const int C = p.cluster;
+    float* cmerged = mine + 16 * 130;  // block 0's merged state
+    if (C > 1) {
+        cluster_sync();
+        if (cluster_ctarank() == 0) {
+            const uint32_t mine_addr = smem_u32(mine);
+            for (int r = 0; r < hq_g; ++r) {
+                float mr[kMaxCluster], lr[kMaxCluster], orr[kMaxCluster];
+                float M = -INFINITY;
+                for (int c = 0; c < C; ++c) {
+                    const uint32_t a = map_cluster(mine_addr + (uint32_t)(r * 130) * 4u, (uint32_t)c);
+                    mr[c] = ld_cluster_f32(a);
+                    lr[c] = ld_cluster_f32(a + 4);
+                    orr[c] = ld_cluster_f32(a + (uint32_t)(2 + d) * 4u);
+                    M = fmaxf(M, mr[c]);
+                }
+                const float base = (M == -INFINITY) ? 0.0f : M;
+                float L = 0.0f, O = 0.0f;
+                for (int c = 0; c < C; ++c) {
+                    const float sc = exp2f(mr[c] - base);
+                    L += lr[c] * sc;
+                    O += orr[c] * sc;
+                }
+                if (d == 0) {
+                    cmerged[r * 130 + 0] = M;
+                    cmerged[r * 130 + 1] = L;
+                }
+                cmerged[r * 130 + 2 + d] = O;
+            }
+        }
+        cluster_sync();  // peers keep their shared memory until block 0 has read it
+        if (cluster_ctarank() != 0) return;
+    } else {
+        cmerged = mine;
+    }
+    __syncthreads();
+
+    const int nclusters = p.splits / C;
+    const int cid = split / C;
+    if (nclusters == 1) {
+        for (int r = 0; r < hq_g; ++r)
+            p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] =
+                f32_to_bf16_bits(cmerged[r * 130 + 2 + d] / cmerged[r * 130 + 1]);
+        return;
+    }
+    float* part = p.partial + (ng * nclusters + cid) * (int64_t)hq_g * 130;
+    for (int r = 0; r < hq_g; ++r) {
+        if (d == 0) {
+            part[r * 130 + 0] = cmerged[r * 130 + 0];
+            part[r * 130 + 1] = cmerged[r * 130 + 1];
+        }
+        part[r * 130 + 2 + d] = cmerged[r * 130 + 2 + d];
+    }
+
+    // ---- the cluster leader that finishes last merges every cluster's state, in order
     __threadfence();
     __syncthreads();
     if (tid == 0) {
         const uint32_t ticket = atomicAdd(p.counter + ng, 1u);
-        s_last = (ticket == (uint32_t)(p.splits - 1));
+        s_last = (ticket == (uint32_t)(nclusters - 1));
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    const float* pall = p.partial + ng * p.splits * (int64_t)hq_g * 130;
+    const float* pall = p.partial + ng * nclusters * (int64_t)hq_g * 130;
     for (int r = 0; r < hq_g; ++r) {
         float M = -INFINITY;
-        for (int sidx = 0; sidx < p.splits; ++sidx)
-            M = fmaxf(M, __ldcg(pall + ((int64_t)sidx * hq_g + r) * 130));
+        for (int c = 0; c < nclusters; ++c) M = fmaxf(M, __ldcg(pall + ((int64_t)c * hq_g + r) * 130));
         const float base = (M == -INFINITY) ? 0.0f : M;
         float L = 0.0f, O = 0.0f;
-        for (int sidx = 0; sidx < p.splits; ++sidx) {
-            const float* ps = pall + ((int64_t)sidx * hq_g + r) * 130;
+        for (int c = 0; c < nclusters; ++c) {
+            const float* ps = pall + ((int64_t)c * hq_g + r) * 130;
             const float sc = exp2f(__ldcg(ps) - base);
             L += __ldcg(ps + 1) * sc;
             O += __ldcg(ps + 2 + d) * sc;
@@ -368,11 +425,20 @@ cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)p.cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, sparse_attn_kernel, kmap, vmap, p);
 }
 

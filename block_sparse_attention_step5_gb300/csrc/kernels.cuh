@@ -57,6 +57,7 @@ cudaError_t launch_score_split(const ScoreParams& p, cudaStream_t stream, bool p
 constexpr int kAttnWarps = 4;
 constexpr int kAttnStages = 2;          // pair buffers per warp
 constexpr int kMaxSplits = 128;
+constexpr int kMaxCluster = 8;          // portable cluster size
 
 struct AttnParams {
     const uint16_t* q;       // [N][Hq][128]
@@ -65,11 +66,11 @@ struct AttnParams {
     const int32_t* sel_ids;  // [N][G][top_k]
     const int32_t* sel_count;
     uint16_t* out;           // [N][Hq][128]
-    float* partial;          // [N][G][splits][hq_g][130]  (m, l, o[128])
+    float* partial;          // [N][G][splits / cluster][hq_g][130]  (m, l, o[128])
     uint32_t* counter;       // [N][G]  (zero between calls)
     uint32_t* status;
     int N, B, G, Hq, hq_g, t_cap, top_k;
-    int splits, entries_per_split;
+    int splits, entries_per_split, cluster;
     float scale_log2;        // softmax_scale * log2(e)
 };
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,

@@ -313,9 +313,10 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
 // ----------------------------------------------------------------- split path
 
 constexpr int kSplitThreads = 256;
+constexpr int kSplitRegions = 512;  // regions scored by one block of the split path
 
 template <int HPG>
-__global__ void __launch_bounds__(kSplitThreads) score_hist_kernel(ScoreParams p) {
+__global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(ScoreParams p) {
     __shared__ uint32_t s_hist[kHistBins];
     __shared__ float s_q[HPG * 64];
     const int g = blockIdx.y, n = blockIdx.z;
@@ -326,33 +327,33 @@ __global__ void __launch_bounds__(kSplitThreads) score_hist_kernel(ScoreParams p
         if (blockIdx.x == 0 && threadIdx.x == 0) raise_status(p.status, kDevRange);
         return;
     }
-    const int c0 = blockIdx.x * p.regions_per_cta;
-    const int c1 = min(R, c0 + p.regions_per_cta);
+    const int c0 = blockIdx.x * kSplitRegions;
+    const int c1 = min(R, c0 + kSplitRegions);
     if (c0 >= c1) return;
+    // the block's summaries are requested before anything else (they do not depend on
+    // the query): 8 regions of 16 bytes per thread in flight
+    const int qd = threadIdx.x & 3;
+    const int slot = threadIdx.x >> 2;
+    const uint4* base = reinterpret_cast<const uint4*>(p.summ + ((int64_t)b * p.G + g) * p.r_cap * 64);
+    constexpr int U = kSplitRegions / 64;
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int r = c0 + u * 64 + slot;
+        v[u] = (r < c1) ? __ldg(base + (int64_t)r * 4 + qd) : make_uint4(0, 0, 0, 0);
+    }
     for (int i = threadIdx.x; i < kHistBins; i += kSplitThreads) s_hist[i] = 0;
     QFrag<HPG> f;
     load_qfrag<HPG>(p, n, g, pos, s_q, f);  // has a __syncthreads
 
-    const int qd = threadIdx.x & 3;
-    const int slot = threadIdx.x >> 2;
-    const uint4* base = reinterpret_cast<const uint4*>(p.summ + ((int64_t)b * p.G + g) * p.r_cap * 64);
     float* scores = p.scores + ((int64_t)n * p.G + g) * p.r_cap;
-    constexpr int U = 4;
-    for (int r0 = c0; r0 < c1; r0 += 64 * U) {
-        uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int r = r0 + u * 64 + slot;
-            v[u] = (r < c1) ? __ldg(base + (int64_t)r * 4 + qd) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int r = r0 + u * 64 + slot;
-            const float sc = score_from_vec<HPG>(f, v[u]);
-            if (qd == 0 && r < c1) {
-                scores[r] = sc;
-                atomicAdd(&s_hist[desc_key(sc) >> (32 - kHistBits)], 1u);
-            }
+    for (int u = 0; u < U; ++u) {
+        const int r = c0 + u * 64 + slot;
+        const float sc = score_from_vec<HPG>(f, v[u]);
+        if (qd == 0 && r < c1) {
+            scores[r] = sc;
+            atomicAdd(&s_hist[desc_key(sc) >> (32 - kHistBits)], 1u);
         }
     }
     __syncthreads();
@@ -444,6 +445,7 @@ constexpr int kFinalThreads = 512;
 __global__ void __launch_bounds__(kFinalThreads) final_select_kernel(ScoreParams p, int P2, int /*unused*/) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint64_t* s_sel = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* s_cand = s_sel + P2;  // kCandCap
     __shared__ TopkSmem ts;
     const int g = blockIdx.x, n = blockIdx.y;
     pdl_wait();
@@ -454,7 +456,10 @@ __global__ void __launch_bounds__(kFinalThreads) final_select_kernel(ScoreParams
     const int c = (int)p.cand_count[ng];
     int take;
     if (c <= kCandCap) {
-        take = block_topk<kFinalThreads>(CandKeys{p.cand + ng * kCandCap}, c, p.top_k, P2, s_sel, ts);
+        const uint64_t* cand = p.cand + ng * kCandCap;
+        for (int i = threadIdx.x; i < c; i += kFinalThreads) s_cand[i] = __ldcg(cand + i);
+        __syncthreads();
+        take = block_topk<kFinalThreads>(CandKeys{s_cand}, c, p.top_k, P2, s_sel, ts);
     } else {
         take = block_topk<kFinalThreads>(ScoreKeys{p.scores + ng * p.r_cap}, R, p.top_k, P2, s_sel, ts);
     }
@@ -519,14 +524,15 @@ cudaError_t fused_for(const ScoreParams& p, cudaStream_t stream, bool pdl) {
 
 template <int HPG>
 cudaError_t split_for(const ScoreParams& p, cudaStream_t stream, bool pdl) {
-    const int chunks = (p.r_cap + p.regions_per_cta - 1) / p.regions_per_cta;
+    const int chunks = (p.r_cap + kSplitRegions - 1) / kSplitRegions;
     cudaError_t e = launch_ex(score_hist_kernel<HPG>, dim3(chunks, p.G, p.N), dim3(kSplitThreads), 0,
                               stream, pdl, p);
     if (e != cudaSuccess) return e;
-    e = launch_ex(filter_kernel, dim3(chunks, p.G, p.N), dim3(kSplitThreads), 0, stream, true, p);
+    const int fchunks = (p.r_cap + p.regions_per_cta - 1) / p.regions_per_cta;
+    e = launch_ex(filter_kernel, dim3(fchunks, p.G, p.N), dim3(kSplitThreads), 0, stream, true, p);
     if (e != cudaSuccess) return e;
     const int P2 = pow2_at_least(p.top_k);
-    const size_t smem = (size_t)P2 * 8;
+    const size_t smem = (size_t)P2 * 8 + (size_t)kCandCap * 8;
     e = cudaFuncSetAttribute(final_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_ex2(final_select_kernel, dim3(p.G, p.N), dim3(kFinalThreads), smem, stream, true, p,

@@ -56,24 +56,29 @@ uint32_t* status_ptr() {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // How step (4) splits a row's (top_k + 1)-entry key list: enough blocks to cover the
-// GPU twice, each split a whole number of 16-token pairs for each of the 4 warps.
-void attn_splits(const step5_geometry* g, int N, int* splits_out, int* eps_out) {
+// GPU about twice, each split a whole number of 16-token pairs for each of the 4 warps;
+// the splits of one (row, group) are grouped into clusters of up to 8 blocks that merge
+// on chip, so only one partial state per cluster goes through global memory.
+void attn_splits(const step5_geometry* g, int N, int* splits_out, int* eps_out, int* cluster_out) {
     const int emax = g->top_k + 1;
     const int64_t items = (int64_t)N * g->num_kv_groups;
+    auto eps_for = [&](int64_t splits) {
+        int64_t e = (emax + splits - 1) / splits;
+        e = (e + 7) / 8 * 8;
+        return e < 8 ? (int64_t)8 : e;
+    };
     int64_t splits = (2 * 152 + items - 1) / items;
     if (splits < 1) splits = 1;
-    int64_t eps = (emax + splits - 1) / splits;
-    eps = (eps + 7) / 8 * 8;
-    if (eps < 8) eps = 8;
+    int64_t eps = eps_for(splits);
     splits = (emax + eps - 1) / eps;
-    if (splits > kMaxSplits) {
-        splits = kMaxSplits;
-        eps = (emax + splits - 1) / splits;
-        eps = (eps + 7) / 8 * 8;
-        splits = (emax + eps - 1) / eps;
-    }
+    int64_t cluster = 1;
+    while (cluster * 2 <= kMaxCluster && cluster * 2 <= splits) cluster *= 2;
+    splits = (splits + cluster - 1) / cluster * cluster;
+    if (splits > kMaxSplits) splits = kMaxSplits / cluster * cluster;
+    eps = eps_for(splits);
     *splits_out = (int)splits;
     *eps_out = (int)eps;
+    *cluster_out = (int)cluster;
 }
 
 // One workspace serves both calls.  Everything that does not depend on r_cap comes
@@ -87,9 +92,9 @@ Layout layout(const step5_geometry* g, int N, int r_cap) {
     Layout L;
     const int G = g->num_kv_groups;
     const size_t ng = (size_t)N * G;
-    int splits, eps;
-    attn_splits(g, N, &splits, &eps);
-    const size_t partial_bytes = splits > 1 ? ng * (size_t)splits * (g->num_q_heads / G) * 130 * 4 : 0;
+    int splits, eps, cluster;
+    attn_splits(g, N, &splits, &eps, &cluster);
+    const size_t partial_bytes = splits > cluster ? ng * (size_t)(splits / cluster) * (g->num_q_heads / G) * 130 * 4 : 0;
     L.hist = 0;
     L.cand_count = align256(L.hist + ng * kHistBins * 4);
     L.attn_counter = align256(L.cand_count + ng * 4);
@@ -157,6 +162,25 @@ bool cache_maps(const void* kptr, const void* vptr, uint64_t rows, CUtensorMap* 
 
 bool use_pdl() { return true; }
 
+// Fused (one block per (row, group), keys in shared memory) when there are many rows or
+// few regions; the histogram split path when a few rows have many regions.
+bool choose_fused(const step5_geometry* geom, int N, int r_cap) {
+    const int G = geom->num_kv_groups;
+    const int hpg = geom->idx_heads / G;
+    int P2 = 1;
+    while (P2 < geom->top_k) P2 <<= 1;
+    const int fused_need = P2 * 8 + ((r_cap + 3) & ~3) * 4 + hpg * 64 * 4;
+    bool fused;
+    if (g_select_path == 1)
+        fused = true;
+    else if (g_select_path == 2)
+        fused = false;
+    else
+        fused = (int64_t)N * G >= 128 || r_cap <= 2048;
+    if (r_cap > kFusedMaxRegions || fused_need > 200 * 1024) fused = false;
+    return fused;
+}
+
 }  // namespace
 }  // namespace step5
 
@@ -180,6 +204,11 @@ int32_t step5_set_select_path(int32_t mode) {
     const int32_t prev = g_select_path;
     if (mode >= 0 && mode <= 2) g_select_path = mode;
     return prev;
+}
+
+int32_t step5_select_path_for(const step5_geometry* geom, int32_t N, int32_t r_cap) {
+    if (check_geometry(geom) != STEP5_OK || N <= 0 || r_cap <= 0) return 0;
+    return choose_fused(geom, N, r_cap) ? 1 : 2;
 }
 
 size_t step5_workspace_bytes(const step5_geometry* geom, int32_t N, int32_t r_cap) {
@@ -267,16 +296,7 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     if (!aligned16(summaries_e4m3) || !aligned16(idx_q_bf16)) return STEP5_ERR_INVALID_ARGUMENT;
     const int G = geom->num_kv_groups;
     const int hpg = geom->idx_heads / G;
-    const int P2 = [&] { int x = 1; while (x < geom->top_k) x <<= 1; return x; }();
-    const int fused_need = P2 * 8 + ((r_cap + 3) & ~3) * 4 + hpg * 64 * 4;
-    bool fused;
-    if (g_select_path == 1)
-        fused = true;
-    else if (g_select_path == 2)
-        fused = false;
-    else
-        fused = (int64_t)N * G >= 128 || r_cap <= 2048;
-    if (r_cap > kFusedMaxRegions || fused_need > 200 * 1024) fused = false;
+    const bool fused = choose_fused(geom, N, r_cap);
     const Layout L = layout(geom, N, r_cap);
     if (!fused) {
         if (workspace == nullptr) return STEP5_ERR_WORKSPACE;
@@ -342,10 +362,10 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
     if (rows > (uint64_t)INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
     const int hq_g = geom->num_q_heads / G;
 
-    int splits, eps;
-    attn_splits(geom, N, &splits, &eps);
+    int splits, eps, cluster;
+    attn_splits(geom, N, &splits, &eps, &cluster);
     const Layout L = layout(geom, N, 0);
-    if (splits > 1) {
+    if (splits > cluster) {
         if (workspace == nullptr) return STEP5_ERR_WORKSPACE;
         if (workspace_bytes < L.scores) return STEP5_ERR_WORKSPACE;
     }
@@ -361,8 +381,8 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
     p.sel_ids = sel_ids;
     p.sel_count = sel_count;
     p.out = static_cast<uint16_t*>(out_bf16);
-    p.partial = splits > 1 ? reinterpret_cast<float*>(ws + L.partial) : nullptr;
-    p.counter = splits > 1 ? reinterpret_cast<uint32_t*>(ws + L.attn_counter) : nullptr;
+    p.partial = splits > cluster ? reinterpret_cast<float*>(ws + L.partial) : nullptr;
+    p.counter = splits > cluster ? reinterpret_cast<uint32_t*>(ws + L.attn_counter) : nullptr;
     p.status = st;
     p.N = N;
     p.B = B;
@@ -373,6 +393,7 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
     p.top_k = geom->top_k;
     p.splits = splits;
     p.entries_per_split = eps;
+    p.cluster = cluster;
     p.scale_log2 = geom->softmax_scale * 1.4426950408889634f;
     cudaError_t e = launch_attention(p, kmap, vmap, (cudaStream_t)stream, use_pdl());
     return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;

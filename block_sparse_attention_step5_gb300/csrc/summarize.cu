@@ -61,28 +61,38 @@ __global__ void __launch_bounds__(256) summarize_kernel(SummarizeParams p) {
         }
     }
 
+    // every load of the region is issued before any arithmetic
+    uint4 kv[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) kv[t] = __ldg(kz_k + ((row0 + t) * 64 + d0) / 8);
+    uint4 pv[8], cv[8], sv[8];
+    if (rotated) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int64_t tabrow = (int64_t)(r * 8 + t) * half + pair0;
+            pv[t] = __ldg(kz_k + ((row0 + t) * 64 + partner) / 8);
+            cv[t] = __ldg(reinterpret_cast<const uint4*>(p.cos + tabrow));
+            sv[t] = __ldg(reinterpret_cast<const uint4*>(p.sin + tabrow));
+        }
+    }
+
     // pass 2: weights and weighted sum (fp32, tokens in order)
     float den[8], num[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) den[u] = num[u] = 0.0f;
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-        const uint4 kv = __ldg(kz_k + ((row0 + t) * 64 + d0) / 8);
         float kr[8];
-        const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+        const uint32_t kw[4] = {kv[t].x, kv[t].y, kv[t].z, kv[t].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             kr[2 * q] = bf16_lo(kw[q]);
             kr[2 * q + 1] = bf16_hi(kw[q]);
         }
         if (rotated) {
-            const uint4 pv = __ldg(kz_k + ((row0 + t) * 64 + partner) / 8);
-            const int64_t tabrow = (int64_t)(r * 8 + t) * half + pair0;
-            const uint4 cv = __ldg(reinterpret_cast<const uint4*>(p.cos + tabrow));
-            const uint4 sv = __ldg(reinterpret_cast<const uint4*>(p.sin + tabrow));
-            const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
-            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-            const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+            const uint32_t pw[4] = {pv[t].x, pv[t].y, pv[t].z, pv[t].w};
+            const uint32_t cw[4] = {cv[t].x, cv[t].y, cv[t].z, cv[t].w};
+            const uint32_t sw[4] = {sv[t].x, sv[t].y, sv[t].z, sv[t].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 kr[2 * q] = bf16_to_f32(neox_rotate(kr[2 * q], bf16_lo(pw[q]), bf16_lo(cw[q]),

@@ -164,6 +164,11 @@ step5_status step5_device_status(uint32_t* flags_out, step5_stream_t stream);
  * tuning and testing switch.  Returns the previous value. */
 int32_t step5_set_select_path(int32_t mode);
 
+/* The selection path step5_index_score_topk takes for this geometry, N and r_cap under
+ * the current step5_set_select_path setting: 1 (fused, one kernel) or 2 (split, three
+ * kernels: score + histogram, filter, final select); 0 for an unsupported geometry. */
+int32_t step5_select_path_for(const step5_geometry* geom, int32_t N, int32_t r_cap);
+
 /* Human-readable name of a status code (static string). */
 const char* step5_status_string(step5_status status);
 

@@ -15,8 +15,8 @@ import torch
 
 import oracle
 import synthetic as S
-from parity import (check_out, check_scores, check_selection_near_ties, check_summaries,
-                    run_path, score_term_bound)
+from parity import (check_out, check_scores, check_selection_chain, check_selection_near_ties,
+                    check_summaries, run_path, score_term_bound)
 
 pytestmark = pytest.mark.gpu
 
@@ -95,6 +95,12 @@ def full_check(s5, geom, w, t, path=0, chain=True):
     tf_ids, tf_cnt, _ = oracle.select_batch(g["scores"], w.row_pos, K=geom.top_k)
     assert np.array_equal(tf_cnt, g["sel_count"])
     assert np.array_equal(tf_ids, g["sel_ids"])
+    # selection by the oracle fed the GPU's summaries (its own fp64 scores): near-ties only
+    gs_ids, gs_cnt, _ = oracle.select_batch(tf_scores, w.row_pos, K=geom.top_k)
+    for n in range(w.N):
+        for gg in range(G):
+            check_selection_near_ties(g["sel_ids"][n, gg], int(g["sel_count"][n, gg]), gs_ids[n, gg],
+                                      int(gs_cnt[n, gg]), tf_scores[n, gg], where=f"row {n} group {gg}")
     # picked scores export
     for n in range(w.N):
         for gg in range(G):
@@ -112,9 +118,11 @@ def full_check(s5, geom, w, t, path=0, chain=True):
                 R = int(w.row_pos[n]) // 8
                 assert np.all((g["sel_ids"][n, gg, :g["sel_count"][n, gg]] >= 0) &
                               (g["sel_ids"][n, gg, :g["sel_count"][n, gg]] < R))
-                check_selection_near_ties(g["sel_ids"][n, gg], int(g["sel_count"][n, gg]),
-                                          ref["ids"][n, gg], int(ref["cnt"][n, gg]), ref["scores"][n, gg],
-                                          where=f"row {n} group {gg}")
+                b = int(w.row_seq[n])
+                flipped = (g["summaries"][b, gg, :R] != ref["summaries"][b, gg, :R]).any(axis=-1)
+                check_selection_chain(g["sel_ids"][n, gg], int(g["sel_count"][n, gg]), ref["ids"][n, gg],
+                                      int(ref["cnt"][n, gg]), ref["scores"][n, gg, :R], flipped,
+                                      where=f"row {n} group {gg}")
         check_out(g["out"], ref["out"], where="oracle chain")
     return g
 
