@@ -7,18 +7,19 @@
 // order ("one simdgroup walking every key alone left decode waiting on loads").
 //
 // Design (sm_103a):
-//  * work item = (row, KV group, split); a split is a run of entries of the row's key
-//    list (picked regions in selection order, then the own region); 4 warps per block,
-//    each warp takes pairs of entries (16 tokens) with its own 2-stage pipeline.
+//  * one thread-block cluster per (row, KV group): its C blocks (1..16) split the row's
+//    key list (picked regions in selection order, then the own region) into runs of
+//    whole 16-token pairs; 8 warps per block, each warp with its own 2-stage pipeline.
 //  * a region is a contiguous 2 KB tile of the [B][G][t_cap][128] cache; it is fetched
 //    with two 2-D TMA boxes (64 dims x 8 rows each) into 128-byte-swizzled shared
 //    memory, so the ldmatrix reads below hit 8 distinct bank groups.
 //  * S = Q K^T and O += P V run on bf16 mma.sync (m16n8k16, fp32 accumulate) with the
 //    group's query heads as the 16-row left operand (4, 8 or 16 heads; unused rows are
 //    zero); P is rounded to bf16 for the PV product, the softmax state is fp32.
-//  * the 4 warps merge through shared memory; splits of one (row, group) write fp32
-//    partial states and the block that finishes last (atomic ticket, no waiting) merges
-//    them in split order, so the result does not depend on timing.
+//  * the warps merge through shared memory; every block then pushes its state into a
+//    slot of block 0's shared memory with remote (distributed shared memory) stores,
+//    one cluster barrier publishes them, and block 0 merges the slots in rank order, so
+//    the result does not depend on timing and nothing goes through global memory.
 #include "kernels.cuh"
 
 namespace step5 {
@@ -30,8 +31,14 @@ constexpr int kRegionBytes = 2048;                    // 8 tokens x 128 dims x b
 constexpr int kPairBytes = 4 * kRegionBytes;          // K (2 regions) + V (2 regions)
 constexpr int kStageBytes = kAttnWarps * kAttnStages * kPairBytes;
 constexpr int kMergeFloatsPerWarp = 16 * 128 + 32;    // O[16][128], m[16], l[16]
-constexpr size_t kSmemBytes = kStageBytes + kAttnWarps * kAttnStages * 8 + 1024;
-static_assert((kAttnWarps * kMergeFloatsPerWarp + 2 * 16 * 130) * 4 <= kStageBytes, "merge area must fit");
+constexpr int kBarBytes = kAttnWarps * kAttnStages * 8;
+constexpr int kSlotFloats = 130;                      // m, l, o[128] of one head row
+static_assert(kAttnWarps * kMergeFloatsPerWarp * 4 <= kStageBytes, "warp merge area must fit");
+
+// Dynamic shared memory: [stage area | barriers | push slots C x hq_g x 130 floats]
+size_t attn_smem_bytes(int cluster, int hq_g) {
+    return 1024 + kStageBytes + kBarBytes + (cluster > 1 ? (size_t)cluster * hq_g * kSlotFloats * 4 : 0);
+}
 
 // Shared-memory byte offset of (token row t, 16-byte chunk c16 of the 256-byte row) in a
 // region tile written by two 64-dim TMA boxes with 128-byte swizzle.
@@ -40,28 +47,44 @@ __device__ __forceinline__ uint32_t tile_off(int t, int c16) {
     return (uint32_t)(half * 1024 + t * 128 + ((c ^ t) << 4));
 }
 
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageBytes);
-    __shared__ int s_last;
+    float* slots = reinterpret_cast<float*>(smem + kStageBytes + kBarBytes);  // [C][hq_g][130]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, g = blockIdx.y, n = blockIdx.z;
     const int64_t ng = (int64_t)n * p.G + g;
     const int hq_g = p.hq_g;
+    const int C = p.cluster;
 
     if (tid == 0) {
         prefetch_tmap(&kmap);
         prefetch_tmap(&vmap);
     }
+    STEP5_STAMP(4, 0);
     pdl_wait();
+    pdl_launch_dependents();
+    STEP5_STAMP(4, 1);
 
+    // the row's position, pick count and this warp's first pair ids, in one round trip
+    const int32_t* ids = p.sel_ids + ng * p.top_k;
+    const int e0 = split * p.entries_per_split;
+    const int e_first = e0 + 2 * warp;
+    const int32_t id_pref0 = e_first < p.top_k ? __ldg(ids + e_first) : -1;
+    const int32_t id_pref1 = e_first + 1 < p.top_k ? __ldg(ids + e_first + 1) : -1;
     const int b = p.row_seq[n];
     const int pos = p.row_pos[n];
+    int cnt = p.sel_count[ng];
     if (b < 0 || b >= p.B || pos < 0 || pos >= p.t_cap) {
+        // the same for every block of the cluster: all leave before any cluster barrier
         if (split == 0) {
             if (tid == 0) raise_status(p.status, kDevRange);
             for (int i = tid; i < hq_g * 128; i += kThreads)
@@ -69,7 +92,6 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         }
         return;
     }
-    int cnt = p.sel_count[ng];
     if (cnt < 0 || cnt > p.top_k) {
         if (split == 0 && tid == 0) raise_status(p.status, kDevRange);
         cnt = cnt < 0 ? 0 : p.top_k;
@@ -77,11 +99,9 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     const int own = pos >> 3;
     const int own_tokens = pos - own * 8 + 1;
     const int E = cnt + 1;
-    const int e0 = split * p.entries_per_split;
     const int e1 = min(E, e0 + p.entries_per_split);
     const int npairs = e1 > e0 ? (e1 - e0 + 1) >> 1 : 0;
     const int nmy = npairs > warp ? (npairs - warp + kAttnWarps - 1) / kAttnWarps : 0;
-    const int32_t* ids = p.sel_ids + ng * p.top_k;
     const int64_t row_base = ((int64_t)b * p.G + g) * p.t_cap;
 
     uint8_t* wstage = smem + warp * kAttnStages * kPairBytes;
@@ -102,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
             rid = own;
             return own_tokens;
         }
-        rid = ids[e];
+        rid = e == e_first ? id_pref0 : e == e_first + 1 ? id_pref1 : ids[e];
         if (rid < 0 || rid >= own) {
             raise_status(p.status, kDevRange);
             rid = -1;
@@ -139,6 +159,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     };
 
     for (int li = 0; li < kAttnStages && li < nmy; ++li) issue(li);
+    STEP5_STAMP(4, 2);
 
     // query heads of the group as the A operand (rows >= hq_g are zero)
     const int qr = lane >> 2, qc = (lane & 3) * 2;
@@ -185,6 +206,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
             }
             __syncwarp();
         }
+        if (li == 0) STEP5_STAMP(4, 3);
         const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
 
         // S = Q K^T over the 16 tokens (slot 0: tokens 0-7, slot 1: tokens 8-15)
@@ -269,7 +291,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         if (lane == 0) raise_status(p.status, kDevTimeout);
         // give the copies this warp issued and did not consume a bounded chance to land
         // before the block's shared memory goes away
-        for (int li = li_fail + 1; li < nmy && li < li_fail + kAttnStages; ++li)
+        for (int li = li_fail; li < nmy && li < li_fail + kAttnStages; ++li)
             mbar_wait(&wbar[li % kAttnStages], (uint32_t)((li / kAttnStages) & 1));
     }
 
@@ -278,16 +300,17 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-    // ---- merge the 4 warps through shared memory (reuses the stage buffers)
+    // ---- merge the warps through shared memory (reuses the stage buffers)
+    STEP5_STAMP(4, 4);
     __syncthreads();
     float* mw = reinterpret_cast<float*>(smem) + warp * kMergeFloatsPerWarp;
 #pragma unroll
     for (int nn = 0; nn < 16; ++nn) {
-        const int d = nn * 8 + qc;
-        mw[qr * 128 + d] = o[nn][0];
-        mw[qr * 128 + d + 1] = o[nn][1];
-        mw[(qr + 8) * 128 + d] = o[nn][2];
-        mw[(qr + 8) * 128 + d + 1] = o[nn][3];
+        const int dd = nn * 8 + qc;
+        mw[qr * 128 + dd] = o[nn][0];
+        mw[qr * 128 + dd + 1] = o[nn][1];
+        mw[(qr + 8) * 128 + dd] = o[nn][2];
+        mw[(qr + 8) * 128 + dd + 1] = o[nn][3];
     }
     if ((lane & 3) == 0) {
         mw[2048 + qr] = m0;
@@ -296,12 +319,13 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         mw[2048 + 16 + qr + 8] = l1;
     }
     __syncthreads();
+    STEP5_STAMP(4, 5);
 
-    // this block's state: merge of its warps, kept in shared memory (rows < hq_g)
-    float* mine = reinterpret_cast<float*>(smem) + kAttnWarps * kMergeFloatsPerWarp;
+    // this block's state; thread (rpar, d) handles dim d of rows rpar, rpar + 2, ...
+    const int d = tid & 127, rpar = tid >> 7;
     const float* mall = reinterpret_cast<const float*>(smem);
-    const int d = tid;  // 128 threads = 128 dims
-    for (int r = 0; r < hq_g; ++r) {
+    const uint32_t my_slot = smem_u32(slots + (size_t)cluster_ctarank() * hq_g * kSlotFloats);
+    for (int r = rpar; r < hq_g; r += 2) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mall[w * kMergeFloatsPerWarp + 2048 + r]);
@@ -313,117 +337,94 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
             L += mall[w * kMergeFloatsPerWarp + 2048 + 16 + r] * sc;
             O += mall[w * kMergeFloatsPerWarp + r * 128 + d] * sc;
         }
-        if (p.splits == 1) {
+        if (C == 1) {
             p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / L);
         } else {
+            // push into block 0's slot for this block (remote stores, no waiting)
+            const uint32_t a = map_cluster(my_slot + (uint32_t)(r * kSlotFloats) * 4u, 0u);
             if (d == 0) {
-                mine[r * 130 + 0] = M;
-                mine[r * 130 + 1] = L;
+                st_cluster_f32(a, M);
+                st_cluster_f32(a + 4, L);
             }
-            mine[r * 130 + 2 + d] = O;
+            st_cluster_f32(a + (uint32_t)(2 + d) * 4u, O);
         }
     }
-    if (p.splits == 1) return;
+    if (C == 1) return;
+    cluster_sync();  // every push is visible to block 0
+    STEP5_STAMP(4, 6);
+    if (cluster_ctarank() != 0) return;
 
-    // ---- the cluster's blocks (splits of one row and group) merge on chip: block 0 of
-    // the cluster reads the others' states through distributed shared memory, in rank
-    // order
-    const int C = p.cluster;
-    float* cmerged = mine + 16 * 130;  // block 0's merged state
-    if (C > 1) {
-        cluster_sync();
-        if (cluster_ctarank() == 0) {
-            const uint32_t mine_addr = smem_u32(mine);
-            for (int r = 0; r < hq_g; ++r) {
-                float mr[kMaxCluster], lr[kMaxCluster], orr[kMaxCluster];
-                float M = -INFINITY;
-                for (int c = 0; c < C; ++c) {
-                    const uint32_t a = map_cluster(mine_addr + (uint32_t)(r * 130) * 4u, (uint32_t)c);
-                    mr[c] = ld_cluster_f32(a);
-                    lr[c] = ld_cluster_f32(a + 4);
-                    orr[c] = ld_cluster_f32(a + (uint32_t)(2 + d) * 4u);
-                    M = fmaxf(M, mr[c]);
-                }
-                const float base = (M == -INFINITY) ? 0.0f : M;
-                float L = 0.0f, O = 0.0f;
-                for (int c = 0; c < C; ++c) {
-                    const float sc = exp2f(mr[c] - base);
-                    L += lr[c] * sc;
-                    O += orr[c] * sc;
-                }
-                if (d == 0) {
-                    cmerged[r * 130 + 0] = M;
-                    cmerged[r * 130 + 1] = L;
-                }
-                cmerged[r * 130 + 2 + d] = O;
-            }
-        }
-        cluster_sync();  // peers keep their shared memory until block 0 has read it
-        if (cluster_ctarank() != 0) return;
-    } else {
-        cmerged = mine;
-    }
-    __syncthreads();
-
-    const int nclusters = p.splits / C;
-    const int cid = split / C;
-    if (nclusters == 1) {
-        for (int r = 0; r < hq_g; ++r)
-            p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] =
-                f32_to_bf16_bits(cmerged[r * 130 + 2 + d] / cmerged[r * 130 + 1]);
-        return;
-    }
-    float* part = p.partial + (ng * nclusters + cid) * (int64_t)hq_g * 130;
-    for (int r = 0; r < hq_g; ++r) {
-        if (d == 0) {
-            part[r * 130 + 0] = cmerged[r * 130 + 0];
-            part[r * 130 + 1] = cmerged[r * 130 + 1];
-        }
-        part[r * 130 + 2 + d] = cmerged[r * 130 + 2 + d];
-    }
-
-    // ---- the cluster leader that finishes last merges every cluster's state, in order
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const uint32_t ticket = atomicAdd(p.counter + ng, 1u);
-        s_last = (ticket == (uint32_t)(nclusters - 1));
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    const float* pall = p.partial + ng * nclusters * (int64_t)hq_g * 130;
-    for (int r = 0; r < hq_g; ++r) {
+    // ---- block 0: merge the C slots in rank order, from its own shared memory
+    for (int r = rpar; r < hq_g; r += 2) {
         float M = -INFINITY;
-        for (int c = 0; c < nclusters; ++c) M = fmaxf(M, __ldcg(pall + ((int64_t)c * hq_g + r) * 130));
+        for (int c = 0; c < C; ++c) M = fmaxf(M, slots[((size_t)c * hq_g + r) * kSlotFloats]);
         const float base = (M == -INFINITY) ? 0.0f : M;
         float L = 0.0f, O = 0.0f;
-        for (int c = 0; c < nclusters; ++c) {
-            const float* ps = pall + ((int64_t)c * hq_g + r) * 130;
-            const float sc = exp2f(__ldcg(ps) - base);
-            L += __ldcg(ps + 1) * sc;
-            O += __ldcg(ps + 2 + d) * sc;
+        for (int c = 0; c < C; ++c) {
+            const float* sl = slots + ((size_t)c * hq_g + r) * kSlotFloats;
+            const float sc = exp2f(sl[0] - base);
+            L += sl[1] * sc;
+            O += sl[2 + d] * sc;
         }
         p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / L);
     }
-    if (tid == 0) p.counter[ng] = 0;
+    STEP5_STAMP(4, 7);
 }
 
 }  // namespace
 
-cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                             cudaStream_t stream, bool pdl) {
+static cudaError_t ensure_attn_attr() {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+                                             (int)attn_smem_bytes(16, 8));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    return cudaSuccess;
+}
+
+size_t attention_smem_bytes(int cluster, int hq_g) { return attn_smem_bytes(cluster, hq_g); }
+
+int attention_max_active_clusters(int cluster, int hq_g) {
+    static int cache[64][17][17] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cluster < 1 || cluster > 16 || hq_g < 1 ||
+        hq_g > 16)
+        return 0;
+    if (cache[dev][cluster][hq_g] == 0) {
+        int n = -1;
+        if (ensure_attn_attr() == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = attn_smem_bytes(cluster, hq_g);
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)cluster;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int m = 0;
+            if (cudaOccupancyMaxActiveClusters(&m, sparse_attn_kernel, &cfg) == cudaSuccess && m > 0) n = m;
+            cudaGetLastError();  // clear a refused configuration
+        }
+        cache[dev][cluster][hq_g] = n;
+    }
+    return cache[dev][cluster][hq_g] > 0 ? cache[dev][cluster][hq_g] : 0;
+}
+
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             cudaStream_t stream, bool pdl) {
+    cudaError_t e0 = ensure_attn_attr();
+    if (e0 != cudaSuccess) return e0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.splits, p.G, p.N);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = attn_smem_bytes(p.cluster, p.hq_g);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int na = 0;

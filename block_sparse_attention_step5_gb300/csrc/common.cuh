@@ -9,6 +9,29 @@
 
 namespace step5 {
 
+// ---------------------------------------------------------------------------------
+// Phase trace (build with -DSTEP5_TRACE -rdc=true): thread 0 of each block records
+// %globaltimer at numbered points into a buffer registered by step5_trace_buffer():
+// trace[((kernel * 4096) + block) * 16 + point].  Compiles to nothing otherwise.
+// ---------------------------------------------------------------------------------
+#ifdef STEP5_TRACE
+extern __device__ unsigned long long* g_trace;
+#define STEP5_STAMP(kernel_id, point)                                                            \
+    do {                                                                                         \
+        if (threadIdx.x == 0 && g_trace) {                                                       \
+            const unsigned long long bl_ =                                                       \
+                blockIdx.x + (unsigned long long)gridDim.x * (blockIdx.y + (unsigned long long)gridDim.y * blockIdx.z); \
+            unsigned long long t_;                                                               \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                               \
+            if (bl_ < 4096) g_trace[((kernel_id) * 4096ull + bl_) * 16 + (point)] = t_;         \
+        }                                                                                        \
+    } while (0)
+#else
+#define STEP5_STAMP(kernel_id, point) \
+    do {                              \
+    } while (0)
+#endif
+
 constexpr uint32_t kDevRange = 1u;
 constexpr uint32_t kDevTimeout = 2u;
 
@@ -138,6 +161,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 1-D bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) into shared
+// memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
 

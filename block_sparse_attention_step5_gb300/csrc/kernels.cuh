@@ -27,6 +27,7 @@ cudaError_t launch_convert(const uint16_t* in, uint8_t* out, int64_t n, cudaStre
 // ----------------------------------------------------------------- steps (2) + (3)
 constexpr int kHistBits = 12;
 constexpr int kHistBins = 1 << kHistBits;
+constexpr int kCoarseBins = 64;         // groups of 64 fine bins
 constexpr int kCandCap = 2048;          // candidates per (row, group) on the split path
 constexpr int kFusedMaxRegions = 16384; // regions a fused block keeps in shared memory
 constexpr int kMaxTopK = 2048;
@@ -46,18 +47,20 @@ struct ScoreParams {
     uint32_t* hist;          // [N][G][kHistBins]   (split path, zero between calls)
     uint32_t* cand_count;    // [N][G]              (split path, zero between calls)
     uint64_t* cand;          // [N][G][kCandCap]    (split path)
+    uint32_t* ticket;        // [N][G]              (split path, zero between calls)
+    uint32_t* coarse;        // [N][G][kCoarseBins] (split path, zero between calls)
     uint32_t* status;
     int N, B, G, idx_heads, hpg, t_cap, r_cap, rope_dims, top_k;
-    int regions_per_cta;     // split path: regions scored by one block
+    int regions_per_cta;     // split path: regions filtered by one block
+    int chunks_per_ng, items_per_cta, num_sms;  // split path: persistent scoring blocks
 };
 cudaError_t launch_score_fused(const ScoreParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_score_split(const ScoreParams& p, cudaStream_t stream, bool pdl);
 
 // ----------------------------------------------------------------- step (4)
-constexpr int kAttnWarps = 4;
+constexpr int kAttnWarps = 8;
 constexpr int kAttnStages = 2;          // pair buffers per warp
-constexpr int kMaxSplits = 128;
-constexpr int kMaxCluster = 8;          // portable cluster size
+constexpr int kMaxCluster = 16;         // blocks per (row, group) (non-portable above 8)
 
 struct AttnParams {
     const uint16_t* q;       // [N][Hq][128]
@@ -66,8 +69,6 @@ struct AttnParams {
     const int32_t* sel_ids;  // [N][G][top_k]
     const int32_t* sel_count;
     uint16_t* out;           // [N][Hq][128]
-    float* partial;          // [N][G][splits / cluster][hq_g][130]  (m, l, o[128])
-    uint32_t* counter;       // [N][G]  (zero between calls)
     uint32_t* status;
     int N, B, G, Hq, hq_g, t_cap, top_k;
     int splits, entries_per_split, cluster;
@@ -75,5 +76,8 @@ struct AttnParams {
 };
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream, bool pdl);
+// Clusters of `cluster` attention blocks that can be resident at once (0 if unknown).
+int attention_max_active_clusters(int cluster, int hq_g);
+size_t attention_smem_bytes(int cluster, int hq_g);
 
 }  // namespace step5

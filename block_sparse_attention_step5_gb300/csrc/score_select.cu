@@ -30,7 +30,7 @@ namespace {
 template <int HPG>
 struct QFrag {
     float2 q[HPG][8];  // e4m3 query of head h at dims 16*qd + 2i, 16*qd + 2i + 1
-    float w[HPG];
+    float w[HPG];      // w of every head (HPG == 4: w[0] holds head qd's weight)
 };
 
 // e4m3(bf16(NEOX(q))) for the group's HPG heads into shared memory, then each thread
@@ -52,14 +52,16 @@ __device__ void load_qfrag(const ScoreParams& p, int n, int g, int pos, float* s
         }
         s_q[i] = e4m3x2_to_f32x2(f32_to_e4m3(bf16_to_f32(rb))).x;
     }
-    __syncthreads();
     const int qd = threadIdx.x & 3;
+#pragma unroll
+    for (int h = 0; h < HPG; ++h) f.w[h] = p.w[(int64_t)n * p.idx_heads + (int64_t)g * HPG + h];
+    if constexpr (HPG == 4) f.w[0] = p.w[(int64_t)n * p.idx_heads + (int64_t)g * HPG + qd];
+    __syncthreads();
 #pragma unroll
     for (int h = 0; h < HPG; ++h) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             f.q[h][i] = make_float2(s_q[h * 64 + 16 * qd + 2 * i], s_q[h * 64 + 16 * qd + 2 * i + 1]);
-        f.w[h] = p.w[(int64_t)n * p.idx_heads + (int64_t)g * HPG + h];
     }
 }
 
@@ -82,64 +84,123 @@ __device__ __forceinline__ float score_from_vec(const QFrag<HPG>& f, uint4 v) {
             acc[h] = __ffma2_rn(f.q[h][2 * q + 1], s1, acc[h]);
         }
     }
-    float sc = 0.0f;
+    if constexpr (HPG == 4) {
+        // transpose-reduce over the region's 4 lanes: afterwards lane qd holds head qd's
+        // full dot product; then relu * w and a sum over the 4 lanes
+        const int qd = threadIdx.x & 3;
+        float d0 = __fadd_rn(acc[0].x, acc[0].y), d1 = __fadd_rn(acc[1].x, acc[1].y);
+        float d2 = __fadd_rn(acc[2].x, acc[2].y), d3 = __fadd_rn(acc[3].x, acc[3].y);
+        const bool lo2 = qd < 2;
+        const float send0 = lo2 ? d2 : d0, send1 = lo2 ? d3 : d1;
+        float k0 = lo2 ? d0 : d2, k1 = lo2 ? d1 : d3;
+        k0 = __fadd_rn(k0, __shfl_xor_sync(0xffffffffu, send0, 2));
+        k1 = __fadd_rn(k1, __shfl_xor_sync(0xffffffffu, send1, 2));
+        const bool odd = qd & 1;
+        const float send = odd ? k0 : k1;
+        float dot = __fadd_rn(odd ? k1 : k0, __shfl_xor_sync(0xffffffffu, send, 1));
+        float v = __fmul_rn(fmaxf(dot, 0.0f), f.w[0]);
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 1));
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 2));
+        return __fadd_rn(v, 0.0f);  // -0 -> +0
+    } else {
+        float sc = 0.0f;
 #pragma unroll
-    for (int h = 0; h < HPG; ++h) {
-        float dot = __fadd_rn(acc[h].x, acc[h].y);
-        dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, 1));
-        dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, 2));
-        sc = fmaf(fmaxf(dot, 0.0f), f.w[h], sc);
+        for (int h = 0; h < HPG; ++h) {
+            float dot = __fadd_rn(acc[h].x, acc[h].y);
+            dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, 1));
+            dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, 2));
+            sc = fmaf(fmaxf(dot, 0.0f), f.w[h], sc);
+        }
+        return __fadd_rn(sc, 0.0f);  // -0 -> +0
     }
-    return __fadd_rn(sc, 0.0f);  // -0 -> +0
 }
 
 // ----------------------------------------------------------------- block top-k
 
+constexpr int kRadixBits = 11;
+constexpr int kRadixBins = 1 << kRadixBits;
+
 struct TopkSmem {
-    uint32_t hist[256];
+    uint32_t hist[kRadixBins];
+    uint32_t wsum[32];
     uint32_t count;
     uint32_t v, before, inbin;
 };
 
-// Selects the K smallest of cnt unique 64-bit keys (all of them if cnt <= K), writes
-// them sorted ascending to s_sel[0..P2) (padded with ~0), returns min(cnt, K).
-// get(i) returns key i.  Must be called by all NT threads of the block.
+// Bitonic sort, ascending, of P2 (a power of two >= 32) keys in shared memory.  Stages
+// whose partner distance is below 32 run in registers with warp shuffles; the others
+// exchange through shared memory.
+template <int NT>
+__device__ void block_bitonic_sort(uint64_t* s, int P2) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = NT / 32;
+    for (int k = 2; k <= P2; k <<= 1) {
+        int j = k >> 1;
+        for (; j >= 32; j >>= 1) {
+            for (int i = tid; i < P2; i += NT) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const uint64_t a = s[i], b = s[ixj];
+                    const bool asc = (i & k) == 0;
+                    if ((a > b) == asc) {
+                        s[i] = b;
+                        s[ixj] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        // remaining distances j < 32: within aligned chunks of 32 keys, one per lane
+        for (int c = warp; c < P2 / 32; c += NW) {
+            const int i = c * 32 + lane;
+            uint64_t v = s[i];
+            for (int jj = j; jj > 0; jj >>= 1) {
+                const uint64_t o = __shfl_xor_sync(0xffffffffu, v, jj);
+                const bool asc = (i & k) == 0;
+                const bool lower = (i & jj) == 0;
+                v = (lower == asc) ? (v < o ? v : o) : (v > o ? v : o);
+            }
+            s[i] = v;
+        }
+        __syncthreads();
+    }
+}
+
+// Gathers the K smallest of cnt unique 64-bit keys (all of them if cnt <= K) into
+// s_sel[0..min(cnt, K)) in no particular order, pads s_sel up to P2 (a power of two >=
+// max(K, 32)) with ~0, returns min(cnt, K).  A radix descent over 11-bit digits (most
+// significant first) finds the K-th key; every key at or below it is gathered.  get(i)
+// returns key i.  Must be called by all NT threads of the block.
 template <int NT, class Get>
-__device__ int block_topk(Get get, int cnt, int K, int P2, uint64_t* s_sel, TopkSmem& ts) {
+__device__ int block_select_set(Get get, int cnt, int K, int P2, uint64_t* s_sel, TopkSmem& ts) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint64_t bound = ~0ull;
     if (cnt > K) {
         uint64_t prefix = 0;
         int need = K;
-        for (int shift = 56; shift >= 0; shift -= 8) {
-            for (int i = tid; i < 256; i += NT) ts.hist[i] = 0;
+        int hi = 64;  // key bits at and above `hi` are fixed by `prefix`
+        while (hi > 0) {
+            const int width = hi >= kRadixBits ? kRadixBits : hi;
+            const int shift = hi - width;
+            const uint32_t dmask = (1u << width) - 1u;
+            for (int i = tid; i < kRadixBins; i += NT) ts.hist[i] = 0;
             __syncthreads();
-            const uint64_t mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
-            for (int base = 0; base < cnt; base += NT) {
-                const int i = base + tid;
-                bool act = false;
-                uint32_t bin = 0;
-                if (i < cnt) {
-                    const uint64_t k = get(i);
-                    if ((k & mask) == prefix) {
-                        act = true;
-                        bin = (uint32_t)(k >> shift) & 255u;
-                    }
-                }
-                const uint32_t am = __ballot_sync(0xffffffffu, act);
-                if (act) {
-                    const uint32_t peers = __match_any_sync(am, bin);
-                    if (lane == __ffs(peers) - 1) atomicAdd(&ts.hist[bin], (uint32_t)__popc(peers));
-                }
+            const uint64_t mask = (hi == 64) ? 0ull : (~0ull << hi);
+            for (int i = tid; i < cnt; i += NT) {
+                const uint64_t k = get(i);
+                if ((k & mask) == prefix) atomicAdd(&ts.hist[(uint32_t)(k >> shift) & dmask], 1u);
             }
             __syncthreads();
-            if (warp == 0) {
-                uint32_t loc[8];
+            {
+                // block-wide scan: each thread owns PER consecutive bins
+                constexpr int PER = kRadixBins / NT;
+                constexpr int NW = NT / 32;
+                uint32_t loc[PER];
                 uint32_t sum = 0;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    loc[k] = ts.hist[8 * lane + k];
-                    sum += loc[k];
+                for (int q = 0; q < PER; ++q) {
+                    loc[q] = ts.hist[tid * PER + q];
+                    sum += loc[q];
                 }
                 uint32_t incl = sum;
 #pragma unroll
@@ -147,18 +208,31 @@ __device__ int block_topk(Get get, int cnt, int K, int P2, uint64_t* s_sel, Topk
                     const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
                     if (lane >= o) incl += t;
                 }
+                if (lane == 31) ts.wsum[warp] = incl;
+                __syncthreads();
+                if (warp == 0) {
+                    uint32_t w = lane < NW ? ts.wsum[lane] : 0u;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t t = __shfl_up_sync(0xffffffffu, w, o);
+                        if (lane >= o) w += t;
+                    }
+                    if (lane < NW) ts.wsum[lane] = w;  // inclusive warp prefix
+                }
+                __syncthreads();
+                incl += warp ? ts.wsum[warp - 1] : 0u;
                 const uint32_t excl = incl - sum;
                 if (excl < (uint32_t)need && (uint32_t)need <= incl) {
                     uint32_t c = excl;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        if (c + loc[k] >= (uint32_t)need) {
-                            ts.v = 8 * lane + k;
+                    for (int q = 0; q < PER; ++q) {
+                        if (c + loc[q] >= (uint32_t)need) {
+                            ts.v = tid * PER + q;
                             ts.before = c;
-                            ts.inbin = loc[k];
+                            ts.inbin = loc[q];
                             break;
                         }
-                        c += loc[k];
+                        c += loc[q];
                     }
                 }
             }
@@ -171,6 +245,7 @@ __device__ int block_topk(Get get, int cnt, int K, int P2, uint64_t* s_sel, Topk
                 bound = prefix | ((shift == 0) ? 0ull : ((1ull << shift) - 1ull));
                 break;
             }
+            hi = shift;
         }
     }
     if (tid == 0) ts.count = 0;
@@ -194,23 +269,15 @@ __device__ int block_topk(Get get, int cnt, int K, int P2, uint64_t* s_sel, Topk
         }
     }
     __syncthreads();
-    for (int k = 2; k <= P2; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < P2; i += NT) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const uint64_t a = s_sel[i], b = s_sel[ixj];
-                    const bool asc = (i & k) == 0;
-                    if ((a > b) == asc) {
-                        s_sel[i] = b;
-                        s_sel[ixj] = a;
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
     return cnt < K ? cnt : K;
+}
+
+// block_select_set followed by an ascending sort of the gathered keys.
+template <int NT, class Get>
+__device__ int block_topk(Get get, int cnt, int K, int P2, uint64_t* s_sel, TopkSmem& ts) {
+    const int take = block_select_set<NT>(get, cnt, K, P2, s_sel, ts);
+    block_bitonic_sort<NT>(s_sel, P2);
+    return take;
 }
 
 // Key getters for block_topk.
@@ -271,6 +338,7 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
 
     const int g = blockIdx.x, n = blockIdx.y;
     pdl_wait();
+    pdl_launch_dependents();
     int b, pos;
     int R = row_regions(p, n, b, pos);
     if (R < 0 || R > key_cap) {
@@ -294,17 +362,17 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
             const int r = r0 + u * 64 + slot;
             v[u] = (r < R) ? __ldg(base + (int64_t)r * 4 + qd) : make_uint4(0, 0, 0, 0);
         }
+        float sc[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int r = r0 + u * 64 + slot;
-            const float sc = score_from_vec<HPG>(f, v[u]);
-            if (qd == 0 && r < R) {
-                s_key[r] = desc_key(sc);
-                if (exp_scores) exp_scores[r] = sc;
-            }
+        for (int u = 0; u < U; ++u) sc[u] = score_from_vec<HPG>(f, v[u]);
+        // lane qd keeps the bookkeeping of region u = qd
+        const float mysc = qd == 0 ? sc[0] : qd == 1 ? sc[1] : qd == 2 ? sc[2] : sc[3];
+        const int r = r0 + qd * 64 + slot;
+        if (r < R) {
+            s_key[r] = desc_key(mysc);
+            if (exp_scores) exp_scores[r] = mysc;
         }
     }
-    pdl_launch_dependents();
     __syncthreads();
     const int take = block_topk<kFusedThreads>(SmemKeys{s_key}, R, p.top_k, P2, s_sel, ts);
     write_selection<kFusedThreads>(p, n, g, take, s_sel);
@@ -313,102 +381,251 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
 // ----------------------------------------------------------------- split path
 
 constexpr int kSplitThreads = 256;
-constexpr int kSplitRegions = 512;  // regions scored by one block of the split path
 
-template <int HPG>
-__global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(ScoreParams p) {
-    __shared__ uint32_t s_hist[kHistBins];
-    __shared__ float s_q[HPG * 64];
-    const int g = blockIdx.y, n = blockIdx.z;
-    pdl_wait();
+// ----------------------------------------------------------------- split path scoring
+//
+// Persistent blocks (two per SM) walk a contiguous run of tiles; a tile is kTileRegions
+// consecutive regions of one (row, group), contiguous in the summary store, fetched with
+// one bulk copy into a 2-stage shared-memory ring while the previous tile is scored.
+// Each run of tiles of one (row, group) adds its shared-memory histogram to the global
+// one and takes a ticket; the block holding the last ticket publishes the bin of the
+// k-th key for the filter pass.
+
+constexpr int kTileRegions = 512;                 // 32 KB of summaries
+constexpr int kTileBytes = kTileRegions * 64;
+constexpr int kTileU = kTileRegions / 64;         // regions per thread per tile (8)
+constexpr int kScoreStages = 2;
+constexpr size_t kScoreSmem = kScoreStages * kTileBytes + 1024;
+
+struct Tile {
+    int valid, ng, n, g, b, pos, R, c0, c1;
+};
+
+// Tile `t` of the flattened (row, group, tile) space, with its row's geometry;
+// invalid when the row is out of range or the tile starts past its candidates.
+__device__ __forceinline__ Tile tile_at(const ScoreParams& p, int t) {
+    Tile x;
+    x.valid = 0;
+    const int ng = t / p.chunks_per_ng;
+    const int chunk = t - ng * p.chunks_per_ng;
+    const int n = ng / p.G;
     int b, pos;
     const int R = row_regions(p, n, b, pos);
     if (R < 0) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) raise_status(p.status, kDevRange);
-        return;
+        if (chunk == 0 && threadIdx.x == 0) raise_status(p.status, kDevRange);
+        return x;
     }
-    const int c0 = blockIdx.x * kSplitRegions;
-    const int c1 = min(R, c0 + kSplitRegions);
-    if (c0 >= c1) return;
-    // the block's summaries are requested before anything else (they do not depend on
-    // the query): 8 regions of 16 bytes per thread in flight
-    const int qd = threadIdx.x & 3;
-    const int slot = threadIdx.x >> 2;
-    const uint4* base = reinterpret_cast<const uint4*>(p.summ + ((int64_t)b * p.G + g) * p.r_cap * 64);
-    constexpr int U = kSplitRegions / 64;
-    uint4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int r = c0 + u * 64 + slot;
-        v[u] = (r < c1) ? __ldg(base + (int64_t)r * 4 + qd) : make_uint4(0, 0, 0, 0);
-    }
-    for (int i = threadIdx.x; i < kHistBins; i += kSplitThreads) s_hist[i] = 0;
-    QFrag<HPG> f;
-    load_qfrag<HPG>(p, n, g, pos, s_q, f);  // has a __syncthreads
-
-    float* scores = p.scores + ((int64_t)n * p.G + g) * p.r_cap;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int r = c0 + u * 64 + slot;
-        const float sc = score_from_vec<HPG>(f, v[u]);
-        if (qd == 0 && r < c1) {
-            scores[r] = sc;
-            atomicAdd(&s_hist[desc_key(sc) >> (32 - kHistBits)], 1u);
-        }
-    }
-    __syncthreads();
-    uint32_t* gh = p.hist + ((int64_t)n * p.G + g) * kHistBins;
-    for (int i = threadIdx.x; i < kHistBins; i += kSplitThreads) {
-        const uint32_t c = s_hist[i];
-        if (c) atomicAdd(gh + i, c);
-    }
-    pdl_launch_dependents();
+    const int c0 = chunk * kTileRegions;
+    if (c0 >= R) return x;
+    x.valid = 1;
+    x.ng = ng;
+    x.n = n;
+    x.g = ng - n * p.G;
+    x.b = b;
+    x.pos = pos;
+    x.R = R;
+    x.c0 = c0;
+    x.c1 = min(R, c0 + kTileRegions);
+    return x;
 }
 
-// Bin holding the K-th smallest key of (row, group), from the global histogram; all
-// bins when the row has at most K regions.
-__device__ int threshold_bin(const uint32_t* gh, int R, int K, int* s_part, int* s_out) {
-    constexpr int per = kHistBins / kSplitThreads;  // 16
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (R <= K) return kHistBins - 1;
-    int loc[per];
-    int sum = 0;
+// Scores one staged tile: thread (slot, qd) covers regions u * 64 + slot, u < kTileU;
+// lane qd of each region quad keeps the score and histogram update of every fourth
+// region.  FULL: the tile holds kTileRegions regions (no bounds checks).
+template <int HPG, bool FULL>
+__device__ __forceinline__ void score_tile(const QFrag<HPG>& f, const uint4* tile, int nreg, float* scores,
+                                           uint32_t* s_hist, int qd, int slot) {
 #pragma unroll
-    for (int k = 0; k < per; ++k) {
-        loc[k] = (int)gh[tid * per + k];
-        sum += loc[k];
-    }
-    int incl = sum;
+    for (int u4 = 0; u4 < kTileU; u4 += 4) {
+        float sc[4];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    if (lane == 31) s_part[warp] = incl;
-    __syncthreads();
-    int wbase = 0;
-    for (int w = 0; w < warp; ++w) wbase += s_part[w];
-    incl += wbase;
-    const int excl = incl - sum;
-    if (excl < K && K <= incl) {
-        int c = excl;
-        for (int k = 0; k < per; ++k) {
-            c += loc[k];
-            if (c >= K) {
-                *s_out = tid * per + k;
-                break;
-            }
+        for (int u = 0; u < 4; ++u) {
+            const int lr = (u4 + u) * 64 + slot;
+            const uint4 v = (FULL || lr < nreg) ? tile[lr * 4 + qd] : make_uint4(0, 0, 0, 0);
+            sc[u] = score_from_vec<HPG>(f, v);
         }
+        const float mysc = qd == 0 ? sc[0] : qd == 1 ? sc[1] : qd == 2 ? sc[2] : sc[3];
+        const int lr = (u4 + qd) * 64 + slot;
+        if (FULL || lr < nreg) {
+            scores[lr] = mysc;
+            atomicAdd(&s_hist[desc_key(mysc) >> (32 - kHistBits)], 1u);
+        }
+    }
+}
+
+template <int HPG>
+__global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(ScoreParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint32_t s_hist[kHistBins];
+    __shared__ float s_q[HPG * 64];
+    __shared__ __align__(8) uint64_t s_bar[kScoreStages];
+    const int tid = threadIdx.x;
+    const int qd = tid & 3, slot = tid >> 2;
+
+    if (tid == 0) {
+        for (int st = 0; st < kScoreStages; ++st) mbar_init(&s_bar[st], 1);
+        fence_mbar_init();
+    }
+    STEP5_STAMP(1, 0);
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+    STEP5_STAMP(1, 1);
+    const int total = p.N * p.G * p.chunks_per_ng;
+    const int t0 = blockIdx.x * p.items_per_cta;
+    const int t1 = min(total, t0 + p.items_per_cta);
+
+    int next_t = t0;
+    auto next_valid = [&]() -> Tile {
+        Tile x;
+        x.valid = 0;
+        while (next_t < t1 && !x.valid) x = tile_at(p, next_t++);
+        return x;
+    };
+    auto issue = [&](const Tile& x, int st) {
+        if (tid == 0) {
+            const uint32_t bytes = (uint32_t)(x.c1 - x.c0) * 64u;
+            mbar_arrive_expect_tx(&s_bar[st], bytes);
+            bulk_load(ring + st * kTileBytes, p.summ + (((int64_t)x.b * p.G + x.g) * p.r_cap + x.c0) * 64,
+                      bytes, &s_bar[st]);
+        }
+    };
+    // two tiles in flight: `cur` in stage st, `nxt` in stage st ^ 1
+    Tile cur = next_valid();
+    if (cur.valid) issue(cur, 0);
+    Tile nxt = next_valid();
+    if (nxt.valid) issue(nxt, 1);
+    STEP5_STAMP(1, 2);
+
+    int seg_ng = -1;
+    int ntile = 0;
+    QFrag<HPG> f;
+    auto finish = [&](int ng) {
+        __syncthreads();
+        uint32_t* gh = p.hist + (int64_t)ng * kHistBins;
+        uint32_t coarse = 0;
+        // each thread flushes kHistBins / 256 = 16 consecutive fine bins; 4 threads make
+        // one coarse bin of 64
+        for (int i = 0; i < kHistBins / kSplitThreads; ++i) {
+            const int bin = tid * (kHistBins / kSplitThreads) + i;
+            const uint32_t c = s_hist[bin];
+            coarse += c;
+            if (c) atomicAdd(gh + bin, c);
+        }
+        coarse += __shfl_xor_sync(0xffffffffu, coarse, 1);
+        coarse += __shfl_xor_sync(0xffffffffu, coarse, 2);
+        if ((tid & 3) == 0 && coarse) atomicAdd(p.coarse + (int64_t)ng * kCoarseBins + (tid >> 2), coarse);
+    };
+
+    uint32_t ph0 = 0, ph1 = 0;
+    int st = 0;
+    bool timed_out = false;
+    while (cur.valid) {
+        if (cur.ng != seg_ng) {
+            if (seg_ng >= 0) finish(seg_ng);
+            seg_ng = cur.ng;
+            for (int i = tid; i < kHistBins; i += kSplitThreads) s_hist[i] = 0;
+            load_qfrag<HPG>(p, cur.n, cur.g, cur.pos, s_q, f);  // has a __syncthreads
+        }
+        if (ntile < 4) STEP5_STAMP(1, 3 + 2 * ntile);
+        if (!mbar_wait(&s_bar[st], st ? ph1 : ph0)) {
+            timed_out = true;
+            break;
+        }
+        if (ntile < 4) STEP5_STAMP(1, 4 + 2 * ntile);
+        ++ntile;
+        if (st) ph1 ^= 1u; else ph0 ^= 1u;
+        const uint4* tile = reinterpret_cast<const uint4*>(ring + st * kTileBytes);
+        float* scores = p.scores + (int64_t)cur.ng * p.r_cap + cur.c0;
+        const int nreg = cur.c1 - cur.c0;
+        if (nreg == kTileRegions)
+            score_tile<HPG, true>(f, tile, nreg, scores, s_hist, qd, slot);
+        else
+            score_tile<HPG, false>(f, tile, nreg, scores, s_hist, qd, slot);
+        __syncthreads();  // every thread is done with this stage before it is refilled
+        cur = nxt;
+        nxt = next_valid();
+        if (nxt.valid) {
+            if (tid == 0) fence_proxy_async();
+            issue(nxt, st);
+        }
+        st ^= 1;
+    }
+    if (timed_out) {
+        if (tid == 0) raise_status(p.status, kDevTimeout);
+        // give copies still in flight a bounded chance to land before the block exits
+        if (cur.valid) mbar_wait(&s_bar[st], st ? ph1 : ph0);
+        if (nxt.valid) mbar_wait(&s_bar[st ^ 1], st ? ph0 : ph1);
+    }
+    STEP5_STAMP(1, 11);
+    if (seg_ng >= 0 && !timed_out) finish(seg_ng);
+    STEP5_STAMP(1, 12);
+}
+
+// Bin holding the K-th smallest key of (row, group) from the coarse (64-bin) and fine
+// (4096-bin) histograms; all bins when the row has at most K regions.  Two small reads
+// (256 bytes each) instead of the whole fine histogram.
+__device__ int threshold_bin2(const uint32_t* coarse, const uint32_t* fine, int R, int K, int* s_out) {
+    if (R <= K) return kHistBins - 1;
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid < 32) {
+        const uint32_t c0 = __ldcg(coarse + 2 * lane), c1 = __ldcg(coarse + 2 * lane + 1);
+        uint32_t incl = c0 + c1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const uint32_t excl = incl - c0 - c1;
+        // the coarse bin holding the K-th key
+        int cb = -1;
+        uint32_t before = 0;
+        if (excl < (uint32_t)K && (uint32_t)K <= excl + c0) {
+            cb = 2 * lane;
+            before = excl;
+        } else if (excl + c0 < (uint32_t)K && (uint32_t)K <= incl) {
+            cb = 2 * lane + 1;
+            before = excl + c0;
+        }
+        const uint32_t found = __ballot_sync(0xffffffffu, cb >= 0);
+        const int src = found ? __ffs(found) - 1 : 0;
+        cb = __shfl_sync(0xffffffffu, cb, src);
+        before = __shfl_sync(0xffffffffu, before, src);
+        if (!found) cb = kCoarseBins - 1, before = 0;
+        // the fine bins of that coarse bin
+        const uint32_t f0 = __ldcg(fine + cb * 64 + 2 * lane), f1 = __ldcg(fine + cb * 64 + 2 * lane + 1);
+        uint32_t fin = f0 + f1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, fin, o);
+            if (lane >= o) fin += t;
+        }
+        const uint32_t fex = before + fin - f0 - f1;
+        int fb = -1;
+        if (fex < (uint32_t)K && (uint32_t)K <= fex + f0)
+            fb = cb * 64 + 2 * lane;
+        else if (fex + f0 < (uint32_t)K && (uint32_t)K <= before + fin)
+            fb = cb * 64 + 2 * lane + 1;
+        const uint32_t ff = __ballot_sync(0xffffffffu, fb >= 0);
+        fb = __shfl_sync(0xffffffffu, fb, ff ? __ffs(ff) - 1 : 0);
+        if (lane == 0) *s_out = ff ? fb : kHistBins - 1;
     }
     __syncthreads();
     return *s_out;
 }
 
+constexpr int kFilterPerThread = 4;  // scores per thread (regions_per_cta = 1024)
+
 __global__ void __launch_bounds__(kSplitThreads) filter_kernel(ScoreParams p) {
-    __shared__ int s_part[kSplitThreads / 32];
+    __shared__ uint32_t s_wcnt[kSplitThreads / 32];
+    __shared__ uint32_t s_base;
     __shared__ int s_bin;
     const int g = blockIdx.y, n = blockIdx.z;
+    STEP5_STAMP(2, 0);
     pdl_wait();
+    pdl_launch_dependents();
+    STEP5_STAMP(2, 1);
     int b, pos;
     const int R = row_regions(p, n, b, pos);
     if (R < 0) return;
@@ -416,64 +633,138 @@ __global__ void __launch_bounds__(kSplitThreads) filter_kernel(ScoreParams p) {
     const int c1 = min(R, c0 + p.regions_per_cta);
     if (c0 >= c1) return;
     const int64_t ng = (int64_t)n * p.G + g;
-    const int b1 = threshold_bin(p.hist + ng * kHistBins, R, p.top_k, s_part, &s_bin);
     const float* scores = p.scores + ng * p.r_cap;
-    uint64_t* cand = p.cand + ng * kCandCap;
-    const int lane = threadIdx.x & 31;
-    for (int r0 = c0; r0 < c1; r0 += kSplitThreads) {
-        const int r = r0 + threadIdx.x;
-        bool act = false;
-        uint32_t key = 0;
-        if (r < c1) {
-            key = desc_key(scores[r]);
-            act = (int)(key >> (32 - kHistBits)) <= b1;
+    // every score of the block is requested at once
+    float sc[kFilterPerThread];
+#pragma unroll
+    for (int u = 0; u < kFilterPerThread; ++u) {
+        const int r = c0 + u * kSplitThreads + threadIdx.x;
+        sc[u] = r < c1 ? __ldcg(scores + r) : 0.0f;
+    }
+    const int b1 = threshold_bin2(p.coarse + ng * kCoarseBins, p.hist + ng * kHistBins, R, p.top_k, &s_bin);
+    STEP5_STAMP(2, 2);
+    uint32_t mine = 0, keys[kFilterPerThread];
+#pragma unroll
+    for (int u = 0; u < kFilterPerThread; ++u) {
+        const int r = c0 + u * kSplitThreads + threadIdx.x;
+        keys[u] = desc_key(sc[u]);
+        if (r < c1 && (int)(keys[u] >> (32 - kHistBits)) <= b1) ++mine;
+    }
+    // one atomic per block: block-wide exclusive scan of the per-thread counts
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_wcnt[warp] = incl;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t tot = 0;
+        for (int w = 0; w < kSplitThreads / 32; ++w) {
+            const uint32_t c = s_wcnt[w];
+            s_wcnt[w] = tot;
+            tot += c;
         }
-        const uint32_t am = __ballot_sync(0xffffffffu, act);
-        uint32_t slot = 0;
-        if (lane == 0 && am) slot = atomicAdd(p.cand_count + ng, (uint32_t)__popc(am));
-        slot = __shfl_sync(0xffffffffu, slot, 0);
-        if (act) {
-            const uint32_t idx = slot + __popc(am & ((1u << lane) - 1u));
-            if (idx < (uint32_t)kCandCap) cand[idx] = ((uint64_t)key << 32) | (uint32_t)r;
+        s_base = tot ? atomicAdd(p.cand_count + ng, tot) : 0u;
+    }
+    __syncthreads();
+    STEP5_STAMP(2, 3);
+    uint32_t slot = s_base + s_wcnt[warp] + incl - mine;
+    uint64_t* cand = p.cand + ng * kCandCap;
+#pragma unroll
+    for (int u = 0; u < kFilterPerThread; ++u) {
+        const int r = c0 + u * kSplitThreads + threadIdx.x;
+        if (r < c1 && (int)(keys[u] >> (32 - kHistBits)) <= b1) {
+            if (slot < (uint32_t)kCandCap) cand[slot] = ((uint64_t)keys[u] << 32) | (uint32_t)r;
+            ++slot;
         }
     }
-    pdl_launch_dependents();
 }
 
 constexpr int kFinalThreads = 512;
+constexpr int kFinalSlices = 8;  // blocks per (row, group) in the final select
 
+// Final select of the split path: kFinalSlices blocks per (row, group) each gather the
+// same k winners from the candidate list (radix descent in shared memory), then each
+// places only the winners whose id falls in its slice (id mod kFinalSlices), at the rank
+// it counts among all winners.  The last slice to finish reading the candidates leaves
+// the histogram, candidate counter and ticket of its (row, group) zero for the next call.
 __global__ void __launch_bounds__(kFinalThreads) final_select_kernel(ScoreParams p, int P2, int /*unused*/) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint64_t* s_sel = reinterpret_cast<uint64_t*>(smem);
     uint64_t* s_cand = s_sel + P2;  // kCandCap
     __shared__ TopkSmem ts;
-    const int g = blockIdx.x, n = blockIdx.y;
+    __shared__ int s_last;
+    const int slice = blockIdx.x, g = blockIdx.y, n = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    STEP5_STAMP(3, 0);
     pdl_wait();
+    pdl_launch_dependents();
+    STEP5_STAMP(3, 1);
     int b, pos;
     int R = row_regions(p, n, b, pos);
     if (R < 0) R = 0;
     const int64_t ng = (int64_t)n * p.G + g;
-    const int c = (int)p.cand_count[ng];
-    int take;
-    if (c <= kCandCap) {
-        const uint64_t* cand = p.cand + ng * kCandCap;
-        for (int i = threadIdx.x; i < c; i += kFinalThreads) s_cand[i] = __ldcg(cand + i);
-        __syncthreads();
-        take = block_topk<kFinalThreads>(CandKeys{s_cand}, c, p.top_k, P2, s_sel, ts);
-    } else {
-        take = block_topk<kFinalThreads>(ScoreKeys{p.scores + ng * p.r_cap}, R, p.top_k, P2, s_sel, ts);
-    }
-    pdl_launch_dependents();
-    write_selection<kFinalThreads>(p, n, g, take, s_sel);
-    // leave the histogram and the candidate counter zero for the next call
+    // the whole candidate buffer is requested together with its count
+    const uint64_t* cand = p.cand + ng * kCandCap;
+    uint64_t cv[kCandCap / kFinalThreads];
+#pragma unroll
+    for (int k = 0; k < kCandCap / kFinalThreads; ++k) cv[k] = __ldcg(cand + k * kFinalThreads + tid);
+    const int c = (int)__ldcg(p.cand_count + ng);
+    const bool from_cand = c <= kCandCap;
+#pragma unroll
+    for (int k = 0; k < kCandCap / kFinalThreads; ++k)
+        if (k * kFinalThreads + tid < c) s_cand[k * kFinalThreads + tid] = cv[k];
     __syncthreads();
-    uint32_t* gh = p.hist + ng * kHistBins;
-    for (int i = threadIdx.x; i < kHistBins; i += kFinalThreads) gh[i] = 0;
-    if (threadIdx.x == 0) p.cand_count[ng] = 0;
+    if (tid == 0) {
+        const uint32_t t = atomicAdd(p.ticket + ng, 1u);
+        s_last = (t == (uint32_t)(kFinalSlices - 1));
+    }
+    __syncthreads();
+    if (s_last) {
+        uint32_t* gh = p.hist + ng * kHistBins;
+        for (int i = tid; i < kHistBins; i += kFinalThreads) gh[i] = 0;
+        if (tid < kCoarseBins) p.coarse[ng * kCoarseBins + tid] = 0;
+        if (tid == 0) {
+            p.cand_count[ng] = 0;
+            p.ticket[ng] = 0;
+        }
+    }
+    STEP5_STAMP(3, 2);
+    const int take = from_cand
+                         ? block_select_set<kFinalThreads>(CandKeys{s_cand}, c, p.top_k, P2, s_sel, ts)
+                         : block_select_set<kFinalThreads>(ScoreKeys{p.scores + ng * p.r_cap}, R, p.top_k, P2,
+                                                           s_sel, ts);
+    STEP5_STAMP(3, 3);
+    // rank by counting: one warp per winner of this slice, lanes split the comparisons
+    int32_t* ids = p.sel_ids + ng * p.top_k;
+    float* ss = p.sel_scores ? p.sel_scores + ng * p.top_k : nullptr;
+    for (int i = warp; i < take; i += kFinalThreads / 32) {
+        const uint64_t key = s_sel[i];
+        if ((int)((uint32_t)key % kFinalSlices) != slice) continue;
+        uint32_t cnt_less = 0;
+        for (int j = lane; j < take; j += 32) cnt_less += s_sel[j] < key ? 1u : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt_less += __shfl_xor_sync(0xffffffffu, cnt_less, o);
+        if (lane == 0) {
+            ids[cnt_less] = (int32_t)(uint32_t)(key & 0xffffffffu);
+            if (ss) ss[cnt_less] = score_of_desc_key((uint32_t)(key >> 32));
+        }
+    }
+    STEP5_STAMP(3, 4);
+    if (slice == 0) {
+        for (int i = take + tid; i < p.top_k; i += kFinalThreads) {
+            ids[i] = -1;
+            if (ss) ss[i] = -INFINITY;
+        }
+        if (tid == 0) p.sel_count[ng] = take;
+    }
 }
 
 int pow2_at_least(int x) {
-    int p2 = 1;
+    int p2 = 32;
     while (p2 < x) p2 <<= 1;
     return p2;
 }
@@ -523,9 +814,22 @@ cudaError_t fused_for(const ScoreParams& p, cudaStream_t stream, bool pdl) {
 }
 
 template <int HPG>
-cudaError_t split_for(const ScoreParams& p, cudaStream_t stream, bool pdl) {
-    const int chunks = (p.r_cap + kSplitRegions - 1) / kSplitRegions;
-    cudaError_t e = launch_ex(score_hist_kernel<HPG>, dim3(chunks, p.G, p.N), dim3(kSplitThreads), 0,
+cudaError_t split_for(const ScoreParams& p_in, cudaStream_t stream, bool pdl) {
+    ScoreParams p = p_in;
+    p.chunks_per_ng = (p.r_cap + kTileRegions - 1) / kTileRegions;
+    const int64_t total = (int64_t)p.N * p.G * p.chunks_per_ng;
+    int64_t grid = 2 * (int64_t)p.num_sms;
+    if (grid > total) grid = total;
+    p.items_per_cta = (int)((total + grid - 1) / grid);
+    grid = (total + p.items_per_cta - 1) / p.items_per_cta;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e0 = cudaFuncSetAttribute(score_hist_kernel<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)kScoreSmem);
+        if (e0 != cudaSuccess) return e0;
+        attr = true;
+    }
+    cudaError_t e = launch_ex(score_hist_kernel<HPG>, dim3((unsigned)grid), dim3(kSplitThreads), kScoreSmem,
                               stream, pdl, p);
     if (e != cudaSuccess) return e;
     const int fchunks = (p.r_cap + p.regions_per_cta - 1) / p.regions_per_cta;
@@ -535,8 +839,8 @@ cudaError_t split_for(const ScoreParams& p, cudaStream_t stream, bool pdl) {
     const size_t smem = (size_t)P2 * 8 + (size_t)kCandCap * 8;
     e = cudaFuncSetAttribute(final_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_ex2(final_select_kernel, dim3(p.G, p.N), dim3(kFinalThreads), smem, stream, true, p,
-                      P2, 0);
+    return launch_ex2(final_select_kernel, dim3(kFinalSlices, p.G, p.N), dim3(kFinalThreads), smem, stream, true,
+                      p, P2, 0);
 }
 
 }  // namespace

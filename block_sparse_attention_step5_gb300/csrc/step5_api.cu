@@ -52,54 +52,59 @@ uint32_t* status_ptr() {
     return ptr[dev];
 }
 
+int num_sms() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
 // ------------------------------------------------------------------ workspace layout
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// How step (4) splits a row's (top_k + 1)-entry key list: enough blocks to cover the
-// GPU about twice, each split a whole number of 16-token pairs for each of the 4 warps;
-// the splits of one (row, group) are grouped into clusters of up to 8 blocks that merge
-// on chip, so only one partial state per cluster goes through global memory.
-void attn_splits(const step5_geometry* g, int N, int* splits_out, int* eps_out, int* cluster_out) {
-    const int emax = g->top_k + 1;
+// How step (4) splits a row's (top_k + 1)-entry key list: with fewer (row, group) pairs
+// than SMs, each pair gets a cluster of `cluster` blocks (a power of two up to 16, one
+// block per SM) whose shared memory fits and whose whole grid is resident at once;
+// otherwise one block per pair.  Each block takes `eps` entries (whole pairs).
+void attn_plan(const step5_geometry* g, int N, int* cluster_out, int* eps_out, bool query_device) {
+    const int E = g->top_k + 1;
     const int64_t items = (int64_t)N * g->num_kv_groups;
-    auto eps_for = [&](int64_t splits) {
-        int64_t e = (emax + splits - 1) / splits;
-        e = (e + 7) / 8 * 8;
-        return e < 8 ? (int64_t)8 : e;
-    };
-    int64_t splits = (2 * 152 + items - 1) / items;
-    if (splits < 1) splits = 1;
-    int64_t eps = eps_for(splits);
-    splits = (emax + eps - 1) / eps;
-    int64_t cluster = 1;
-    while (cluster * 2 <= kMaxCluster && cluster * 2 <= splits) cluster *= 2;
-    splits = (splits + cluster - 1) / cluster * cluster;
-    if (splits > kMaxSplits) splits = kMaxSplits / cluster * cluster;
-    eps = eps_for(splits);
-    *splits_out = (int)splits;
-    *eps_out = (int)eps;
-    *cluster_out = (int)cluster;
+    const int hq_g = g->num_q_heads / g->num_kv_groups;
+    const int sms = query_device ? num_sms() : 152;
+    int cluster = 1;
+    if (items < sms) {
+        const int per_item = (int)(sms / items);
+        while (cluster * 2 <= kMaxCluster && cluster * 2 <= per_item) cluster *= 2;
+        while (cluster > 1 && attention_smem_bytes(cluster, hq_g) > 232448) cluster /= 2;
+        if (query_device)
+            while (cluster > 1 && attention_max_active_clusters(cluster, hq_g) < items) cluster /= 2;
+    }
+    int eps = (E + cluster - 1) / cluster;
+    eps = (eps + 1) / 2 * 2;
+    *cluster_out = cluster;
+    *eps_out = eps;
 }
 
-// One workspace serves both calls.  Everything that does not depend on r_cap comes
-// first (the zero-maintained histogram and counters, then the attention partials), so
-// step (4), which does not know r_cap, finds its part at the same offsets.
+// Workspace of step (2)-(3).  The zero-maintained parts (histograms and counters) come
+// first.
 struct Layout {
-    size_t hist, cand_count, attn_counter, partial, scores, cand, end;
+    size_t hist, cand_count, ticket, coarse, scores, cand, end;
 };
 
 Layout layout(const step5_geometry* g, int N, int r_cap) {
     Layout L;
     const int G = g->num_kv_groups;
     const size_t ng = (size_t)N * G;
-    int splits, eps, cluster;
-    attn_splits(g, N, &splits, &eps, &cluster);
-    const size_t partial_bytes = splits > cluster ? ng * (size_t)(splits / cluster) * (g->num_q_heads / G) * 130 * 4 : 0;
     L.hist = 0;
     L.cand_count = align256(L.hist + ng * kHistBins * 4);
-    L.attn_counter = align256(L.cand_count + ng * 4);
-    L.partial = align256(L.attn_counter + ng * 4);
-    L.scores = align256(L.partial + partial_bytes);
+    L.ticket = align256(L.cand_count + ng * 4);
+    L.coarse = align256(L.ticket + ng * 4);
+    L.scores = align256(L.coarse + ng * kCoarseBins * 4);
     L.cand = align256(L.scores + ng * (size_t)(r_cap > 0 ? r_cap : 0) * 4);
     L.end = align256(L.cand + ng * kCandCap * 8);
     return L;
@@ -162,6 +167,7 @@ bool cache_maps(const void* kptr, const void* vptr, uint64_t rows, CUtensorMap* 
 
 bool use_pdl() { return true; }
 
+
 // Fused (one block per (row, group), keys in shared memory) when there are many rows or
 // few regions; the histogram split path when a few rows have many regions.
 bool choose_fused(const step5_geometry* geom, int N, int r_cap) {
@@ -184,9 +190,20 @@ bool choose_fused(const step5_geometry* geom, int N, int r_cap) {
 }  // namespace
 }  // namespace step5
 
+#ifdef STEP5_TRACE
+__device__ unsigned long long* step5::g_trace = nullptr;
+#endif
+
 using namespace step5;
 
 extern "C" {
+
+#ifdef STEP5_TRACE
+// Trace builds only: registers the device buffer the phase stamps go to (NULL stops).
+int step5_trace_buffer(void* device_buffer) {
+    return (int)cudaMemcpyToSymbol(g_trace, &device_buffer, sizeof(device_buffer));
+}
+#endif
 
 const char* step5_status_string(step5_status s) {
     switch (s) {
@@ -320,6 +337,9 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     p.hist = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.hist);
     p.cand_count = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.cand_count);
     p.cand = fused ? nullptr : reinterpret_cast<uint64_t*>(ws + L.cand);
+    p.ticket = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.ticket);
+    p.coarse = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.coarse);
+    p.num_sms = num_sms();
     p.status = st;
     p.N = N;
     p.B = B;
@@ -330,16 +350,7 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     p.r_cap = r_cap;
     p.rope_dims = rope_cos_bf16 ? geom->rope_dims : 0;
     p.top_k = geom->top_k;
-    // split path: enough blocks per (row, group) to cover the GPU about four times over
-    {
-        const int64_t want_ctas = 4 * 152;
-        int64_t per = (int64_t)N * G;
-        int64_t chunks = (want_ctas + per - 1) / per;
-        int64_t rpc = (r_cap + chunks - 1) / chunks;
-        rpc = (rpc + 255) / 256 * 256;
-        if (rpc < 256) rpc = 256;
-        p.regions_per_cta = (int)rpc;
-    }
+    p.regions_per_cta = 1024;  // filter pass: 4 scores per thread
     cudaError_t e = fused ? launch_score_fused(p, (cudaStream_t)stream, use_pdl())
                           : launch_score_split(p, (cudaStream_t)stream, use_pdl());
     return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
@@ -362,18 +373,14 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
     if (rows > (uint64_t)INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
     const int hq_g = geom->num_q_heads / G;
 
-    int splits, eps, cluster;
-    attn_splits(geom, N, &splits, &eps, &cluster);
-    const Layout L = layout(geom, N, 0);
-    if (splits > cluster) {
-        if (workspace == nullptr) return STEP5_ERR_WORKSPACE;
-        if (workspace_bytes < L.scores) return STEP5_ERR_WORKSPACE;
-    }
     uint32_t* st = status_ptr();
     if (!st) return STEP5_ERR_CUDA;
+    int cluster, eps;
+    attn_plan(geom, N, &cluster, &eps, true);
     CUtensorMap kmap, vmap;
     if (!cache_maps(k_cache_bf16, v_cache_bf16, rows, &kmap, &vmap)) return STEP5_ERR_CUDA;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    (void)workspace;
+    (void)workspace_bytes;
     AttnParams p;
     p.q = static_cast<const uint16_t*>(q_bf16);
     p.row_seq = row_seq;
@@ -381,8 +388,6 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
     p.sel_ids = sel_ids;
     p.sel_count = sel_count;
     p.out = static_cast<uint16_t*>(out_bf16);
-    p.partial = splits > cluster ? reinterpret_cast<float*>(ws + L.partial) : nullptr;
-    p.counter = splits > cluster ? reinterpret_cast<uint32_t*>(ws + L.attn_counter) : nullptr;
     p.status = st;
     p.N = N;
     p.B = B;
@@ -391,7 +396,7 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
     p.hq_g = hq_g;
     p.t_cap = t_cap;
     p.top_k = geom->top_k;
-    p.splits = splits;
+    p.splits = cluster;
     p.entries_per_split = eps;
     p.cluster = cluster;
     p.scale_log2 = geom->softmax_scale * 1.4426950408889634f;

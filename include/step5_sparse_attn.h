@@ -132,7 +132,8 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
  * step5_index_score_topk (ids must be distinct candidates of the row, < o);
  * out_bf16: [N][num_q_heads][head_dim].  Cache rows past p are never read into the
  * result (they may hold anything).  t_cap must be a multiple of region_tokens; pointers
- * 16-byte aligned. */
+ * 16-byte aligned.  workspace / workspace_bytes: not used by this call (may be NULL / 0);
+ * the splits of a row merge on chip. */
 step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
                                int32_t t_cap, const void* q_bf16,
                                const void* k_cache_bf16, const void* v_cache_bf16,
@@ -141,8 +142,8 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
                                void* out_bf16, void* workspace, size_t workspace_bytes,
                                step5_stream_t stream);
 
-/* Bytes of device workspace that step5_index_score_topk and step5_sparse_attn need for
- * N rows and r_cap summary slots (one workspace serves both calls on one stream).
+/* Bytes of device workspace that step5_index_score_topk needs for N rows and r_cap
+ * summary slots (the same buffer may be passed to step5_sparse_attn, which ignores it).
  * Returns 0 for an unsupported geometry. */
 size_t step5_workspace_bytes(const step5_geometry* geom, int32_t N, int32_t r_cap);
 
