@@ -26,6 +26,7 @@ from ._build import LIB, build  # noqa: F401
 __all__ = [
     "Step5Error", "Geometry", "STEP5_GEOMETRY", "library_path", "load",
     "step5_region_summarize", "step5_index_score_topk", "step5_sparse_attn",
+    "step5_index_score_topk_noalloc",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
     "step5_set_select_path", "step5_select_path_for", "step5_status_string", "step5_convert_bf16_to_e4m3",
     "Workspace", "decode_step",
@@ -89,6 +90,8 @@ def load():
         "step5_index_score_topk": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P,
                                          P, sz, P]),
         "step5_sparse_attn": (i32, [G, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]),
+        "step5_index_score_topk_noalloc": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P,
+                                                 P, P, P]),
         "step5_workspace_bytes": (sz, [G, i32, i32]),
         "step5_workspace_init": (i32, [P, sz, P]),
         "step5_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32), P]),
@@ -189,6 +192,18 @@ def step5_index_score_topk(geom, idx_q, w, row_seq, row_pos, cos, sin, summaries
         _ptr(row_seq), _ptr(row_pos), _ptr(cos), _ptr(sin), _ptr(summaries), _ptr(sel_ids),
         _ptr(sel_count), _ptr(scores), _ptr(sel_scores), _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def step5_index_score_topk_noalloc(geom, idx_q, w, row_seq, row_pos, cos, sin, summaries, sel_ids,
+                                   sel_count, t_cap, scores=None, sel_scores=None, stream=None):
+    """step5_index_score_topk with the library's fixed 4 MiB scratch instead of a caller
+    workspace, for callers that cannot allocate device memory (see the header)."""
+    N = idx_q.shape[0]
+    B, _, r_cap, _ = summaries.shape
+    _check("step5_index_score_topk_noalloc", load().step5_index_score_topk_noalloc(
+        ctypes.byref(Geometry.of(geom)), N, B, int(t_cap), r_cap, _ptr(idx_q), _ptr(w),
+        _ptr(row_seq), _ptr(row_pos), _ptr(cos), _ptr(sin), _ptr(summaries), _ptr(sel_ids),
+        _ptr(sel_count), _ptr(scores), _ptr(sel_scores), _stream(stream)))
 
 
 def step5_sparse_attn(geom, q, k_cache, v_cache, row_seq, row_pos, sel_ids, sel_count, out,

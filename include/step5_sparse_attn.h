@@ -121,6 +121,31 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
                                     void* workspace, size_t workspace_bytes,
                                     step5_stream_t stream);
 
+/* Steps (2) and (3) without a caller-provided workspace (the paper has no counterpart:
+ * this is a deployment variant).  For callers that cannot allocate device memory -- code
+ * whose device allocations all belong to a host framework, or a path where no allocator
+ * is reachable or allocating would synchronise the device -- this call takes the same
+ * inputs and outputs as step5_index_score_topk and keeps its scratch in a fixed 4 MiB
+ * array of static device memory inside the library (one per device that loads it,
+ * held until the process exits).  It allocates nothing.
+ *  - Limit: step5_workspace_bytes(geom, N, r_cap) must be at most 4 MiB (for Step-5's
+ *    geometry about N * r_cap <= 220,000, e.g. one row at 1M tokens or four at 128K);
+ *    larger problems return STEP5_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device looks up the array's device address (with that device
+ *    current); make that first call before any stream capture.
+ *  - Each call clears the part of the array it uses (an enqueued memset), since the
+ *    array keeps the previous call's contents.  All calls share the one array: calls
+ *    whose executions overlap on the GPU (other streams, other threads) race. */
+step5_status step5_index_score_topk_noalloc(const step5_geometry* geom, int32_t N, int32_t B,
+                                            int32_t t_cap, int32_t r_cap,
+                                            const void* idx_q_bf16, const float* w,
+                                            const int32_t* row_seq, const int32_t* row_pos,
+                                            const void* rope_cos_bf16, const void* rope_sin_bf16,
+                                            const uint8_t* summaries_e4m3,
+                                            int32_t* sel_ids, int32_t* sel_count,
+                                            float* scores_or_null, float* sel_scores_or_null,
+                                            step5_stream_t stream);
+
 /* Step (4): attention over the picked regions plus the row's own region.
  * For every row n, query head h of KV group g = h / (num_q_heads / G):
  *   keys  = tokens 8r .. 8r+7 of every r in sel_ids[n][g][0 .. sel_count[n][g]),
