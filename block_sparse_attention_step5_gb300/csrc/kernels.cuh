@@ -52,10 +52,12 @@ struct ScoreParams {
     uint32_t* status;
     int N, B, G, idx_heads, hpg, t_cap, r_cap, rope_dims, top_k;
     int regions_per_cta;     // split path: regions filtered by one block
-    int chunks_per_ng, items_per_cta, num_sms;  // split path: persistent scoring blocks
+    int num_sms;             // split path: persistent scoring blocks (two per SM)
 };
 cudaError_t launch_score_fused(const ScoreParams& p, cudaStream_t stream, bool pdl);
-cudaError_t launch_score_split(const ScoreParams& p, cudaStream_t stream, bool pdl);
+// smap: 2-D tensor map of the summaries, [B*G*r_cap rows][64 bytes], box 64 x 256,
+// 64-byte swizzle (used when idx_heads / G == 4).
+cudaError_t launch_score_split(const ScoreParams& p, const CUtensorMap& smap, cudaStream_t stream, bool pdl);
 
 // ----------------------------------------------------------------- step (4)
 constexpr int kAttnWarps = 8;

@@ -33,10 +33,10 @@ struct QFrag {
     float w[HPG];      // w of every head (HPG == 4: w[0] holds head qd's weight)
 };
 
-// e4m3(bf16(NEOX(q))) for the group's HPG heads into shared memory, then each thread
-// keeps the 16 dims it multiplies (qd = lane & 3).
+// e4m3(bf16(NEOX(q))) of the group's HPG heads, as floats, into s_q[h * 64 + d].  Ends
+// with a __syncthreads.
 template <int HPG>
-__device__ void load_qfrag(const ScoreParams& p, int n, int g, int pos, float* s_q, QFrag<HPG>& f) {
+__device__ void stage_query(const ScoreParams& p, int n, int g, int pos, float* s_q) {
     const int half = p.rope_dims >> 1;
     for (int i = threadIdx.x; i < HPG * 64; i += blockDim.x) {
         const int h = i >> 6, d = i & 63;
@@ -52,17 +52,86 @@ __device__ void load_qfrag(const ScoreParams& p, int n, int g, int pos, float* s
         }
         s_q[i] = e4m3x2_to_f32x2(f32_to_e4m3(bf16_to_f32(rb))).x;
     }
+    __syncthreads();
+}
+
+// The staged query into registers for the 4-lanes-per-region layout: each thread keeps
+// the 16 dims it multiplies (qd = lane & 3).
+template <int HPG>
+__device__ void load_qfrag(const ScoreParams& p, int n, int g, int pos, float* s_q, QFrag<HPG>& f) {
     const int qd = threadIdx.x & 3;
 #pragma unroll
     for (int h = 0; h < HPG; ++h) f.w[h] = p.w[(int64_t)n * p.idx_heads + (int64_t)g * HPG + h];
     if constexpr (HPG == 4) f.w[0] = p.w[(int64_t)n * p.idx_heads + (int64_t)g * HPG + qd];
-    __syncthreads();
+    stage_query<HPG>(p, n, g, pos, s_q);
 #pragma unroll
     for (int h = 0; h < HPG; ++h) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             f.q[h][i] = make_float2(s_q[h * 64 + 16 * qd + 2 * i], s_q[h * 64 + 16 * qd + 2 * i + 1]);
     }
+}
+
+// ----------------------------------------------------------------- one thread per region
+//
+// For 4 indexer heads per group: a thread scores whole regions (64 dims, 4 heads), two at
+// a time, so no cross-lane reduction is needed.  The query lives in shared memory as
+// q4[2 * pair + hp] = (q_{2hp}[2 pair], q_{2hp}[2 pair + 1], q_{2hp+1}[2 pair],
+// q_{2hp+1}[2 pair + 1]); every lane reads the same element (broadcast) and one query
+// load serves both regions.
+
+// Rearranges s_q [4][64] into q4 [64]; ends with a __syncthreads.
+__device__ __forceinline__ void build_q4(const float* s_q, float4* q4) {
+    if (threadIdx.x < 64) {
+        const int pr = threadIdx.x >> 1, hp = threadIdx.x & 1;
+        q4[threadIdx.x] = make_float4(s_q[(2 * hp) * 64 + 2 * pr], s_q[(2 * hp) * 64 + 2 * pr + 1],
+                                      s_q[(2 * hp + 1) * 64 + 2 * pr], s_q[(2 * hp + 1) * 64 + 2 * pr + 1]);
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ float finish_score4(const float2 (&acc)[4], const float (&w)[4]) {
+    float sc = 0.0f;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) sc = fmaf(fmaxf(__fadd_rn(acc[h].x, acc[h].y), 0.0f), w[h], sc);
+    return __fadd_rn(sc, 0.0f);  // -0 -> +0
+}
+
+// Scores of two regions whose 64 summary bytes are a[0..3] and b[0..3] (dims 16k..16k+15
+// in chunk k).  Each head's dot product is the sum of an even-dim and an odd-dim partial
+// sum, accumulated in dim order.
+__device__ __forceinline__ void score_rows2(const uint4 (&a)[4], const uint4 (&b)[4], const float4* q4,
+                                            const float (&w)[4], float& sa, float& sb) {
+    float2 A[4], Bc[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) A[h] = Bc[h] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t wa[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+        const uint32_t wb[4] = {b[k].x, b[k].y, b[k].z, b[k].w};
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const int p0 = 8 * k + 2 * qq;
+#pragma unroll
+            for (int hw = 0; hw < 2; ++hw) {  // low / high 16 bits: pair p0 / p0 + 1
+                const float2 xa = e4m3x2_to_f32x2((uint16_t)(hw ? wa[qq] >> 16 : wa[qq] & 0xffffu));
+                const float2 xb = e4m3x2_to_f32x2((uint16_t)(hw ? wb[qq] >> 16 : wb[qq] & 0xffffu));
+                const float4 q01 = q4[2 * (p0 + hw)], q23 = q4[2 * (p0 + hw) + 1];
+                const float2 q0 = make_float2(q01.x, q01.y), q1 = make_float2(q01.z, q01.w);
+                const float2 q2 = make_float2(q23.x, q23.y), q3 = make_float2(q23.z, q23.w);
+                A[0] = __ffma2_rn(q0, xa, A[0]);
+                A[1] = __ffma2_rn(q1, xa, A[1]);
+                A[2] = __ffma2_rn(q2, xa, A[2]);
+                A[3] = __ffma2_rn(q3, xa, A[3]);
+                Bc[0] = __ffma2_rn(q0, xb, Bc[0]);
+                Bc[1] = __ffma2_rn(q1, xb, Bc[1]);
+                Bc[2] = __ffma2_rn(q2, xb, Bc[2]);
+                Bc[3] = __ffma2_rn(q3, xb, Bc[3]);
+            }
+        }
+    }
+    sa = finish_score4(A, w);
+    sb = finish_score4(Bc, w);
 }
 
 // Score of the region whose 16 dims [16*qd, 16*qd + 16) this thread holds in v.  All
@@ -347,30 +416,57 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
         b = 0;
         pos = 0;
     }
-    QFrag<HPG> f;
-    load_qfrag<HPG>(p, n, g, pos, s_q, f);
-
-    const int qd = threadIdx.x & 3;
-    const int slot = threadIdx.x >> 2;  // 64 regions per pass
     const uint4* base = reinterpret_cast<const uint4*>(p.summ + ((int64_t)b * p.G + g) * p.r_cap * 64);
     float* exp_scores = p.scores ? p.scores + ((int64_t)n * p.G + g) * p.r_cap : nullptr;
-    constexpr int U = 4;
-    for (int r0 = 0; r0 < R; r0 += 64 * U) {
-        uint4 v[U];
+    if constexpr (HPG == 4) {
+        __shared__ float4 s_q4[64];
+        float w[4];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int r = r0 + u * 64 + slot;
-            v[u] = (r < R) ? __ldg(base + (int64_t)r * 4 + qd) : make_uint4(0, 0, 0, 0);
+        for (int h = 0; h < 4; ++h) w[h] = p.w[(int64_t)n * p.idx_heads + (int64_t)g * 4 + h];
+        stage_query<4>(p, n, g, pos, s_q);
+        build_q4(s_q, s_q4);
+        for (int r0 = 0; r0 < R; r0 += 2 * kFusedThreads) {
+            const int ra = r0 + threadIdx.x, rb = ra + kFusedThreads;
+            uint4 va[4], vb[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                va[k] = ra < R ? __ldg(base + (int64_t)ra * 4 + k) : make_uint4(0, 0, 0, 0);
+                vb[k] = rb < R ? __ldg(base + (int64_t)rb * 4 + k) : make_uint4(0, 0, 0, 0);
+            }
+            float sa, sb;
+            score_rows2(va, vb, s_q4, w, sa, sb);
+            if (ra < R) {
+                s_key[ra] = desc_key(sa);
+                if (exp_scores) exp_scores[ra] = sa;
+            }
+            if (rb < R) {
+                s_key[rb] = desc_key(sb);
+                if (exp_scores) exp_scores[rb] = sb;
+            }
         }
-        float sc[U];
+    } else {
+        QFrag<HPG> f;
+        load_qfrag<HPG>(p, n, g, pos, s_q, f);
+        const int qd = threadIdx.x & 3;
+        const int slot = threadIdx.x >> 2;  // 64 regions per pass
+        constexpr int U = 4;
+        for (int r0 = 0; r0 < R; r0 += 64 * U) {
+            uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) sc[u] = score_from_vec<HPG>(f, v[u]);
-        // lane qd keeps the bookkeeping of region u = qd
-        const float mysc = qd == 0 ? sc[0] : qd == 1 ? sc[1] : qd == 2 ? sc[2] : sc[3];
-        const int r = r0 + qd * 64 + slot;
-        if (r < R) {
-            s_key[r] = desc_key(mysc);
-            if (exp_scores) exp_scores[r] = mysc;
+            for (int u = 0; u < U; ++u) {
+                const int r = r0 + u * 64 + slot;
+                v[u] = (r < R) ? __ldg(base + (int64_t)r * 4 + qd) : make_uint4(0, 0, 0, 0);
+            }
+            float sc[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) sc[u] = score_from_vec<HPG>(f, v[u]);
+            // lane qd keeps the bookkeeping of region u = qd
+            const float mysc = qd == 0 ? sc[0] : qd == 1 ? sc[1] : qd == 2 ? sc[2] : sc[3];
+            const int r = r0 + qd * 64 + slot;
+            if (r < R) {
+                s_key[r] = desc_key(mysc);
+                if (exp_scores) exp_scores[r] = mysc;
+            }
         }
     }
     __syncthreads();
@@ -401,32 +497,44 @@ struct Tile {
     int valid, ng, n, g, b, pos, R, c0, c1;
 };
 
-// Tile `t` of the flattened (row, group, tile) space, with its row's geometry;
-// invalid when the row is out of range or the tile starts past its candidates.
-__device__ __forceinline__ Tile tile_at(const ScoreParams& p, int t) {
-    Tile x;
-    x.valid = 0;
-    const int ng = t / p.chunks_per_ng;
-    const int chunk = t - ng * p.chunks_per_ng;
-    const int n = ng / p.G;
-    int b, pos;
-    const int R = row_regions(p, n, b, pos);
-    if (R < 0) {
-        if (chunk == 0 && threadIdx.x == 0) raise_status(p.status, kDevRange);
-        return x;
+// The next tile of this block's range [x, hi) of the flattened (row, group, region)
+// space (r_cap regions per (row, group)): at most kTileRegions consecutive candidate
+// regions of one (row, group).  Regions past a row's R, and rows out of range, are
+// skipped.  Advances x past the tile.
+__device__ __forceinline__ Tile next_tile(const ScoreParams& p, int64_t& x, int64_t hi) {
+    Tile t;
+    t.valid = 0;
+    while (x < hi) {
+        const int ng = (int)(x / p.r_cap);
+        const int r = (int)(x - (int64_t)ng * p.r_cap);
+        const int n = ng / p.G;
+        int b, pos;
+        const int R = row_regions(p, n, b, pos);
+        if (R < 0) {
+            if (threadIdx.x == 0) raise_status(p.status, kDevRange);
+            x = (int64_t)(ng + 1) * p.r_cap;
+            continue;
+        }
+        if (r >= R) {
+            x = (int64_t)(ng + 1) * p.r_cap;
+            continue;
+        }
+        int c1 = min(R, r + kTileRegions);
+        const int64_t lim = hi - (int64_t)ng * p.r_cap;
+        if ((int64_t)c1 > lim) c1 = (int)lim;
+        t.valid = 1;
+        t.ng = ng;
+        t.n = n;
+        t.g = ng - n * p.G;
+        t.b = b;
+        t.pos = pos;
+        t.R = R;
+        t.c0 = r;
+        t.c1 = c1;
+        x = (int64_t)ng * p.r_cap + c1;
+        return t;
     }
-    const int c0 = chunk * kTileRegions;
-    if (c0 >= R) return x;
-    x.valid = 1;
-    x.ng = ng;
-    x.n = n;
-    x.g = ng - n * p.G;
-    x.b = b;
-    x.pos = pos;
-    x.R = R;
-    x.c0 = c0;
-    x.c1 = min(R, c0 + kTileRegions);
-    return x;
+    return t;
 }
 
 // Scores one staged tile: thread (slot, qd) covers regions u * 64 + slot, u < kTileU;
@@ -453,8 +561,37 @@ __device__ __forceinline__ void score_tile(const QFrag<HPG>& f, const uint4* til
     }
 }
 
+// One thread per region (HPG == 4): thread t scores rows t and t + 256 of a tile that
+// arrived as two 256-row boxes through the summaries' tensor map with 64-byte swizzle
+// (16-byte chunk k of row r sits at chunk k ^ ((r >> 1) & 3)), so the 8 rows a quarter
+// warp reads at once fall in 8 different bank groups.
+__device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, const float4* q4,
+                                                const float (&w)[4], float* scores, uint32_t* s_hist) {
+    const int t = threadIdx.x;  // 0..255
+    const int sw = (t >> 1) & 3;
+    const uint4* ra = reinterpret_cast<const uint4*>(tile + t * 64);
+    const uint4* rb = reinterpret_cast<const uint4*>(tile + 16384 + t * 64);
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        a[k] = ra[k ^ sw];
+        b[k] = rb[k ^ sw];
+    }
+    float sa, sb;
+    score_rows2(a, b, q4, w, sa, sb);
+    if (t < nreg) {
+        scores[t] = sa;
+        atomicAdd(&s_hist[desc_key(sa) >> (32 - kHistBits)], 1u);
+    }
+    if (t + 256 < nreg) {
+        scores[t + 256] = sb;
+        atomicAdd(&s_hist[desc_key(sb) >> (32 - kHistBits)], 1u);
+    }
+}
+
 template <int HPG>
-__global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(ScoreParams p) {
+__global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(const __grid_constant__ CUtensorMap smap,
+                                                                      ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint32_t s_hist[kHistBins];
@@ -472,23 +609,25 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(ScoreParam
     pdl_wait();
     pdl_launch_dependents();
     STEP5_STAMP(1, 1);
-    const int total = p.N * p.G * p.chunks_per_ng;
-    const int t0 = blockIdx.x * p.items_per_cta;
-    const int t1 = min(total, t0 + p.items_per_cta);
-
-    int next_t = t0;
-    auto next_valid = [&]() -> Tile {
-        Tile x;
-        x.valid = 0;
-        while (next_t < t1 && !x.valid) x = tile_at(p, next_t++);
-        return x;
-    };
+    // this block's even share of the flattened (row, group, region) space
+    const int64_t total = (int64_t)p.N * p.G * p.r_cap;
+    int64_t xpos = total * blockIdx.x / gridDim.x;
+    const int64_t xend = total * (blockIdx.x + 1) / gridDim.x;
+    auto next_valid = [&]() -> Tile { return next_tile(p, xpos, xend); };
     auto issue = [&](const Tile& x, int st) {
         if (tid == 0) {
-            const uint32_t bytes = (uint32_t)(x.c1 - x.c0) * 64u;
-            mbar_arrive_expect_tx(&s_bar[st], bytes);
-            bulk_load(ring + st * kTileBytes, p.summ + (((int64_t)x.b * p.G + x.g) * p.r_cap + x.c0) * 64,
-                      bytes, &s_bar[st]);
+            if constexpr (HPG == 4) {
+                // two full boxes (rows past the tensor end arrive as zeros)
+                const int y = (int)(((int64_t)x.b * p.G + x.g) * p.r_cap + x.c0);
+                mbar_arrive_expect_tx(&s_bar[st], (uint32_t)kTileBytes);
+                tma_load_2d(ring + st * kTileBytes, &smap, &s_bar[st], 0, y);
+                tma_load_2d(ring + st * kTileBytes + kTileBytes / 2, &smap, &s_bar[st], 0, y + kTileRegions / 2);
+            } else {
+                const uint32_t bytes = (uint32_t)(x.c1 - x.c0) * 64u;
+                mbar_arrive_expect_tx(&s_bar[st], bytes);
+                bulk_load(ring + st * kTileBytes, p.summ + (((int64_t)x.b * p.G + x.g) * p.r_cap + x.c0) * 64,
+                          bytes, &s_bar[st]);
+            }
         }
     };
     // two tiles in flight: `cur` in stage st, `nxt` in stage st ^ 1
@@ -501,6 +640,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(ScoreParam
     int seg_ng = -1;
     int ntile = 0;
     QFrag<HPG> f;
+    __shared__ float4 s_q4[64];
+    float w4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     auto finish = [&](int ng) {
         __syncthreads();
         uint32_t* gh = p.hist + (int64_t)ng * kHistBins;
@@ -526,7 +667,14 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(ScoreParam
             if (seg_ng >= 0) finish(seg_ng);
             seg_ng = cur.ng;
             for (int i = tid; i < kHistBins; i += kSplitThreads) s_hist[i] = 0;
-            load_qfrag<HPG>(p, cur.n, cur.g, cur.pos, s_q, f);  // has a __syncthreads
+            if constexpr (HPG == 4) {
+#pragma unroll
+                for (int h = 0; h < 4; ++h) w4[h] = p.w[(int64_t)cur.n * p.idx_heads + (int64_t)cur.g * 4 + h];
+                stage_query<4>(p, cur.n, cur.g, cur.pos, s_q);
+                build_q4(s_q, s_q4);
+            } else {
+                load_qfrag<HPG>(p, cur.n, cur.g, cur.pos, s_q, f);  // has a __syncthreads
+            }
         }
         if (ntile < 4) STEP5_STAMP(1, 3 + 2 * ntile);
         if (!mbar_wait(&s_bar[st], st ? ph1 : ph0)) {
@@ -536,13 +684,17 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(ScoreParam
         if (ntile < 4) STEP5_STAMP(1, 4 + 2 * ntile);
         ++ntile;
         if (st) ph1 ^= 1u; else ph0 ^= 1u;
-        const uint4* tile = reinterpret_cast<const uint4*>(ring + st * kTileBytes);
         float* scores = p.scores + (int64_t)cur.ng * p.r_cap + cur.c0;
         const int nreg = cur.c1 - cur.c0;
-        if (nreg == kTileRegions)
-            score_tile<HPG, true>(f, tile, nreg, scores, s_hist, qd, slot);
-        else
-            score_tile<HPG, false>(f, tile, nreg, scores, s_hist, qd, slot);
+        if constexpr (HPG == 4) {
+            score_tile_rows(ring + st * kTileBytes, nreg, s_q4, w4, scores, s_hist);
+        } else {
+            const uint4* tile = reinterpret_cast<const uint4*>(ring + st * kTileBytes);
+            if (nreg == kTileRegions)
+                score_tile<HPG, true>(f, tile, nreg, scores, s_hist, qd, slot);
+            else
+                score_tile<HPG, false>(f, tile, nreg, scores, s_hist, qd, slot);
+        }
         __syncthreads();  // every thread is done with this stage before it is refilled
         cur = nxt;
         nxt = next_valid();
@@ -813,15 +965,29 @@ cudaError_t fused_for(const ScoreParams& p, cudaStream_t stream, bool pdl) {
                       (key_cap + 3) & ~3);
 }
 
+template <class K>
+cudaError_t launch_map(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                       const CUtensorMap& map, const ScoreParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, map, p);
+}
+
 template <int HPG>
-cudaError_t split_for(const ScoreParams& p_in, cudaStream_t stream, bool pdl) {
+cudaError_t split_for(const ScoreParams& p_in, const CUtensorMap& smap, cudaStream_t stream, bool pdl) {
     ScoreParams p = p_in;
-    p.chunks_per_ng = (p.r_cap + kTileRegions - 1) / kTileRegions;
-    const int64_t total = (int64_t)p.N * p.G * p.chunks_per_ng;
+    // two persistent blocks per SM, each an even share of the regions
+    const int64_t tiles = ((int64_t)p.N * p.G * p.r_cap + kTileRegions - 1) / kTileRegions;
     int64_t grid = 2 * (int64_t)p.num_sms;
-    if (grid > total) grid = total;
-    p.items_per_cta = (int)((total + grid - 1) / grid);
-    grid = (total + p.items_per_cta - 1) / p.items_per_cta;
+    if (grid > tiles) grid = tiles;
     static bool attr = false;
     if (!attr) {
         cudaError_t e0 = cudaFuncSetAttribute(score_hist_kernel<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -829,8 +995,8 @@ cudaError_t split_for(const ScoreParams& p_in, cudaStream_t stream, bool pdl) {
         if (e0 != cudaSuccess) return e0;
         attr = true;
     }
-    cudaError_t e = launch_ex(score_hist_kernel<HPG>, dim3((unsigned)grid), dim3(kSplitThreads), kScoreSmem,
-                              stream, pdl, p);
+    cudaError_t e = launch_map(score_hist_kernel<HPG>, dim3((unsigned)grid), dim3(kSplitThreads), kScoreSmem,
+                               stream, pdl, smap, p);
     if (e != cudaSuccess) return e;
     const int fchunks = (p.r_cap + p.regions_per_cta - 1) / p.regions_per_cta;
     e = launch_ex(filter_kernel, dim3(fchunks, p.G, p.N), dim3(kSplitThreads), 0, stream, true, p);
@@ -855,12 +1021,12 @@ cudaError_t launch_score_fused(const ScoreParams& p, cudaStream_t stream, bool p
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_score_split(const ScoreParams& p, cudaStream_t stream, bool pdl) {
+cudaError_t launch_score_split(const ScoreParams& p, const CUtensorMap& smap, cudaStream_t stream, bool pdl) {
     switch (p.hpg) {
-        case 1: return split_for<1>(p, stream, pdl);
-        case 2: return split_for<2>(p, stream, pdl);
-        case 4: return split_for<4>(p, stream, pdl);
-        case 8: return split_for<8>(p, stream, pdl);
+        case 1: return split_for<1>(p, smap, stream, pdl);
+        case 2: return split_for<2>(p, smap, stream, pdl);
+        case 4: return split_for<4>(p, smap, stream, pdl);
+        case 8: return split_for<8>(p, smap, stream, pdl);
     }
     return cudaErrorInvalidValue;
 }

@@ -140,6 +140,43 @@ bool encode_cache_map(CUtensorMap* map, const void* base, uint64_t rows) {
     return r == CUDA_SUCCESS;
 }
 
+// 2-D view [rows][64] bytes of the e4m3 summaries; box 64 bytes x 256 rows, 64-byte
+// swizzle.
+bool encode_summary_map(CUtensorMap* map, const void* base, uint64_t rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {64, rows};
+    cuuint64_t strides[1] = {64};
+    cuuint32_t box[2] = {64, 256};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct SummaryMapCache {
+    std::mutex mu;
+    const void* ptr = nullptr;
+    uint64_t rows = 0;
+    CUtensorMap map;
+};
+SummaryMapCache g_smap;
+
+bool cache_summary_map(const void* ptr, uint64_t rows, CUtensorMap* out) {
+    std::lock_guard<std::mutex> lock(g_smap.mu);
+    if (g_smap.ptr != ptr || g_smap.rows != rows) {
+        if (!encode_summary_map(&g_smap.map, ptr, rows)) {
+            g_smap.ptr = nullptr;
+            return false;
+        }
+        g_smap.ptr = ptr;
+        g_smap.rows = rows;
+    }
+    *out = g_smap.map;
+    return true;
+}
+
 struct MapCache {
     std::mutex mu;
     const void* kptr = nullptr;
@@ -166,6 +203,8 @@ bool cache_maps(const void* kptr, const void* vptr, uint64_t rows, CUtensorMap* 
 }
 
 bool use_pdl() { return true; }
+
+constexpr uint64_t kTileRegionsHost = 512;  // regions per scoring tile (score_select.cu)
 
 
 // Fused (one block per (row, group), keys in shared memory) when there are many rows or
@@ -351,8 +390,16 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     p.rope_dims = rope_cos_bf16 ? geom->rope_dims : 0;
     p.top_k = geom->top_k;
     p.regions_per_cta = 1024;  // filter pass: 4 scores per thread
-    cudaError_t e = fused ? launch_score_fused(p, (cudaStream_t)stream, use_pdl())
-                          : launch_score_split(p, (cudaStream_t)stream, use_pdl());
+    cudaError_t e;
+    if (fused) {
+        e = launch_score_fused(p, (cudaStream_t)stream, use_pdl());
+    } else {
+        CUtensorMap smap;
+        const uint64_t srows = (uint64_t)B * G * r_cap;
+        if (srows > (uint64_t)INT32_MAX - kTileRegionsHost) return STEP5_ERR_INVALID_ARGUMENT;
+        if (!cache_summary_map(summaries_e4m3, srows, &smap)) return STEP5_ERR_CUDA;
+        e = launch_score_split(p, smap, (cudaStream_t)stream, use_pdl());
+    }
     return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
 }
 
