@@ -9,10 +9,13 @@
 // Design (sm_103a):
 //  * one thread-block cluster per (row, KV group): its C blocks (1..16) split the row's
 //    key list (picked regions in selection order, then the own region) into runs of
-//    whole 16-token pairs; 8 warps per block, each warp with its own 2-stage pipeline.
+//    whole 16-token pairs; 8 warps per block, each warp with its own pipeline of 2
+//    pair buffers (warp 0: 3, so that the 17 pairs of a block's share of a 513-entry
+//    list split 16 ways are all requested at once).
 //  * a region is a contiguous 2 KB tile of the [B][G][t_cap][128] cache; it is fetched
-//    with two 2-D TMA boxes (64 dims x 8 rows each) into 128-byte-swizzled shared
-//    memory, so the ldmatrix reads below hit 8 distinct bank groups.
+//    with one TMA box of a 3-D view (64 dims x 8 rows x 2 row halves) into two
+//    128-byte-swizzled half tiles, so the ldmatrix reads below hit 8 distinct bank
+//    groups.
 //  * S = Q K^T and O += P V run on bf16 mma.sync (m16n8k16, fp32 accumulate) with the
 //    group's query heads as the 16-row left operand (4, 8 or 16 heads; unused rows are
 //    zero); P is rounded to bf16 for the PV product, the softmax state is fp32.
@@ -29,9 +32,10 @@ namespace {
 constexpr int kThreads = kAttnWarps * 32;
 constexpr int kRegionBytes = 2048;                    // 8 tokens x 128 dims x bf16
 constexpr int kPairBytes = 4 * kRegionBytes;          // K (2 regions) + V (2 regions)
-constexpr int kStageBytes = kAttnWarps * kAttnStages * kPairBytes;
+constexpr int kPairBufs = kAttnWarps * kAttnStages + 1;  // warp 0 has one more
+constexpr int kStageBytes = kPairBufs * kPairBytes;
 constexpr int kMergeFloatsPerWarp = 16 * 128 + 32;    // O[16][128], m[16], l[16]
-constexpr int kBarBytes = kAttnWarps * kAttnStages * 8;
+constexpr int kBarBytes = kPairBufs * 8;
 constexpr int kSlotFloats = 130;                      // m, l, o[128] of one head row
 static_assert(kAttnWarps * kMergeFloatsPerWarp * 4 <= kStageBytes, "warp merge area must fit");
 
@@ -55,7 +59,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = align_smem(smem_raw, 1024);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageBytes);
     float* slots = reinterpret_cast<float*>(smem + kStageBytes + kBarBytes);  // [C][hq_g][130]
 
@@ -74,15 +78,18 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     pdl_launch_dependents();
     STEP5_STAMP(4, 1);
 
-    // the row's position, pick count and this warp's first pair ids, in one round trip
+    // the row's position, pick count and every picked id of this block's run, in one
+    // round trip
+    __shared__ int32_t s_ids[kAttnStaticSmem / 4];
     const int32_t* ids = p.sel_ids + ng * p.top_k;
     const int e0 = split * p.entries_per_split;
-    const int e_first = e0 + 2 * warp;
-    const int32_t id_pref0 = e_first < p.top_k ? __ldg(ids + e_first) : -1;
-    const int32_t id_pref1 = e_first + 1 < p.top_k ? __ldg(ids + e_first + 1) : -1;
+    for (int i = tid; i < p.entries_per_split; i += kThreads)
+        s_ids[i] = e0 + i < p.top_k ? __ldg(ids + e0 + i) : -1;
     const int b = p.row_seq[n];
     const int pos = p.row_pos[n];
     int cnt = p.sel_count[ng];
+    __syncthreads();
+    STEP5_STAMP(4, 8);
     if (b < 0 || b >= p.B || pos < 0 || pos >= p.t_cap) {
         // the same for every block of the cluster: all leave before any cluster barrier
         if (split == 0) {
@@ -104,13 +111,16 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     const int nmy = npairs > warp ? (npairs - warp + kAttnWarps - 1) / kAttnWarps : 0;
     const int64_t row_base = ((int64_t)b * p.G + g) * p.t_cap;
 
-    uint8_t* wstage = smem + warp * kAttnStages * kPairBytes;
-    uint64_t* wbar = bars + warp * kAttnStages;
+    const int nst = warp == 0 ? kAttnStages + 1 : kAttnStages;  // this warp's pair buffers
+    const int wfirst = warp == 0 ? 0 : warp * kAttnStages + 1;
+    uint8_t* wstage = smem + wfirst * kPairBytes;
+    uint64_t* wbar = bars + wfirst;
     if (lane == 0) {
-        for (int st = 0; st < kAttnStages; ++st) mbar_init(&wbar[st], 1);
+        for (int st = 0; st < nst; ++st) mbar_init(&wbar[st], 1);
         fence_mbar_init();
     }
     __syncwarp();
+    STEP5_STAMP(4, 9);
 
     // entry e -> (region id, valid tokens); invalid ids are masked out entirely
     auto entry = [&](int e, int& rid) -> int {
@@ -122,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
             rid = own;
             return own_tokens;
         }
-        rid = e == e_first ? id_pref0 : e == e_first + 1 ? id_pref1 : ids[e];
+        rid = s_ids[e - e0];
         if (rid < 0 || rid >= own) {
             raise_status(p.status, kDevRange);
             rid = -1;
@@ -134,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     auto issue = [&](int li) {
         if (lane != 0) return;
         const int pi = warp + li * kAttnWarps;
-        const int st = li % kAttnStages;
+        const int st = li % nst;
         uint8_t* kt = wstage + st * kPairBytes;
         uint8_t* vt = kt + 2 * kRegionBytes;
         int ra, rb;
@@ -144,21 +154,17 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         mbar_arrive_expect_tx(&wbar[st], bytes);
         if (na > 0) {
             const int y = (int)(row_base + (int64_t)ra * 8);
-            tma_load_2d(kt, &kmap, &wbar[st], 0, y);
-            tma_load_2d(kt + 1024, &kmap, &wbar[st], 64, y);
-            tma_load_2d(vt, &vmap, &wbar[st], 0, y);
-            tma_load_2d(vt + 1024, &vmap, &wbar[st], 64, y);
+            tma_load_3d(kt, &kmap, &wbar[st], 0, y, 0);
+            tma_load_3d(vt, &vmap, &wbar[st], 0, y, 0);
         }
         if (nb > 0) {
             const int y = (int)(row_base + (int64_t)rb * 8);
-            tma_load_2d(kt + kRegionBytes, &kmap, &wbar[st], 0, y);
-            tma_load_2d(kt + kRegionBytes + 1024, &kmap, &wbar[st], 64, y);
-            tma_load_2d(vt + kRegionBytes, &vmap, &wbar[st], 0, y);
-            tma_load_2d(vt + kRegionBytes + 1024, &vmap, &wbar[st], 64, y);
+            tma_load_3d(kt + kRegionBytes, &kmap, &wbar[st], 0, y, 0);
+            tma_load_3d(vt + kRegionBytes, &vmap, &wbar[st], 0, y, 0);
         }
     };
 
-    for (int li = 0; li < kAttnStages && li < nmy; ++li) issue(li);
+    for (int li = 0; li < nst && li < nmy; ++li) issue(li);
     STEP5_STAMP(4, 2);
 
     // query heads of the group as the A operand (rows >= hq_g are zero)
@@ -185,13 +191,13 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     int li_fail = -1;
     for (int li = 0; li < nmy; ++li) {
         const int pi = warp + li * kAttnWarps;
-        const int st = li % kAttnStages;
+        const int st = li % nst;
         uint8_t* kt = wstage + st * kPairBytes;
         uint8_t* vt = kt + 2 * kRegionBytes;
         int ra, rb;
         const int na = entry(e0 + 2 * pi, ra);
         const int nb = entry(e0 + 2 * pi + 1, rb);
-        if (!mbar_wait(&wbar[st], (uint32_t)((li / kAttnStages) & 1))) {
+        if (!mbar_wait(&wbar[st], (uint32_t)((li / nst) & 1))) {
             li_fail = li;
             break;
         }
@@ -285,14 +291,14 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         }
         __syncwarp();
         fence_proxy_async();
-        if (li + kAttnStages < nmy) issue(li + kAttnStages);
+        if (li + nst < nmy) issue(li + nst);
     }
     if (li_fail >= 0) {
         if (lane == 0) raise_status(p.status, kDevTimeout);
         // give the copies this warp issued and did not consume a bounded chance to land
         // before the block's shared memory goes away
-        for (int li = li_fail; li < nmy && li < li_fail + kAttnStages; ++li)
-            mbar_wait(&wbar[li % kAttnStages], (uint32_t)((li / kAttnStages) & 1));
+        for (int li = li_fail; li < nmy && li < li_fail + nst; ++li)
+            mbar_wait(&wbar[li % nst], (uint32_t)((li / nst) & 1));
     }
 
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);

@@ -26,9 +26,30 @@ extern __device__ unsigned long long* g_trace;
             if (bl_ < 4096) g_trace[((kernel_id) * 4096ull + bl_) * 16 + (point)] = t_;         \
         }                                                                                        \
     } while (0)
+// Records the SM of the block (plus one) at `point` instead of a time.
+#define STEP5_SMID(kernel_id, point)                                                             \
+    do {                                                                                         \
+        if (threadIdx.x == 0 && g_trace) {                                                       \
+            uint32_t sm_;                                                                        \
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));                                     \
+            if (blockIdx.x < 4096) g_trace[((kernel_id) * 4096ull + blockIdx.x) * 16 + (point)] = sm_ + 1; \
+        }                                                                                        \
+    } while (0)
+// Records a value (plus one) at `point` instead of a time.
+#define STEP5_VALUE(kernel_id, point, value)                                                     \
+    do {                                                                                         \
+        if (threadIdx.x == 0 && g_trace && blockIdx.x < 4096)                                    \
+            g_trace[((kernel_id) * 4096ull + blockIdx.x) * 16 + (point)] = (unsigned long long)(value) + 1; \
+    } while (0)
 #else
+#define STEP5_VALUE(kernel_id, point, value) \
+    do {                                     \
+    } while (0)
 #define STEP5_STAMP(kernel_id, point) \
     do {                              \
+    } while (0)
+#define STEP5_SMID(kernel_id, point) \
+    do {                             \
     } while (0)
 #endif
 
@@ -137,6 +158,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// p advanced to the next multiple of `align` (a power of two) bytes of the shared
+// window.  The offset is added to p itself so that the compiler keeps knowing p points to
+// shared memory (a round trip through an integer would turn its accesses generic).
+__device__ __forceinline__ uint8_t* align_smem(uint8_t* p, uint32_t align) {
+    const uint32_t a = smem_u32(p);
+    return p + (((a + align - 1u) & ~(align - 1u)) - a);
+}
+
 // Waits for phase `parity` of the barrier; gives up after kSpinLimit polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     uint32_t addr = smem_u32(bar);
@@ -154,6 +183,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
+// As mbar_wait, but each poll may suspend the thread for up to hint_ns (it resumes when
+// the phase completes), so waiting warps leave the issue slots to the others; gives up
+// after kSpinLimit / 64 polls.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t addr = smem_u32(bar);
+    for (uint32_t i = 0; i < kSpinLimit / 64; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity), "r"(hint_ns)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
 // 2-D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_t* bar, int32_t x,
                                             int32_t y) {
@@ -161,6 +209,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y,
+                                            int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 

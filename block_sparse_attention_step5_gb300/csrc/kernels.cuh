@@ -27,7 +27,6 @@ cudaError_t launch_convert(const uint16_t* in, uint8_t* out, int64_t n, cudaStre
 // ----------------------------------------------------------------- steps (2) + (3)
 constexpr int kHistBits = 12;
 constexpr int kHistBins = 1 << kHistBits;
-constexpr int kCoarseBins = 64;         // groups of 64 fine bins
 constexpr int kCandCap = 2048;          // candidates per (row, group) on the split path
 constexpr int kFusedMaxRegions = 16384; // regions a fused block keeps in shared memory
 constexpr int kMaxTopK = 2048;
@@ -44,17 +43,18 @@ struct ScoreParams {
     int32_t* sel_count;      // [N][G]
     float* sel_scores;       // [N][G][top_k] or null
     float* scores;           // [N][G][r_cap]: caller's export or workspace (split path)
-    uint32_t* hist;          // [N][G][kHistBins]   (split path, zero between calls)
-    uint32_t* cand_count;    // [N][G]              (split path, zero between calls)
+    uint32_t* hist;          // [N][G][kHistBins]   (split path, left zero by every call)
+    uint32_t* cand_count;    // [N][G]              (split path)
     uint64_t* cand;          // [N][G][kCandCap]    (split path)
-    uint32_t* ticket;        // [N][G]              (split path, zero between calls)
-    uint32_t* coarse;        // [N][G][kCoarseBins] (split path, zero between calls)
+    uint32_t* arrive1;       // [N][G] histogram arrivals   (split path, left zero by every call)
+    uint32_t* thr;           // [N][G] generation | threshold bin (split path)
+    uint32_t* bar2;          // [N][G] generation | arrivals      (split path)
     uint32_t* status;
     int N, B, G, idx_heads, hpg, t_cap, r_cap, rope_dims, top_k;
-    int regions_per_cta;     // split path: regions filtered by one block
-    int num_sms;             // split path: persistent scoring blocks (two per SM)
+    int num_sms;             // split path: persistent blocks (two per SM)
 };
 cudaError_t launch_score_fused(const ScoreParams& p, cudaStream_t stream, bool pdl);
+// Split path: one persistent launch (score, candidates, ranks) with grid barriers.
 // smap: 2-D tensor map of the summaries, [B*G*r_cap rows][64 bytes], box 64 x 256,
 // 64-byte swizzle (used when idx_heads / G == 4).
 cudaError_t launch_score_split(const ScoreParams& p, const CUtensorMap& smap, cudaStream_t stream, bool pdl);
@@ -80,6 +80,7 @@ cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const
                              cudaStream_t stream, bool pdl);
 // Clusters of `cluster` attention blocks that can be resident at once (0 if unknown).
 int attention_max_active_clusters(int cluster, int hq_g);
-size_t attention_smem_bytes(int cluster, int hq_g);
+size_t attention_smem_bytes(int cluster, int hq_g);  // dynamic part
+constexpr size_t kAttnStaticSmem = (kMaxTopK + 1) * 4;  // the block's picked ids
 
 }  // namespace step5

@@ -5,20 +5,21 @@
 // ascending.  Provider groups own contiguous blocks of indexer heads (vLLM Step5 DSA
 // geometry: "the sparse indexer reduces scores within provider groups").
 //
-// Scoring runs on the CUDA cores: each region is read as four 16-byte vectors, one per
-// thread, every e4m3 pair is widened to fp32 (exact) and multiplied with the thread's
-// 16 query dims per head using packed fp32x2 FMAs; a two-step butterfly completes the
-// 64-dim dot products.  Selection works on 64-bit keys (desc(score) << 32 | id), which
-// are unique, so any exact selection yields the same ordered ids.
+// Scoring runs on the CUDA cores.  With 4 indexer heads per group a thread scores whole
+// regions (two at a time against a shared-memory query broadcast); otherwise each region
+// is read as four 16-byte vectors, one per thread, and a butterfly completes the 64-dim
+// dot products.  Every e4m3 pair is widened to fp32 (exact) and multiplied with packed
+// fp32x2 FMAs.  Selection works on 64-bit keys (desc(score) << 32 | id), which are
+// unique, so any exact selection yields the same ordered ids.
 //
 // Two selection paths with identical results:
 //  * fused: one block per (row, group) scores every region into shared memory, then
-//    runs an 8-bit radix descent over the keys and a bitonic sort of the k winners.
-//  * split: many blocks per (row, group) score a slice each and add a 12-bit histogram
-//    of the keys into global memory; a filter pass copies every key in or above the
-//    bin holding the k-th key into a candidate list; one block per (row, group) then
-//    runs the same radix descent + sort over the candidates.  Used when there are few
-//    rows and many regions (decode at 128K-1M tokens).
+//    runs an 11-bit radix descent over the keys and a bitonic sort of the k winners.
+//  * split: one persistent launch for few rows with many regions (decode at 128K-1M
+//    tokens).  Blocks score an even share each and add a 12-bit histogram of the keys
+//    into global memory; after a grid barrier each block copies its keys in or above
+//    the bin holding the k-th key into a candidate list; after a second barrier the
+//    blocks place every candidate at its rank (a count of the smaller candidates).
 #include "kernels.cuh"
 
 namespace step5 {
@@ -356,10 +357,6 @@ struct SmemKeys {  // keys indexed by region id: desc(score) << 32 | id
         return ((uint64_t)key[i] << 32) | (uint32_t)i;
     }
 };
-struct CandKeys {  // explicit candidate list
-    const uint64_t* cand;
-    __device__ __forceinline__ uint64_t operator()(int i) const { return cand[i]; }
-};
 struct ScoreKeys {  // every score of the row, from global memory
     const float* scores;
     __device__ __forceinline__ uint64_t operator()(int i) const {
@@ -480,12 +477,11 @@ constexpr int kSplitThreads = 256;
 
 // ----------------------------------------------------------------- split path scoring
 //
-// Persistent blocks (two per SM) walk a contiguous run of tiles; a tile is kTileRegions
-// consecutive regions of one (row, group), contiguous in the summary store, fetched with
-// one bulk copy into a 2-stage shared-memory ring while the previous tile is scored.
-// Each run of tiles of one (row, group) adds its shared-memory histogram to the global
-// one and takes a ticket; the block holding the last ticket publishes the bin of the
-// k-th key for the filter pass.
+// Persistent blocks (two per SM) each walk an even share of the flattened (row, group,
+// region) space in tiles of kTileRegions consecutive regions of one (row, group),
+// contiguous in the summary store and fetched by TMA into a 2-stage shared-memory ring
+// while the previous tile is scored.  Each run of tiles of one (row, group) adds its
+// shared-memory histogram to the global one.
 
 constexpr int kTileRegions = 512;                 // 32 KB of summaries
 constexpr int kTileBytes = kTileRegions * 64;
@@ -497,41 +493,56 @@ struct Tile {
     int valid, ng, n, g, b, pos, R, c0, c1;
 };
 
-// The next tile of this block's range [x, hi) of the flattened (row, group, region)
-// space (r_cap regions per (row, group)): at most kTileRegions consecutive candidate
-// regions of one (row, group).  Regions past a row's R, and rows out of range, are
-// skipped.  Advances x past the tile.
-__device__ __forceinline__ Tile next_tile(const ScoreParams& p, int64_t& x, int64_t hi) {
+// A block's walk over its range of the flattened (row, group, region) space (r_cap
+// regions per (row, group)): the position, the regions of the range still ahead, and the
+// position data of the current row (loaded once per row).
+struct Walk {
+    int64_t left;
+    int ng, r;
+    int cn, cb, cpos, cR;
+};
+
+__device__ __forceinline__ Walk walk_start(const ScoreParams& p, int64_t x, int64_t hi) {
+    Walk k;
+    k.left = hi - x;
+    k.ng = (int)(x / p.r_cap);
+    k.r = (int)(x - (int64_t)k.ng * p.r_cap);
+    k.cn = -1;
+    k.cb = k.cpos = k.cR = 0;
+    return k;
+}
+
+// The next tile of the walk: at most kTileRegions consecutive candidate regions of one
+// (row, group).  Regions past a row's R, and rows out of range, are skipped.
+__device__ __forceinline__ Tile next_tile(const ScoreParams& p, Walk& k) {
     Tile t;
     t.valid = 0;
-    while (x < hi) {
-        const int ng = (int)(x / p.r_cap);
-        const int r = (int)(x - (int64_t)ng * p.r_cap);
-        const int n = ng / p.G;
-        int b, pos;
-        const int R = row_regions(p, n, b, pos);
-        if (R < 0) {
-            if (threadIdx.x == 0) raise_status(p.status, kDevRange);
-            x = (int64_t)(ng + 1) * p.r_cap;
+    while (k.left > 0) {
+        const int n = k.ng / p.G;
+        if (n != k.cn) {
+            k.cn = n;
+            k.cR = row_regions(p, n, k.cb, k.cpos);
+            if (k.cR < 0 && threadIdx.x == 0) raise_status(p.status, kDevRange);
+        }
+        if (k.r >= k.cR) {  // the rest of this (row, group) holds no candidate
+            k.left -= p.r_cap - k.r;
+            ++k.ng;
+            k.r = 0;
             continue;
         }
-        if (r >= R) {
-            x = (int64_t)(ng + 1) * p.r_cap;
-            continue;
-        }
-        int c1 = min(R, r + kTileRegions);
-        const int64_t lim = hi - (int64_t)ng * p.r_cap;
-        if ((int64_t)c1 > lim) c1 = (int)lim;
+        int c1 = min(k.cR, k.r + kTileRegions);
+        if ((int64_t)(c1 - k.r) > k.left) c1 = k.r + (int)k.left;
         t.valid = 1;
-        t.ng = ng;
+        t.ng = k.ng;
         t.n = n;
-        t.g = ng - n * p.G;
-        t.b = b;
-        t.pos = pos;
-        t.R = R;
-        t.c0 = r;
+        t.g = k.ng - n * p.G;
+        t.b = k.cb;
+        t.pos = k.cpos;
+        t.R = k.cR;
+        t.c0 = k.r;
         t.c1 = c1;
-        x = (int64_t)ng * p.r_cap + c1;
+        k.left -= c1 - k.r;
+        k.r = c1;
         return t;
     }
     return t;
@@ -542,7 +553,7 @@ __device__ __forceinline__ Tile next_tile(const ScoreParams& p, int64_t& x, int6
 // region.  FULL: the tile holds kTileRegions regions (no bounds checks).
 template <int HPG, bool FULL>
 __device__ __forceinline__ void score_tile(const QFrag<HPG>& f, const uint4* tile, int nreg, float* scores,
-                                           uint32_t* s_hist, int qd, int slot) {
+                                           float* keep, uint32_t* s_hist, int qd, int slot) {
 #pragma unroll
     for (int u4 = 0; u4 < kTileU; u4 += 4) {
         float sc[4];
@@ -556,64 +567,478 @@ __device__ __forceinline__ void score_tile(const QFrag<HPG>& f, const uint4* til
         const int lr = (u4 + qd) * 64 + slot;
         if (FULL || lr < nreg) {
             scores[lr] = mysc;
+            if (keep) keep[lr] = mysc;
             atomicAdd(&s_hist[desc_key(mysc) >> (32 - kHistBits)], 1u);
         }
     }
 }
 
-// One thread per region (HPG == 4): thread t scores rows t and t + 256 of a tile that
-// arrived as two 256-row boxes through the summaries' tensor map with 64-byte swizzle
-// (16-byte chunk k of row r sits at chunk k ^ ((r >> 1) & 3)), so the 8 rows a quarter
-// warp reads at once fall in 8 different bank groups.
-__device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, const float4* q4,
-                                                const float (&w)[4], float* scores, uint32_t* s_hist) {
-    const int t = threadIdx.x;  // 0..255
-    const int sw = (t >> 1) & 3;
-    const uint4* ra = reinterpret_cast<const uint4*>(tile + t * 64);
-    const uint4* rb = reinterpret_cast<const uint4*>(tile + 16384 + t * 64);
-    uint4 a[4], b[4];
+// The split path stages a (row, group)'s query in two parts so that its loads overlap
+// the first tile's copy: load_query_raw reads the bf16 q (and NEOX partner dims) and the
+// weights, which need only (n, g); load_rope reads cos/sin at the row's position;
+// finish_query rotates, rounds to e4m3 and stores the query and weights into one of two
+// shared-memory buffers.
+template <int HPG>
+struct QRaw {
+    static constexpr int kPer = (HPG * 64 + kSplitThreads - 1) / kSplitThreads;
+    uint16_t q[kPer], qp[kPer];  // element i = threadIdx.x + kSplitThreads * j
+    float w;                     // weight of head threadIdx.x (threads below HPG)
+};
+
+template <int HPG>
+__device__ __forceinline__ void load_query_raw(const ScoreParams& p, int n, int g, QRaw<HPG>& r) {
+    const int half = p.rope_dims >> 1;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        a[k] = ra[k ^ sw];
-        b[k] = rb[k ^ sw];
+    for (int j = 0; j < QRaw<HPG>::kPer; ++j) {
+        const int i = threadIdx.x + kSplitThreads * j;
+        r.q[j] = r.qp[j] = 0;
+        if (i < HPG * 64) {
+            const int h = i >> 6, d = i & 63;
+            const uint16_t* qrow = p.idx_q + ((int64_t)n * p.idx_heads + (int64_t)g * HPG + h) * 64;
+            r.q[j] = qrow[d];
+            if (p.cos != nullptr && d < p.rope_dims) r.qp[j] = qrow[d < half ? d + half : d - half];
+        }
     }
-    float sa, sb;
-    score_rows2(a, b, q4, w, sa, sb);
-    if (t < nreg) {
-        scores[t] = sa;
-        atomicAdd(&s_hist[desc_key(sa) >> (32 - kHistBits)], 1u);
-    }
-    if (t + 256 < nreg) {
-        scores[t + 256] = sb;
-        atomicAdd(&s_hist[desc_key(sb) >> (32 - kHistBits)], 1u);
+    r.w = threadIdx.x < HPG ? p.w[(int64_t)n * p.idx_heads + (int64_t)g * HPG + threadIdx.x] : 0.0f;
+}
+
+// The bf16 cos/sin of each staged element's NEOX pair at position pos (zero when the
+// element is not rotated).
+template <int HPG>
+struct QRope {
+    uint16_t c[QRaw<HPG>::kPer], s[QRaw<HPG>::kPer];
+};
+
+template <int HPG>
+__device__ __forceinline__ void load_rope(const ScoreParams& p, int pos, QRope<HPG>& r) {
+    const int half = p.rope_dims >> 1;
+#pragma unroll
+    for (int j = 0; j < QRaw<HPG>::kPer; ++j) {
+        const int i = threadIdx.x + kSplitThreads * j;
+        const int d = i & 63;
+        r.c[j] = r.s[j] = 0;
+        if (i < HPG * 64 && p.cos != nullptr && d < p.rope_dims) {
+            const int pi = d < half ? d : d - half;
+            r.c[j] = p.cos[(int64_t)pos * half + pi];
+            r.s[j] = p.sin[(int64_t)pos * half + pi];
+        }
     }
 }
 
+// Shared-memory query buffers of the split scoring kernel.  HPG == 4 keeps the query in
+// the q4 layout of score_rows2; the others as q[h * 64 + d].
 template <int HPG>
-__global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(const __grid_constant__ CUtensorMap smap,
-                                                                      ScoreParams p) {
+struct QBuf {
+    float q[HPG * 64];
+    float w[HPG];
+};
+
+// e4m3(bf16(NEOX(q))) of each staged element, and the weights, into buffer qb.  The
+// caller synchronises before reading it.
+template <int HPG>
+__device__ __forceinline__ void finish_query(const ScoreParams& p, const QRaw<HPG>& r, const QRope<HPG>& ro,
+                                             QBuf<HPG>& qb) {
+    const int half = p.rope_dims >> 1;
+#pragma unroll
+    for (int j = 0; j < QRaw<HPG>::kPer; ++j) {
+        const int i = threadIdx.x + kSplitThreads * j;
+        if (i < HPG * 64) {
+            const int h = i >> 6, d = i & 63;
+            uint16_t rb = r.q[j];
+            if (p.cos != nullptr && d < p.rope_dims)
+                rb = neox_rotate(bf16_to_f32(rb), bf16_to_f32(r.qp[j]), bf16_to_f32(ro.c[j]), bf16_to_f32(ro.s[j]),
+                                 d < half);
+            const float v = e4m3x2_to_f32x2(f32_to_e4m3(bf16_to_f32(rb))).x;
+            if constexpr (HPG == 4)
+                qb.q[(2 * (d >> 1) + (h >> 1)) * 4 + (h & 1) * 2 + (d & 1)] = v;
+            else
+                qb.q[i] = v;
+        }
+    }
+    if (threadIdx.x < HPG) qb.w[threadIdx.x] = r.w;
+}
+
+// The 4-lanes-per-region query registers from a staged buffer (after a __syncthreads).
+template <int HPG>
+__device__ __forceinline__ void qfrag_from_smem(const QBuf<HPG>& qb, QFrag<HPG>& f) {
+    const int qd = threadIdx.x & 3;
+#pragma unroll
+    for (int h = 0; h < HPG; ++h) f.w[h] = qb.w[h];
+#pragma unroll
+    for (int h = 0; h < HPG; ++h) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            f.q[h][i] = make_float2(qb.q[h * 64 + 16 * qd + 2 * i], qb.q[h * 64 + 16 * qd + 2 * i + 1]);
+    }
+}
+
+// Position of row n for its rope lookup, 0 when the row is out of range (its tiles are
+// skipped).
+__device__ __forceinline__ int row_pos_or0(const ScoreParams& p, int n) {
+    int b, pos;
+    return row_regions(p, n, b, pos) < 0 ? 0 : pos;
+}
+
+// Score of one region whose 64 summary bytes are a[0..3] (the one-row form of
+// score_rows2, same arithmetic and order).
+__device__ __forceinline__ float score_row1(const uint4 (&a)[4], const float4* q4, const float (&w)[4]) {
+    float2 A[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) A[h] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t wa[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const int p0 = 8 * k + 2 * qq;
+#pragma unroll
+            for (int hw = 0; hw < 2; ++hw) {
+                const float2 xa = e4m3x2_to_f32x2((uint16_t)(hw ? wa[qq] >> 16 : wa[qq] & 0xffffu));
+                const float4 q01 = q4[2 * (p0 + hw)], q23 = q4[2 * (p0 + hw) + 1];
+                A[0] = __ffma2_rn(make_float2(q01.x, q01.y), xa, A[0]);
+                A[1] = __ffma2_rn(make_float2(q01.z, q01.w), xa, A[1]);
+                A[2] = __ffma2_rn(make_float2(q23.x, q23.y), xa, A[2]);
+                A[3] = __ffma2_rn(make_float2(q23.z, q23.w), xa, A[3]);
+            }
+        }
+    }
+    return finish_score4(A, w);
+}
+
+// One thread per region (HPG == 4): thread t scores rows t and t + 256 of a tile that
+// arrived as two 256-row boxes through the summaries' tensor map with 64-byte swizzle
+// (16-byte chunk k of row r sits at chunk k ^ ((r >> 1) & 3)), so the 8 rows a quarter
+// warp reads at once fall in 8 different bank groups.  Rows at or past nreg are skipped
+// a warp at a time.
+__device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, const float4* q4,
+                                                const float (&w)[4], float* scores, float* keep,
+                                                uint32_t* s_hist) {
+    const int t = threadIdx.x;  // 0..255
+    const int wbase = t & ~31;
+    if (wbase >= nreg) return;
+    const int sw = (t >> 1) & 3;
+    const uint4* ra = reinterpret_cast<const uint4*>(tile + t * 64);
+    uint4 a[4];
+    if (wbase + 256 < nreg) {
+        const uint4* rb = reinterpret_cast<const uint4*>(tile + 16384 + t * 64);
+        uint4 b[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            a[k] = ra[k ^ sw];
+            b[k] = rb[k ^ sw];
+        }
+        float sa, sb;
+        score_rows2(a, b, q4, w, sa, sb);
+        scores[t] = sa;  // t < 256 < nreg
+        if (keep) keep[t] = sa;
+        atomicAdd(&s_hist[desc_key(sa) >> (32 - kHistBits)], 1u);
+        if (t + 256 < nreg) {
+            scores[t + 256] = sb;
+            if (keep) keep[t + 256] = sb;
+            atomicAdd(&s_hist[desc_key(sb) >> (32 - kHistBits)], 1u);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a[k] = ra[k ^ sw];
+        const float sa = score_row1(a, q4, w);
+        if (t < nreg) {
+            scores[t] = sa;
+            if (keep) keep[t] = sa;
+            atomicAdd(&s_hist[desc_key(sa) >> (32 - kHistBits)], 1u);
+        }
+    }
+}
+
+// ----------------------------------------------------------------- grid-wide steps
+
+constexpr uint32_t kBarrierPolls = 1u << 22;  // polls of a grid barrier before giving up
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* a) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
+// Block-wide exclusive scan of one count per thread; returns the thread's offset and
+// leaves the block total in *total.  s_w: kSplitThreads / 32 words of scratch.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_w, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_w[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kSplitThreads / 32; ++w) {
+        const uint32_t c = s_w[w];
+        before += w < warp ? c : 0u;
+        tot += c;
+    }
+    __syncthreads();
+    *total = tot;
+    return before + incl - v;
+}
+
+// Fine bin holding the K-th smallest key of a (row, group) with R regions, from its
+// whole fine histogram (one 16 KB read shared by the block: each thread owns 16
+// consecutive bins); kHistBins - 1 when R <= K or the histogram counts fewer than K
+// keys.  Called by the whole block; the result lands in *s_out.
+__device__ void block_threshold(const uint4 (&h)[4], int R, int K, uint32_t* s_w, int* s_out) {
+    if (threadIdx.x == 0) *s_out = kHistBins - 1;
+    uint32_t loc[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        loc[4 * q] = h[q].x;
+        loc[4 * q + 1] = h[q].y;
+        loc[4 * q + 2] = h[q].z;
+        loc[4 * q + 3] = h[q].w;
+    }
+    uint32_t sum = 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) sum += loc[q];
+    uint32_t tot = 0;
+    const uint32_t before = block_excl_scan(sum, s_w, &tot);  // synchronises (after the default)
+    if (R > K && before < (uint32_t)K && (uint32_t)K <= before + sum) {
+        uint32_t c = before;
+        int bin = 15;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            if (bin == 15 && c + loc[q] >= (uint32_t)K) bin = q;
+            c += loc[q];
+        }
+        *s_out = threadIdx.x * 16 + bin;
+    }
+    __syncthreads();
+}
+
+// Block holding flattened position x of a launch whose block b covers
+// [total * b / grid, total * (b + 1) / grid).
+__device__ __forceinline__ int block_of(int64_t x, int64_t total, int grid) {
+    return (int)(((x + 1) * grid - 1) / total);
+}
+
+// Last of the blocks that contribute candidates to one (row, group) to arrive:
+// releases this block's candidate writes and, for the last, acquires everyone's.
+__device__ __forceinline__ bool arrive_last(uint32_t* ctr, uint32_t nblocks) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
+    return old == nblocks - 1u;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* a, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+// Per-(row, group) synchronisation words of the split path.  Each is a generation
+// number (high bits) with a payload, so none needs clearing between calls:
+//  * thr[ng] = gen << 12 | bin: the threshold bin, published by the last block to add
+//    its histogram share (counted in arrive1[ng], which that block clears);
+//  * bar2[ng] = gen << 16 | arrivals: a barrier over the (row, group)'s blocks once
+//    their candidates are written; the last arrival clears the count and advances the
+//    generation with one release add.
+constexpr uint32_t kArrivedLast = 0x80000000u;
+
+// Arrival at a count/generation barrier word of nb blocks: the generation seen, or
+// kArrivedLast for the last arrival (which has released the others).
+__device__ __forceinline__ uint32_t arrive_gen(uint32_t* word, uint32_t nb) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(word) : "memory");
+    if ((old & 0xffffu) == nb - 1u) {
+        asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(word), "r"(0x10000u - nb) : "memory");
+        return kArrivedLast;
+    }
+    return old >> 16;
+}
+
+// Waits until the generation of a barrier word differs from gen (kArrivedLast: no
+// wait); false when the wait gives up.
+__device__ __forceinline__ bool wait_gen(const uint32_t* word, uint32_t gen) {
+    if (gen == kArrivedLast) return true;
+    for (uint32_t it = 0; it < kBarrierPolls; ++it)
+        if ((ld_acquire_u32(word) >> 16) != gen) return true;
+    return false;
+}
+
+// Threshold of one (row, group), by the whole block that added its histogram share
+// last: the fine bin holding the K-th key (block_threshold over the complete
+// histogram).  Clears the histogram, the arrival counter and the candidate counter for
+// the candidates that follow, then publishes thr[ng] = (gen + 1) << 12 | bin with
+// release semantics.
+__device__ void publish_threshold(const ScoreParams& p, int ng, uint32_t gen, uint32_t* s_w, int* s_tmp) {
+    const int tid = threadIdx.x;
+    uint4* gh = reinterpret_cast<uint4*>(p.hist + (int64_t)ng * kHistBins) + tid * 4;
+    uint4 h[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) h[q] = __ldcg(gh + q);
+    int b, pos;
+    int R = row_regions(p, ng / p.G, b, pos);
+    if (R < 0) R = 0;
+    block_threshold(h, R, p.top_k, s_w, s_tmp);  // ends with a __syncthreads
+#pragma unroll
+    for (int q = 0; q < 4; ++q) gh[q] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (tid == 0) {
+        p.arrive1[ng] = 0;
+        p.cand_count[ng] = 0;
+        st_release_u32(p.thr + ng, ((gen + 1u) << 12) | (uint32_t)*s_tmp);
+    }
+}
+
+// Waits (thread 0) for the threshold of (row, group) ng published after generation
+// gen; -1 when the wait gives up.
+__device__ int wait_threshold(const ScoreParams& p, int ng, uint32_t gen) {
+    for (uint32_t it = 0; it < kBarrierPolls; ++it) {
+        const uint32_t v = ld_acquire_u32(p.thr + ng);
+        if ((v >> 12) != gen) return (int)(v & (kHistBins - 1));
+    }
+    return -1;
+}
+
+// Ranks of the candidates of (row, group) ng, after every candidate is written: block
+// `sub` of the nb blocks covering it takes chunks of 32 candidates (one per lane), and
+// each warp counts the smaller keys in its eighth of the list; a candidate ranked below
+// K is written at its rank.  Block 0 writes the padding and the count, or, when the
+// list overflowed, selects from every score of the row.
+__device__ void rank_segment(const ScoreParams& p, int ng, int sub, int nb, uint8_t* ring, uint32_t* s_w) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = p.top_k;
+    const int n = ng / p.G;
+    // the count and the first slots of the list are requested at once
+    const uint64_t* cl = p.cand + (int64_t)ng * kCandCap;
+    constexpr int kSpec = 4;  // slots per thread read before the count is known
+    uint64_t cv[kSpec];
+    const bool works = sub * 32 < kCandCap;
+#pragma unroll
+    for (int u = 0; u < kSpec; ++u) cv[u] = works ? __ldcg(cl + u * kSplitThreads + tid) : 0ull;
+    const int C = (int)__ldcg(p.cand_count + ng);
+    int32_t* ids = p.sel_ids + (int64_t)ng * K;
+    float* ss = p.sel_scores ? p.sel_scores + (int64_t)ng * K : nullptr;
+    if (C > kCandCap) {
+        if (sub == 0) {
+            int b, pos;
+            int R = row_regions(p, n, b, pos);
+            if (R < 0) R = 0;
+            int P2 = 32;
+            while (P2 < K) P2 <<= 1;
+            uint64_t* s_sel = reinterpret_cast<uint64_t*>(ring);
+            TopkSmem& ts = *reinterpret_cast<TopkSmem*>(ring + kMaxTopK * 8);
+            const int take =
+                block_topk<kSplitThreads>(ScoreKeys{p.scores + (int64_t)ng * p.r_cap}, R, K, P2, s_sel, ts);
+            write_selection<kSplitThreads>(p, n, ng - n * p.G, take, s_sel);
+        }
+        return;
+    }
+    if (sub * 32 < C) {
+        uint64_t* s_keys = reinterpret_cast<uint64_t*>(ring);
+#pragma unroll
+        for (int u = 0; u < kSpec; ++u)
+            if (u * kSplitThreads + tid < C) s_keys[u * kSplitThreads + tid] = cv[u];
+        for (int i = kSpec * kSplitThreads + tid; i < C; i += kSplitThreads) s_keys[i] = __ldcg(cl + i);
+        __syncthreads();
+        const int j0 = (int)((int64_t)C * warp / 8), j1 = (int)((int64_t)C * (warp + 1) / 8);
+        for (int c0 = sub * 32; c0 < C; c0 += nb * 32) {
+            const int idx = c0 + lane;
+            const uint64_t key = idx < C ? s_keys[idx] : ~0ull;
+            uint32_t less = 0;
+            for (int j = j0; j < j1; ++j) less += s_keys[j] < key ? 1u : 0u;
+            s_w[warp * 32 + lane] = less;
+            __syncthreads();
+            if (warp == 0 && idx < C) {
+                uint32_t rank = 0;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) rank += s_w[w * 32 + lane];
+                if (rank < (uint32_t)K) {
+                    ids[rank] = (int32_t)(uint32_t)(key & 0xffffffffu);
+                    if (ss) ss[rank] = score_of_desc_key((uint32_t)(key >> 32));
+                }
+            }
+            __syncthreads();
+        }
+    }
+    if (sub == 0) {
+        const int take = C < K ? C : K;
+        for (int i = take + tid; i < K; i += kSplitThreads) {
+            ids[i] = -1;
+            if (ss) ss[i] = -INFINITY;
+        }
+        if (tid == 0) p.sel_count[ng] = take;
+    }
+}
+
+constexpr int kKeep = 2048;                      // scores of a block's range kept on chip
+constexpr int kMaxShareSegs = 32;                // (row, group)s one block's share may cover
+constexpr int kKeepPer = kKeep / kSplitThreads;  // 8 per thread
+constexpr int kRankWarps = kSplitThreads / 32;
+
+// Split path, one persistent launch (every block resident):
+//  1. score an even share of the (row, group, region) space and add shared-memory
+//     histograms of the keys to the global histograms; the last block of each
+//     (row, group) to add its share publishes the bin holding the (row, group)'s K-th key;
+//  2. copy every key of the share in or below that bin into the (row, group)'s
+//     candidate list;
+//  3. once all blocks of the (row, group) have done so, they split its candidates and
+//     write each one ranked below K at its rank (rank_segment).
+// Histograms and counters are left zero and the synchronisation words carry
+// generations, so nothing needs clearing between calls.  A share covers at most
+// kMaxShareSegs (row, group)s (the host launches row batches).
+template <int HPG>
+__global__ void __launch_bounds__(kSplitThreads, 2) score_select_kernel(const __grid_constant__ CUtensorMap smap,
+                                                                        ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = align_smem(smem_raw, 1024);
     __shared__ uint32_t s_hist[kHistBins];
-    __shared__ float s_q[HPG * 64];
+    __shared__ __align__(16) QBuf<HPG> s_qb[2];
+    __shared__ float s_keep[kKeep];
     __shared__ __align__(8) uint64_t s_bar[kScoreStages];
+    __shared__ uint32_t s_w[kRankWarps * 32];
+    __shared__ int s_thr[2], s_R[2];
+    __shared__ uint32_t s_base[2];
     const int tid = threadIdx.x;
     const int qd = tid & 3, slot = tid >> 2;
 
+    // set-up that touches no input: barriers, the histogram, the tensor map
     if (tid == 0) {
         for (int st = 0; st < kScoreStages; ++st) mbar_init(&s_bar[st], 1);
         fence_mbar_init();
+        if constexpr (HPG == 4) prefetch_tmap(&smap);
     }
+    for (int i = tid; i < kHistBins; i += kSplitThreads) s_hist[i] = 0;
     STEP5_STAMP(1, 0);
     __syncthreads();
     pdl_wait();
-    pdl_launch_dependents();
     STEP5_STAMP(1, 1);
     // this block's even share of the flattened (row, group, region) space
-    const int64_t total = (int64_t)p.N * p.G * p.r_cap;
-    int64_t xpos = total * blockIdx.x / gridDim.x;
+    const int NG = p.N * p.G;
+    const int64_t total = (int64_t)NG * p.r_cap;
+    const int64_t xbeg = total * blockIdx.x / gridDim.x;
     const int64_t xend = total * (blockIdx.x + 1) / gridDim.x;
-    auto next_valid = [&]() -> Tile { return next_tile(p, xpos, xend); };
+    const int ngA = (int)(xbeg / p.r_cap);
+    const int ngB = (int)((xend - 1) / p.r_cap);
+    // the share's scores stay on chip when it is short and spans at most two (row, group)s
+    const bool keep_all = xend - xbeg <= kKeep && ngB <= ngA + 1;
+    Walk wk = walk_start(p, xbeg, xend);
+    // The queries of the first two (row, group)s of the range are requested together
+    // with their rows' positions, their cos/sin before the first tiles, so these small
+    // reads do not queue behind every block's tile copies; later (row, group)s (ranges
+    // over short rows) are staged when reached.
+    int staged0 = ngA;  // (row, group) held by query buffer 0 / 1 (-1: none)
+    int staged1 = ngB > ngA ? ngA + 1 : -1;
+    QRaw<HPG> r0, r1;
+    QRope<HPG> o0, o1;
+    {
+        const int n0 = staged0 / p.G;
+        const int n1 = staged1 < 0 ? n0 : staged1 / p.G;
+        load_query_raw<HPG>(p, n0, staged0 - n0 * p.G, r0);
+        if (staged1 >= 0) load_query_raw<HPG>(p, n1, staged1 - n1 * p.G, r1);
+        const int pos0 = row_pos_or0(p, n0);
+        const int pos1 = n1 == n0 ? pos0 : row_pos_or0(p, n1);
+        load_rope<HPG>(p, pos0, o0);
+        if (staged1 >= 0) load_rope<HPG>(p, pos1, o1);
+    }
     auto issue = [&](const Tile& x, int st) {
         if (tid == 0) {
             if constexpr (HPG == 4) {
@@ -631,310 +1056,272 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_hist_kernel(const __gr
         }
     };
     // two tiles in flight: `cur` in stage st, `nxt` in stage st ^ 1
-    Tile cur = next_valid();
+    Tile cur = next_tile(p, wk);
     if (cur.valid) issue(cur, 0);
-    Tile nxt = next_valid();
+    Tile nxt = next_tile(p, wk);
     if (nxt.valid) issue(nxt, 1);
+    finish_query<HPG>(p, r0, o0, s_qb[0]);
+    if (staged1 >= 0) finish_query<HPG>(p, r1, o1, s_qb[1]);
+    __syncthreads();  // staged queries visible
     STEP5_STAMP(1, 2);
 
-    int seg_ng = -1;
-    int ntile = 0;
+    int seg_ng = -1, qbuf = 0;
     QFrag<HPG> f;
-    __shared__ float4 s_q4[64];
     float w4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    auto finish = [&](int ng) {
+    // makes (row, group) x.ng the current segment, staging its query if needed
+    auto enter = [&](const Tile& x) {
+        int bsel = staged0 == x.ng ? 0 : staged1 == x.ng ? 1 : -1;
+        if (bsel < 0) {
+            bsel = qbuf ^ 1;  // the buffer of the segment just finished is free
+            QRaw<HPG> r;
+            QRope<HPG> o;
+            load_query_raw<HPG>(p, x.n, x.g, r);
+            load_rope<HPG>(p, x.pos, o);
+            finish_query<HPG>(p, r, o, s_qb[bsel]);
+            if (bsel) staged1 = x.ng; else staged0 = x.ng;
+            __syncthreads();
+        }
+        qbuf = bsel;
+        seg_ng = x.ng;
+        if constexpr (HPG == 4) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) w4[h] = s_qb[bsel].w[h];
+        } else {
+            qfrag_from_smem<HPG>(s_qb[bsel], f);
+        }
+    };
+    auto flush_hist = [&](int ng) {
         __syncthreads();
         uint32_t* gh = p.hist + (int64_t)ng * kHistBins;
-        uint32_t coarse = 0;
-        // each thread flushes kHistBins / 256 = 16 consecutive fine bins; 4 threads make
-        // one coarse bin of 64
+        // each thread flushes kHistBins / 256 = 16 consecutive bins
+#pragma unroll
         for (int i = 0; i < kHistBins / kSplitThreads; ++i) {
             const int bin = tid * (kHistBins / kSplitThreads) + i;
             const uint32_t c = s_hist[bin];
-            coarse += c;
             if (c) atomicAdd(gh + bin, c);
         }
-        coarse += __shfl_xor_sync(0xffffffffu, coarse, 1);
-        coarse += __shfl_xor_sync(0xffffffffu, coarse, 2);
-        if ((tid & 3) == 0 && coarse) atomicAdd(p.coarse + (int64_t)ng * kCoarseBins + (tid >> 2), coarse);
     };
 
+    // ---------------- phase 1: scores and histograms
     uint32_t ph0 = 0, ph1 = 0;
-    int st = 0;
-    bool timed_out = false;
+    int st = 0, ntile = 0;
+    bool ok = true;
     while (cur.valid) {
         if (cur.ng != seg_ng) {
-            if (seg_ng >= 0) finish(seg_ng);
-            seg_ng = cur.ng;
-            for (int i = tid; i < kHistBins; i += kSplitThreads) s_hist[i] = 0;
-            if constexpr (HPG == 4) {
-#pragma unroll
-                for (int h = 0; h < 4; ++h) w4[h] = p.w[(int64_t)cur.n * p.idx_heads + (int64_t)cur.g * 4 + h];
-                stage_query<4>(p, cur.n, cur.g, cur.pos, s_q);
-                build_q4(s_q, s_q4);
-            } else {
-                load_qfrag<HPG>(p, cur.n, cur.g, cur.pos, s_q, f);  // has a __syncthreads
+            if (seg_ng >= 0) {
+                flush_hist(seg_ng);
+                __syncthreads();  // every bin is flushed before it is cleared
+                for (int i = tid; i < kHistBins; i += kSplitThreads) s_hist[i] = 0;
             }
+            enter(cur);
         }
-        if (ntile < 4) STEP5_STAMP(1, 3 + 2 * ntile);
-        if (!mbar_wait(&s_bar[st], st ? ph1 : ph0)) {
-            timed_out = true;
+        if (ntile < 3) STEP5_STAMP(1, 3 + 2 * ntile);
+        // one thread waits for the tile; the barrier releases the others (they do not
+        // spin on the issue slots the other block of the SM is computing with)
+        bool got = true;
+        if (tid == 0) got = mbar_wait(&s_bar[st], st ? ph1 : ph0);
+        if (__syncthreads_or(!got)) {
+            ok = false;
             break;
         }
-        if (ntile < 4) STEP5_STAMP(1, 4 + 2 * ntile);
+        if (ntile < 3) STEP5_STAMP(1, 4 + 2 * ntile);
         ++ntile;
         if (st) ph1 ^= 1u; else ph0 ^= 1u;
-        float* scores = p.scores + (int64_t)cur.ng * p.r_cap + cur.c0;
+        const int64_t x0 = (int64_t)cur.ng * p.r_cap + cur.c0;
+        float* scores = p.scores + x0;
+        float* keep = keep_all ? s_keep + (int)(x0 - xbeg) : nullptr;
         const int nreg = cur.c1 - cur.c0;
         if constexpr (HPG == 4) {
-            score_tile_rows(ring + st * kTileBytes, nreg, s_q4, w4, scores, s_hist);
+            score_tile_rows(ring + st * kTileBytes, nreg, reinterpret_cast<const float4*>(s_qb[qbuf].q), w4,
+                            scores, keep, s_hist);
         } else {
             const uint4* tile = reinterpret_cast<const uint4*>(ring + st * kTileBytes);
             if (nreg == kTileRegions)
-                score_tile<HPG, true>(f, tile, nreg, scores, s_hist, qd, slot);
+                score_tile<HPG, true>(f, tile, nreg, scores, keep, s_hist, qd, slot);
             else
-                score_tile<HPG, false>(f, tile, nreg, scores, s_hist, qd, slot);
+                score_tile<HPG, false>(f, tile, nreg, scores, keep, s_hist, qd, slot);
         }
         __syncthreads();  // every thread is done with this stage before it is refilled
         cur = nxt;
-        nxt = next_valid();
+        nxt = next_tile(p, wk);
         if (nxt.valid) {
             if (tid == 0) fence_proxy_async();
             issue(nxt, st);
         }
         st ^= 1;
     }
-    if (timed_out) {
-        if (tid == 0) raise_status(p.status, kDevTimeout);
-        // give copies still in flight a bounded chance to land before the block exits
-        if (cur.valid) mbar_wait(&s_bar[st], st ? ph1 : ph0);
-        if (nxt.valid) mbar_wait(&s_bar[st ^ 1], st ? ph0 : ph1);
+    if (!ok) {
+        if (tid == 0) {
+            raise_status(p.status, kDevTimeout);
+            // give copies still in flight a bounded chance to land before the block exits
+            if (cur.valid) mbar_wait(&s_bar[st], st ? ph1 : ph0);
+            if (nxt.valid) mbar_wait(&s_bar[st ^ 1], st ? ph0 : ph1);
+        }
+        return;
+    }
+    STEP5_STAMP(1, 9);
+    if (seg_ng >= 0) flush_hist(seg_ng);
+    STEP5_STAMP(1, 10);
+    // Every block that covers part of a (row, group) arrives once its histogram share is
+    // in; the last one computes and publishes the (row, group)'s threshold bin.  The
+    // threshold word's generation is read before arriving.
+    __shared__ int s_last;
+    __shared__ int s_tmp;
+    __shared__ uint32_t s_gen1[kMaxShareSegs], s_gen2[kMaxShareSegs];
+    auto seg_first = [&](int ng) { return block_of((int64_t)ng * p.r_cap, total, gridDim.x); };
+    auto seg_blocks = [&](int ng) { return block_of((int64_t)(ng + 1) * p.r_cap - 1, total, gridDim.x) - seg_first(ng) + 1; };
+    for (int ng = ngA; ng <= ngB; ++ng) {
+        __syncthreads();  // the block's histogram additions come before its arrival
+        if (tid == 0) {
+            const uint32_t gen = ld_acquire_u32(p.thr + ng) >> 12;
+            s_gen1[ng - ngA] = gen;
+            s_last = arrive_last(p.arrive1 + ng, (uint32_t)seg_blocks(ng));
+        }
+        __syncthreads();
+        if (s_last) publish_threshold(p, ng, s_gen1[ng - ngA], s_w, &s_tmp);
     }
     STEP5_STAMP(1, 11);
-    if (seg_ng >= 0 && !timed_out) finish(seg_ng);
-    STEP5_STAMP(1, 12);
-}
-
-// Bin holding the K-th smallest key of (row, group) from the coarse (64-bin) and fine
-// (4096-bin) histograms; all bins when the row has at most K regions.  Two small reads
-// (256 bytes each) instead of the whole fine histogram.
-__device__ int threshold_bin2(const uint32_t* coarse, const uint32_t* fine, int R, int K, int* s_out) {
-    if (R <= K) return kHistBins - 1;
-    const int tid = threadIdx.x, lane = tid & 31;
-    if (tid < 32) {
-        const uint32_t c0 = __ldcg(coarse + 2 * lane), c1 = __ldcg(coarse + 2 * lane + 1);
-        uint32_t incl = c0 + c1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        const uint32_t excl = incl - c0 - c1;
-        // the coarse bin holding the K-th key
-        int cb = -1;
-        uint32_t before = 0;
-        if (excl < (uint32_t)K && (uint32_t)K <= excl + c0) {
-            cb = 2 * lane;
-            before = excl;
-        } else if (excl + c0 < (uint32_t)K && (uint32_t)K <= incl) {
-            cb = 2 * lane + 1;
-            before = excl + c0;
-        }
-        const uint32_t found = __ballot_sync(0xffffffffu, cb >= 0);
-        const int src = found ? __ffs(found) - 1 : 0;
-        cb = __shfl_sync(0xffffffffu, cb, src);
-        before = __shfl_sync(0xffffffffu, before, src);
-        if (!found) cb = kCoarseBins - 1, before = 0;
-        // the fine bins of that coarse bin
-        const uint32_t f0 = __ldcg(fine + cb * 64 + 2 * lane), f1 = __ldcg(fine + cb * 64 + 2 * lane + 1);
-        uint32_t fin = f0 + f1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, fin, o);
-            if (lane >= o) fin += t;
-        }
-        const uint32_t fex = before + fin - f0 - f1;
-        int fb = -1;
-        if (fex < (uint32_t)K && (uint32_t)K <= fex + f0)
-            fb = cb * 64 + 2 * lane;
-        else if (fex + f0 < (uint32_t)K && (uint32_t)K <= before + fin)
-            fb = cb * 64 + 2 * lane + 1;
-        const uint32_t ff = __ballot_sync(0xffffffffu, fb >= 0);
-        fb = __shfl_sync(0xffffffffu, fb, ff ? __ffs(ff) - 1 : 0);
-        if (lane == 0) *s_out = ff ? fb : kHistBins - 1;
-    }
-    __syncthreads();
-    return *s_out;
-}
-
-constexpr int kFilterPerThread = 4;  // scores per thread (regions_per_cta = 1024)
-
-__global__ void __launch_bounds__(kSplitThreads) filter_kernel(ScoreParams p) {
-    __shared__ uint32_t s_wcnt[kSplitThreads / 32];
-    __shared__ uint32_t s_base;
-    __shared__ int s_bin;
-    const int g = blockIdx.y, n = blockIdx.z;
-    STEP5_STAMP(2, 0);
-    pdl_wait();
     pdl_launch_dependents();
-    STEP5_STAMP(2, 1);
-    int b, pos;
-    const int R = row_regions(p, n, b, pos);
-    if (R < 0) return;
-    const int c0 = blockIdx.x * p.regions_per_cta;
-    const int c1 = min(R, c0 + p.regions_per_cta);
-    if (c0 >= c1) return;
-    const int64_t ng = (int64_t)n * p.G + g;
-    const float* scores = p.scores + ng * p.r_cap;
-    // every score of the block is requested at once
-    float sc[kFilterPerThread];
-#pragma unroll
-    for (int u = 0; u < kFilterPerThread; ++u) {
-        const int r = c0 + u * kSplitThreads + threadIdx.x;
-        sc[u] = r < c1 ? __ldcg(scores + r) : 0.0f;
-    }
-    const int b1 = threshold_bin2(p.coarse + ng * kCoarseBins, p.hist + ng * kHistBins, R, p.top_k, &s_bin);
-    STEP5_STAMP(2, 2);
-    uint32_t mine = 0, keys[kFilterPerThread];
-#pragma unroll
-    for (int u = 0; u < kFilterPerThread; ++u) {
-        const int r = c0 + u * kSplitThreads + threadIdx.x;
-        keys[u] = desc_key(sc[u]);
-        if (r < c1 && (int)(keys[u] >> (32 - kHistBits)) <= b1) ++mine;
-    }
-    // one atomic per block: block-wide exclusive scan of the per-thread counts
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    if (lane == 31) s_wcnt[warp] = incl;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t tot = 0;
-        for (int w = 0; w < kSplitThreads / 32; ++w) {
-            const uint32_t c = s_wcnt[w];
-            s_wcnt[w] = tot;
-            tot += c;
-        }
-        s_base = tot ? atomicAdd(p.cand_count + ng, tot) : 0u;
-    }
-    __syncthreads();
-    STEP5_STAMP(2, 3);
-    uint32_t slot = s_base + s_wcnt[warp] + incl - mine;
-    uint64_t* cand = p.cand + ng * kCandCap;
-#pragma unroll
-    for (int u = 0; u < kFilterPerThread; ++u) {
-        const int r = c0 + u * kSplitThreads + threadIdx.x;
-        if (r < c1 && (int)(keys[u] >> (32 - kHistBits)) <= b1) {
-            if (slot < (uint32_t)kCandCap) cand[slot] = ((uint64_t)keys[u] << 32) | (uint32_t)r;
-            ++slot;
-        }
-    }
-}
 
-constexpr int kFinalThreads = 512;
-constexpr int kFinalSlices = 8;  // blocks per (row, group) in the final select
-
-// Final select of the split path: kFinalSlices blocks per (row, group) each gather the
-// same k winners from the candidate list (radix descent in shared memory), then each
-// places only the winners whose id falls in its slice (id mod kFinalSlices), at the rank
-// it counts among all winners.  The last slice to finish reading the candidates leaves
-// the histogram, candidate counter and ticket of its (row, group) zero for the next call.
-__global__ void __launch_bounds__(kFinalThreads) final_select_kernel(ScoreParams p, int P2, int /*unused*/) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint64_t* s_sel = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* s_cand = s_sel + P2;  // kCandCap
-    __shared__ TopkSmem ts;
-    __shared__ int s_last;
-    const int slice = blockIdx.x, g = blockIdx.y, n = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    STEP5_STAMP(3, 0);
-    pdl_wait();
-    pdl_launch_dependents();
-    STEP5_STAMP(3, 1);
-    int b, pos;
-    int R = row_regions(p, n, b, pos);
-    if (R < 0) R = 0;
-    const int64_t ng = (int64_t)n * p.G + g;
-    // the whole candidate buffer is requested together with its count
-    const uint64_t* cand = p.cand + ng * kCandCap;
-    uint64_t cv[kCandCap / kFinalThreads];
-#pragma unroll
-    for (int k = 0; k < kCandCap / kFinalThreads; ++k) cv[k] = __ldcg(cand + k * kFinalThreads + tid);
-    const int c = (int)__ldcg(p.cand_count + ng);
-    const bool from_cand = c <= kCandCap;
-#pragma unroll
-    for (int k = 0; k < kCandCap / kFinalThreads; ++k)
-        if (k * kFinalThreads + tid < c) s_cand[k * kFinalThreads + tid] = cv[k];
-    __syncthreads();
-    if (tid == 0) {
-        const uint32_t t = atomicAdd(p.ticket + ng, 1u);
-        s_last = (t == (uint32_t)(kFinalSlices - 1));
-    }
-    __syncthreads();
-    if (s_last) {
-        uint32_t* gh = p.hist + ng * kHistBins;
-        for (int i = tid; i < kHistBins; i += kFinalThreads) gh[i] = 0;
-        if (tid < kCoarseBins) p.coarse[ng * kCoarseBins + tid] = 0;
+    // ---------------- phase 2: candidates of this block's share
+    if (keep_all) {
+        // the thresholds (and R) of the share's one or two (row, group)s
         if (tid == 0) {
-            p.cand_count[ng] = 0;
-            p.ticket[ng] = 0;
+            int b, pos;
+            const int RA = row_regions(p, ngA / p.G, b, pos);
+            const int RB = row_regions(p, ngB / p.G, b, pos);
+            s_R[0] = RA < 0 ? 0 : RA;
+            s_R[1] = RB < 0 ? 0 : RB;
+            s_thr[0] = wait_threshold(p, ngA, s_gen1[0]);
+            s_thr[1] = ngB != ngA ? wait_threshold(p, ngB, s_gen1[1]) : s_thr[0];
         }
-    }
-    STEP5_STAMP(3, 2);
-    const int take = from_cand
-                         ? block_select_set<kFinalThreads>(CandKeys{s_cand}, c, p.top_k, P2, s_sel, ts)
-                         : block_select_set<kFinalThreads>(ScoreKeys{p.scores + ng * p.r_cap}, R, p.top_k, P2,
-                                                           s_sel, ts);
-    STEP5_STAMP(3, 3);
-    // rank by counting: one warp per winner of this slice, lanes split the comparisons
-    int32_t* ids = p.sel_ids + ng * p.top_k;
-    float* ss = p.sel_scores ? p.sel_scores + ng * p.top_k : nullptr;
-    for (int i = warp; i < take; i += kFinalThreads / 32) {
-        const uint64_t key = s_sel[i];
-        if ((int)((uint32_t)key % kFinalSlices) != slice) continue;
-        uint32_t cnt_less = 0;
-        for (int j = lane; j < take; j += 32) cnt_less += s_sel[j] < key ? 1u : 0u;
+        if (__syncthreads_or(tid == 0 && (s_thr[0] < 0 || s_thr[1] < 0))) {
+            if (tid == 0) raise_status(p.status, kDevTimeout);
+            return;
+        }
+        const int64_t bstart = (int64_t)(ngA + 1) * p.r_cap;  // first position of the second
+        const int len = (int)(xend - xbeg);
+        uint64_t keys[kKeepPer];
+        uint32_t sel = 0, inb = 0, cnt = 0;  // bit u: key u selected / in the second; counts
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cnt_less += __shfl_xor_sync(0xffffffffu, cnt_less, o);
-        if (lane == 0) {
-            ids[cnt_less] = (int32_t)(uint32_t)(key & 0xffffffffu);
-            if (ss) ss[cnt_less] = score_of_desc_key((uint32_t)(key >> 32));
+        for (int u = 0; u < kKeepPer; ++u) {
+            const int i = tid + u * kSplitThreads;
+            keys[u] = 0;
+            if (i < len) {
+                const int64_t x = xbeg + i;
+                const int second = x >= bstart;
+                const int r = (int)(x - (second ? bstart : (int64_t)ngA * p.r_cap));
+                if (r < s_R[second]) {
+                    const uint32_t k = desc_key(s_keep[i]);
+                    if ((int)(k >> (32 - kHistBits)) <= s_thr[second]) {
+                        keys[u] = ((uint64_t)k << 32) | (uint32_t)r;
+                        sel |= 1u << u;
+                        inb |= (uint32_t)second << u;
+                        cnt += second ? 0x10000u : 1u;
+                    }
+                }
+            }
+        }
+        uint32_t tot = 0;
+        uint32_t off = block_excl_scan(cnt, s_w, &tot);
+        if (tid == 0) {
+            const uint32_t ta = tot & 0xffffu, tb = tot >> 16;
+            s_base[0] = ta ? atomicAdd(p.cand_count + ngA, ta) : 0u;
+            s_base[1] = tb ? atomicAdd(p.cand_count + ngB, tb) : 0u;
+        }
+        __syncthreads();
+        uint32_t sa = s_base[0] + (off & 0xffffu), sb = s_base[1] + (off >> 16);
+        uint64_t* ca = p.cand + (int64_t)ngA * kCandCap;
+        uint64_t* cb = p.cand + (int64_t)ngB * kCandCap;
+#pragma unroll
+        for (int u = 0; u < kKeepPer; ++u) {
+            if (sel >> u & 1u) {
+                if (inb >> u & 1u) {
+                    if (sb < (uint32_t)kCandCap) cb[sb] = keys[u];
+                    ++sb;
+                } else {
+                    if (sa < (uint32_t)kCandCap) ca[sa] = keys[u];
+                    ++sa;
+                }
+            }
+        }
+    } else {
+        // long shares: batches of up to kKeep regions of one (row, group), scores re-read
+        Walk fw = walk_start(p, xbeg, xend);
+        int thr_ng = -1;
+        for (;;) {
+            // the batch: consecutive tiles of one (row, group), at most kKeep regions
+            Tile t = next_tile(p, fw);
+            if (!t.valid) break;
+            int c1 = t.c1;
+            while (c1 - t.c0 + kTileRegions <= kKeep && fw.left > 0 && fw.ng == t.ng && fw.r < fw.cR) {
+                const Tile u = next_tile(p, fw);
+                c1 = u.c1;
+            }
+            if (t.ng != thr_ng) {
+                if (tid == 0) s_thr[0] = wait_threshold(p, t.ng, s_gen1[t.ng - ngA]);
+                if (__syncthreads_or(tid == 0 && s_thr[0] < 0)) {
+                    if (tid == 0) raise_status(p.status, kDevTimeout);
+                    return;
+                }
+                thr_ng = t.ng;
+            }
+            const float* sc = p.scores + (int64_t)t.ng * p.r_cap;
+            uint64_t keys[kKeepPer];
+            uint32_t sel = 0, cnt = 0;
+            const int T = s_thr[0];
+#pragma unroll
+            for (int u = 0; u < kKeepPer; ++u) {
+                const int r = t.c0 + tid + u * kSplitThreads;
+                keys[u] = 0;
+                if (r < c1) {
+                    const uint32_t k = desc_key(__ldcg(sc + r));
+                    if ((int)(k >> (32 - kHistBits)) <= T) {
+                        keys[u] = ((uint64_t)k << 32) | (uint32_t)r;
+                        sel |= 1u << u;
+                        ++cnt;
+                    }
+                }
+            }
+            uint32_t tot = 0;
+            uint32_t off = block_excl_scan(cnt, s_w, &tot);
+            if (tid == 0) s_base[0] = tot ? atomicAdd(p.cand_count + t.ng, tot) : 0u;
+            __syncthreads();
+            uint32_t slot2 = s_base[0] + off;
+            uint64_t* cl = p.cand + (int64_t)t.ng * kCandCap;
+#pragma unroll
+            for (int u = 0; u < kKeepPer; ++u) {
+                if (sel >> u & 1u) {
+                    if (slot2 < (uint32_t)kCandCap) cl[slot2] = keys[u];
+                    ++slot2;
+                }
+            }
+            __syncthreads();  // s_thr / s_base reused by the next batch
         }
     }
-    STEP5_STAMP(3, 4);
-    if (slice == 0) {
-        for (int i = take + tid; i < p.top_k; i += kFinalThreads) {
-            ids[i] = -1;
-            if (ss) ss[i] = -INFINITY;
-        }
-        if (tid == 0) p.sel_count[ng] = take;
+    STEP5_STAMP(1, 12);
+    // ---------------- phase 3: ranks, once every block of the (row, group) has written
+    // its candidates (arrive at every (row, group) of the share first, then wait)
+    for (int ng = ngA; ng <= ngB; ++ng) {
+        __syncthreads();  // the block's candidate writes come before its arrival
+        if (tid == 0) s_gen2[ng - ngA] = arrive_gen(p.bar2 + ng, (uint32_t)seg_blocks(ng));
     }
+    for (int ng = ngA; ng <= ngB; ++ng) {
+        __syncthreads();
+        if (__syncthreads_or(tid == 0 && !wait_gen(p.bar2 + ng, s_gen2[ng - ngA]))) {
+            if (tid == 0) raise_status(p.status, kDevTimeout);
+            return;
+        }
+        STEP5_STAMP(1, 13);
+        rank_segment(p, ng, blockIdx.x - seg_first(ng), seg_blocks(ng), ring, s_w);
+    }
+    STEP5_STAMP(1, 14);
 }
 
 int pow2_at_least(int x) {
     int p2 = 32;
     while (p2 < x) p2 <<= 1;
     return p2;
-}
-
-template <class K>
-cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
-                      const ScoreParams& p) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 template <class K>
@@ -983,30 +1370,49 @@ cudaError_t launch_map(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 template <int HPG>
 cudaError_t split_for(const ScoreParams& p_in, const CUtensorMap& smap, cudaStream_t stream, bool pdl) {
-    ScoreParams p = p_in;
-    // two persistent blocks per SM, each an even share of the regions
-    const int64_t tiles = ((int64_t)p.N * p.G * p.r_cap + kTileRegions - 1) / kTileRegions;
-    int64_t grid = 2 * (int64_t)p.num_sms;
-    if (grid > tiles) grid = tiles;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e0 = cudaFuncSetAttribute(score_hist_kernel<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // one persistent launch with every block resident: as many blocks as fit at once
+    // (two per SM), at most one per tile
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        cudaError_t e0 = cudaFuncSetAttribute(score_select_kernel<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               (int)kScoreSmem);
         if (e0 != cudaSuccess) return e0;
-        attr = true;
+        int b = 0;
+        e0 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, score_select_kernel<HPG>, kSplitThreads, kScoreSmem);
+        if (e0 != cudaSuccess) return e0;
+        if (b < 1) return cudaErrorInvalidConfiguration;
+        per_sm = b < 2 ? b : 2;
     }
-    cudaError_t e = launch_map(score_hist_kernel<HPG>, dim3((unsigned)grid), dim3(kSplitThreads), kScoreSmem,
-                               stream, pdl, smap, p);
-    if (e != cudaSuccess) return e;
-    const int fchunks = (p.r_cap + p.regions_per_cta - 1) / p.regions_per_cta;
-    e = launch_ex(filter_kernel, dim3(fchunks, p.G, p.N), dim3(kSplitThreads), 0, stream, true, p);
-    if (e != cudaSuccess) return e;
-    const int P2 = pow2_at_least(p.top_k);
-    const size_t smem = (size_t)P2 * 8 + (size_t)kCandCap * 8;
-    e = cudaFuncSetAttribute(final_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_ex2(final_select_kernel, dim3(kFinalSlices, p.G, p.N), dim3(kFinalThreads), smem, stream, true,
-                      p, P2, 0);
+    // rows in batches small enough that a block's share covers at most kMaxShareSegs
+    // (row, group)s
+    const int64_t full_grid = (int64_t)per_sm * p_in.num_sms;
+    int64_t rows_per = (full_grid * (kMaxShareSegs - 2)) / p_in.G;
+    if (rows_per < 1) rows_per = 1;
+    for (int n0 = 0; n0 < p_in.N; n0 += (int)rows_per) {
+        ScoreParams p = p_in;
+        p.N = (int)((p_in.N - n0) < rows_per ? (p_in.N - n0) : rows_per);
+        const int64_t g0 = (int64_t)n0 * p.G;  // first (row, group) of the batch
+        p.idx_q = p_in.idx_q + (int64_t)n0 * p.idx_heads * 64;
+        p.w = p_in.w + (int64_t)n0 * p.idx_heads;
+        p.row_seq = p_in.row_seq + n0;
+        p.row_pos = p_in.row_pos + n0;
+        p.sel_ids = p_in.sel_ids + g0 * p.top_k;
+        p.sel_count = p_in.sel_count + g0;
+        p.sel_scores = p_in.sel_scores ? p_in.sel_scores + g0 * p.top_k : nullptr;
+        p.scores = p_in.scores + g0 * p.r_cap;
+        p.hist = p_in.hist + g0 * kHistBins;
+        p.cand_count = p_in.cand_count + g0;
+        p.cand = p_in.cand + g0 * kCandCap;
+        p.arrive1 = p_in.arrive1 + g0;
+        p.thr = p_in.thr + g0;
+        p.bar2 = p_in.bar2 + g0;
+        const int64_t tiles = ((int64_t)p.N * p.G * p.r_cap + kTileRegions - 1) / kTileRegions;
+        const int64_t grid = full_grid < tiles ? full_grid : tiles;
+        cudaError_t e = launch_map(score_select_kernel<HPG>, dim3((unsigned)grid), dim3(kSplitThreads), kScoreSmem,
+                                   stream, pdl && n0 == 0, smap, p);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace

@@ -80,7 +80,7 @@ void attn_plan(const step5_geometry* g, int N, int* cluster_out, int* eps_out, b
     if (items < sms) {
         const int per_item = (int)(sms / items);
         while (cluster * 2 <= kMaxCluster && cluster * 2 <= per_item) cluster *= 2;
-        while (cluster > 1 && attention_smem_bytes(cluster, hq_g) > 232448) cluster /= 2;
+        while (cluster > 1 && attention_smem_bytes(cluster, hq_g) + kAttnStaticSmem > 232448) cluster /= 2;
         if (query_device)
             while (cluster > 1 && attention_max_active_clusters(cluster, hq_g) < items) cluster /= 2;
     }
@@ -93,7 +93,7 @@ void attn_plan(const step5_geometry* g, int N, int* cluster_out, int* eps_out, b
 // Workspace of step (2)-(3).  The zero-maintained parts (histograms and counters) come
 // first.
 struct Layout {
-    size_t hist, cand_count, ticket, coarse, scores, cand, end;
+    size_t hist, cand_count, arrive1, thr, bar2, scores, cand, end;
 };
 
 Layout layout(const step5_geometry* g, int N, int r_cap) {
@@ -102,9 +102,10 @@ Layout layout(const step5_geometry* g, int N, int r_cap) {
     const size_t ng = (size_t)N * G;
     L.hist = 0;
     L.cand_count = align256(L.hist + ng * kHistBins * 4);
-    L.ticket = align256(L.cand_count + ng * 4);
-    L.coarse = align256(L.ticket + ng * 4);
-    L.scores = align256(L.coarse + ng * kCoarseBins * 4);
+    L.arrive1 = align256(L.cand_count + ng * 4);
+    L.thr = align256(L.arrive1 + ng * 4);
+    L.bar2 = align256(L.thr + ng * 4);
+    L.scores = align256(L.bar2 + ng * 4);
     L.cand = align256(L.scores + ng * (size_t)(r_cap > 0 ? r_cap : 0) * 4);
     L.end = align256(L.cand + ng * kCandCap * 8);
     return L;
@@ -125,16 +126,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-// 2-D view [rows][128] bf16 of a [B][G][t_cap][128] cache; box 64 dims x 8 rows,
-// 128-byte swizzle.
+// 3-D view of a [B][G][t_cap][128] bf16 cache as (64 dims, rows, 2 halves of a row):
+// one box (64 x 8 x 2) is a whole 8-token region, landing in shared memory as two
+// 1 KB half tiles [half][token][64 dims] with 128-byte swizzle.
 bool encode_cache_map(CUtensorMap* map, const void* base, uint64_t rows) {
     auto enc = get_encode();
     if (!enc) return false;
-    cuuint64_t dims[2] = {128, rows};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {64, 8};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    cuuint64_t dims[3] = {64, rows, 2};
+    cuuint64_t strides[2] = {256, 128};  // bytes: next row, next half
+    cuuint32_t box[3] = {64, 8, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -376,8 +378,9 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     p.hist = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.hist);
     p.cand_count = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.cand_count);
     p.cand = fused ? nullptr : reinterpret_cast<uint64_t*>(ws + L.cand);
-    p.ticket = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.ticket);
-    p.coarse = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.coarse);
+    p.arrive1 = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.arrive1);
+    p.thr = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.thr);
+    p.bar2 = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.bar2);
     p.num_sms = num_sms();
     p.status = st;
     p.N = N;
@@ -389,7 +392,6 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     p.r_cap = r_cap;
     p.rope_dims = rope_cos_bf16 ? geom->rope_dims : 0;
     p.top_k = geom->top_k;
-    p.regions_per_cta = 1024;  // filter pass: 4 scores per thread
     cudaError_t e;
     if (fused) {
         e = launch_score_fused(p, (cudaStream_t)stream, use_pdl());
