@@ -28,7 +28,7 @@ __all__ = [
     "step5_region_summarize", "step5_index_score_topk", "step5_sparse_attn",
     "step5_index_score_topk_noalloc",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
-    "step5_set_select_path", "step5_select_path_for", "step5_status_string", "step5_convert_bf16_to_e4m3",
+    "step5_set_select_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_status_string", "step5_convert_bf16_to_e4m3",
     "Workspace", "decode_step",
 ]
 
@@ -96,6 +96,7 @@ def load():
         "step5_workspace_init": (i32, [P, sz, P]),
         "step5_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32), P]),
         "step5_set_select_path": (i32, [i32]),
+        "step5_set_prologue_overlap": (i32, [i32]),
         "step5_select_path_for": (i32, [G, i32, i32]),
         "step5_status_string": (ctypes.c_char_p, [i32]),
         "step5_convert_bf16_to_e4m3": (i32, [P, P, i64, P]),
@@ -135,6 +136,12 @@ def step5_status_string(status: int) -> str:
 def step5_set_select_path(mode: int) -> int:
     """0 = automatic, 1 = one block per (row, group), 2 = histogram split path."""
     return load().step5_set_select_path(mode)
+
+
+def step5_set_prologue_overlap(enable: int) -> int:
+    """1 = the scoring kernel reads its non-summary inputs before waiting for the launch
+    before it (which must not write them); 0 = every read waits.  Returns the previous."""
+    return load().step5_set_prologue_overlap(enable)
 
 
 def step5_select_path_for(geom, N: int, r_cap: int) -> int:
@@ -241,8 +248,14 @@ def decode_step(geom, t: dict, ws: Workspace, sel_ids, sel_count, out, max_regio
         step5_region_summarize(geom, t["idx_k"], t["idx_z"], t["cos"], t["sin"], t["sum_begin"],
                                t["sum_end"], t["summaries"],
                                max_regions_per_seq=max_regions_per_seq, stream=stream)
-    step5_index_score_topk(geom, t["idx_q"], t["w"], t["row_seq"], t["row_pos"], t["cos"],
-                           t["sin"], t["summaries"], sel_ids, sel_count, ws.tensor,
-                           t_cap=t["idx_k"].shape[2], stream=stream)
+    # the launch just before the scoring call is the summary kernel (or, without it, the
+    # previous step's attention), which writes none of the scoring inputs but summaries
+    prev = step5_set_prologue_overlap(1 if summarize else 0)
+    try:
+        step5_index_score_topk(geom, t["idx_q"], t["w"], t["row_seq"], t["row_pos"], t["cos"],
+                               t["sin"], t["summaries"], sel_ids, sel_count, ws.tensor,
+                               t_cap=t["idx_k"].shape[2], stream=stream)
+    finally:
+        step5_set_prologue_overlap(prev)
     step5_sparse_attn(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
                       sel_ids, sel_count, out, ws.tensor, stream=stream)

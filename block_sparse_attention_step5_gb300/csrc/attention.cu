@@ -38,6 +38,7 @@ constexpr int kMergeFloatsPerWarp = 16 * 128 + 32;    // O[16][128], m[16], l[16
 constexpr int kBarBytes = kPairBufs * 8;
 constexpr int kSlotFloats = 130;                      // m, l, o[128] of one head row
 static_assert(kAttnWarps * kMergeFloatsPerWarp * 4 <= kStageBytes, "warp merge area must fit");
+static_assert((kMaxTopK + 1) * 4 + (kAttnWarps + kMaxCluster + 2) * 16 * 4 <= kAttnStaticSmem, "static shared memory");
 
 // Dynamic shared memory: [stage area | barriers | push slots C x hq_g x 130 floats]
 size_t attn_smem_bytes(int cluster, int hq_g) {
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
 
     // the row's position, pick count and every picked id of this block's run, in one
     // round trip
-    __shared__ int32_t s_ids[kAttnStaticSmem / 4];
+    __shared__ int32_t s_ids[kMaxTopK + 1];
     const int32_t* ids = p.sel_ids + ng * p.top_k;
     const int e0 = split * p.entries_per_split;
     for (int i = tid; i < p.entries_per_split; i += kThreads)
@@ -107,9 +108,9 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     const int own_tokens = pos - own * 8 + 1;
     const int E = cnt + 1;
     const int e1 = min(E, e0 + p.entries_per_split);
+    const int64_t row_base = ((int64_t)b * p.G + g) * p.t_cap;
     const int npairs = e1 > e0 ? (e1 - e0 + 1) >> 1 : 0;
     const int nmy = npairs > warp ? (npairs - warp + kAttnWarps - 1) / kAttnWarps : 0;
-    const int64_t row_base = ((int64_t)b * p.G + g) * p.t_cap;
 
     const int nst = warp == 0 ? kAttnStages + 1 : kAttnStages;  // this warp's pair buffers
     const int wfirst = warp == 0 ? 0 : warp * kAttnStages + 1;
@@ -327,52 +328,83 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     __syncthreads();
     STEP5_STAMP(4, 5);
 
-    // this block's state; thread (rpar, d) handles dim d of rows rpar, rpar + 2, ...
+    // per-row max, warp weights and sum, once per (row, warp) by warp 0 (its lanes take
+    // 4 rows x 8 warps per pass); then thread (rpar, d) combines dim d of rows rpar,
+    // rpar + 2, ... with those weights
+    __shared__ float s_wsc[kAttnWarps][16], s_M[16], s_L[16];
     const int d = tid & 127, rpar = tid >> 7;
     const float* mall = reinterpret_cast<const float*>(smem);
+    if (warp == 0) {
+        for (int r0 = 0; r0 < hq_g; r0 += 32 / kAttnWarps) {
+            const int r = r0 + lane / kAttnWarps, w = lane % kAttnWarps;
+            const bool ok = r < hq_g;
+            const float m = ok ? mall[w * kMergeFloatsPerWarp + 2048 + r] : -INFINITY;
+            float M = m;
+#pragma unroll
+            for (int o = 1; o < kAttnWarps; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float sc = exp2f(m - ((M == -INFINITY) ? 0.0f : M));
+            float L = ok ? mall[w * kMergeFloatsPerWarp + 2048 + 16 + r] * sc : 0.0f;
+#pragma unroll
+            for (int o = 1; o < kAttnWarps; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+            if (ok) {
+                s_wsc[w][r] = sc;
+                if (w == 0) {
+                    s_M[r] = M;
+                    s_L[r] = L;
+                }
+            }
+        }
+    }
+    __syncthreads();
     const uint32_t my_slot = smem_u32(slots + (size_t)cluster_ctarank() * hq_g * kSlotFloats);
     for (int r = rpar; r < hq_g; r += 2) {
-        float M = -INFINITY;
+        float O = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mall[w * kMergeFloatsPerWarp + 2048 + r]);
-        const float base = (M == -INFINITY) ? 0.0f : M;
-        float L = 0.0f, O = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) {
-            const float sc = exp2f(mall[w * kMergeFloatsPerWarp + 2048 + r] - base);
-            L += mall[w * kMergeFloatsPerWarp + 2048 + 16 + r] * sc;
-            O += mall[w * kMergeFloatsPerWarp + r * 128 + d] * sc;
-        }
+        for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * 128 + d] * s_wsc[w][r];
         if (C == 1) {
-            p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / L);
+            p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / s_L[r]);
         } else {
             // push into block 0's slot for this block (remote stores, no waiting)
             const uint32_t a = map_cluster(my_slot + (uint32_t)(r * kSlotFloats) * 4u, 0u);
             if (d == 0) {
-                st_cluster_f32(a, M);
-                st_cluster_f32(a + 4, L);
+                st_cluster_f32(a, s_M[r]);
+                st_cluster_f32(a + 4, s_L[r]);
             }
             st_cluster_f32(a + (uint32_t)(2 + d) * 4u, O);
         }
     }
     if (C == 1) return;
+    STEP5_STAMP(4, 11);
     cluster_sync();  // every push is visible to block 0
     STEP5_STAMP(4, 6);
     if (cluster_ctarank() != 0) return;
 
-    // ---- block 0: merge the C slots in rank order, from its own shared memory
-    for (int r = rpar; r < hq_g; r += 2) {
-        float M = -INFINITY;
-        for (int c = 0; c < C; ++c) M = fmaxf(M, slots[((size_t)c * hq_g + r) * kSlotFloats]);
-        const float base = (M == -INFINITY) ? 0.0f : M;
-        float L = 0.0f, O = 0.0f;
-        for (int c = 0; c < C; ++c) {
-            const float* sl = slots + ((size_t)c * hq_g + r) * kSlotFloats;
-            const float sc = exp2f(sl[0] - base);
-            L += sl[1] * sc;
-            O += sl[2 + d] * sc;
+    // ---- block 0: merge the C slots in rank order, from its own shared memory: the
+    // weight of every (slot, row) once (lane groups of C per row), then dim d of each row
+    __shared__ float s_csc[kMaxCluster][16];
+    if (tid < ((hq_g * C + 31) & ~31)) {
+        const bool ok = tid < hq_g * C;
+        const int r = tid / C, c = tid - r * C;
+        const float* sl = slots + ((size_t)c * hq_g + r) * kSlotFloats;
+        const float m = ok ? sl[0] : -INFINITY;
+        float M = m;
+        for (int o = 1; o < C; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float sc = exp2f(m - ((M == -INFINITY) ? 0.0f : M));
+        float L = ok ? sl[1] * sc : 0.0f;
+        for (int o = 1; o < C; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (ok) {
+            s_csc[c][r] = sc;
+            if (c == 0) s_L[r] = L;
         }
-        p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / L);
+    }
+    __syncthreads();
+    STEP5_STAMP(4, 10);
+    for (int r = rpar; r < hq_g; r += 2) {
+        float O = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) O += slots[((size_t)c * hq_g + r) * kSlotFloats + 2 + d] * s_csc[c][r];
+        p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / s_L[r]);
     }
     STEP5_STAMP(4, 7);
 }

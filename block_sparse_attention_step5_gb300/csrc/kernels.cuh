@@ -30,6 +30,7 @@ constexpr int kHistBins = 1 << kHistBits;
 constexpr int kCandCap = 2048;          // candidates per (row, group) on the split path
 constexpr int kFusedMaxRegions = 16384; // regions a fused block keeps in shared memory
 constexpr int kMaxTopK = 2048;
+constexpr int kSplitTileRegions = 1024;  // regions of one split-path scoring tile
 
 struct ScoreParams {
     const uint16_t* idx_q;   // [N][idx_heads][64]
@@ -51,7 +52,8 @@ struct ScoreParams {
     uint32_t* bar2;          // [N][G] generation | arrivals      (split path)
     uint32_t* status;
     int N, B, G, idx_heads, hpg, t_cap, r_cap, rope_dims, top_k;
-    int num_sms;             // split path: persistent blocks (two per SM)
+    int num_sms;             // split path: persistent blocks (one per SM)
+    int overlap_prologue;    // split path: read the non-summary inputs before the launch wait
 };
 cudaError_t launch_score_fused(const ScoreParams& p, cudaStream_t stream, bool pdl);
 // Split path: one persistent launch (score, candidates, ranks) with grid barriers.
@@ -81,6 +83,6 @@ cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const
 // Clusters of `cluster` attention blocks that can be resident at once (0 if unknown).
 int attention_max_active_clusters(int cluster, int hq_g);
 size_t attention_smem_bytes(int cluster, int hq_g);  // dynamic part
-constexpr size_t kAttnStaticSmem = (kMaxTopK + 1) * 4;  // the block's picked ids
+constexpr size_t kAttnStaticSmem = (kMaxTopK + 1) * 4 + 4096;  // picked ids + merge weights
 
 }  // namespace step5

@@ -473,19 +473,24 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
 
 // ----------------------------------------------------------------- split path
 
-constexpr int kSplitThreads = 256;
+constexpr int kSplitThreads = 512;                     // one block per SM
+constexpr int kSplitWarps = kSplitThreads / 32;
+constexpr int kBinsPerThread = kHistBins / kSplitThreads;  // histogram bins a thread owns
 
 // ----------------------------------------------------------------- split path scoring
 //
-// Persistent blocks (two per SM) each walk an even share of the flattened (row, group,
+// Persistent blocks (one per SM) each walk an even share of the flattened (row, group,
 // region) space in tiles of kTileRegions consecutive regions of one (row, group),
 // contiguous in the summary store and fetched by TMA into a 2-stage shared-memory ring
 // while the previous tile is scored.  Each run of tiles of one (row, group) adds its
 // shared-memory histogram to the global one.
 
-constexpr int kTileRegions = 512;                 // 32 KB of summaries
+constexpr int kTileRegions = 2 * kSplitThreads;   // 64 KB of summaries, two rows per thread
+static_assert(kTileRegions == kSplitTileRegions, "host and device tile sizes differ");
 constexpr int kTileBytes = kTileRegions * 64;
-constexpr int kTileU = kTileRegions / 64;         // regions per thread per tile (8)
+constexpr int kBoxRows = 256;                     // rows of one summary tensor-map box
+constexpr int kSlots = kSplitThreads / 4;         // region slots of the 4-lane layout
+constexpr int kTileU = kTileRegions / kSlots;     // regions per slot per tile (8)
 constexpr int kScoreStages = 2;
 constexpr size_t kScoreSmem = kScoreStages * kTileBytes + 1024;
 
@@ -548,7 +553,7 @@ __device__ __forceinline__ Tile next_tile(const ScoreParams& p, Walk& k) {
     return t;
 }
 
-// Scores one staged tile: thread (slot, qd) covers regions u * 64 + slot, u < kTileU;
+// Scores one staged tile: thread (slot, qd) covers regions u * kSlots + slot, u < kTileU;
 // lane qd of each region quad keeps the score and histogram update of every fourth
 // region.  FULL: the tile holds kTileRegions regions (no bounds checks).
 template <int HPG, bool FULL>
@@ -559,12 +564,12 @@ __device__ __forceinline__ void score_tile(const QFrag<HPG>& f, const uint4* til
         float sc[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int lr = (u4 + u) * 64 + slot;
+            const int lr = (u4 + u) * kSlots + slot;
             const uint4 v = (FULL || lr < nreg) ? tile[lr * 4 + qd] : make_uint4(0, 0, 0, 0);
             sc[u] = score_from_vec<HPG>(f, v);
         }
         const float mysc = qd == 0 ? sc[0] : qd == 1 ? sc[1] : qd == 2 ? sc[2] : sc[3];
-        const int lr = (u4 + qd) * 64 + slot;
+        const int lr = (u4 + qd) * kSlots + slot;
         if (FULL || lr < nreg) {
             scores[lr] = mysc;
             if (keep) keep[lr] = mysc;
@@ -705,22 +710,22 @@ __device__ __forceinline__ float score_row1(const uint4 (&a)[4], const float4* q
     return finish_score4(A, w);
 }
 
-// One thread per region (HPG == 4): thread t scores rows t and t + 256 of a tile that
-// arrived as two 256-row boxes through the summaries' tensor map with 64-byte swizzle
+// One thread per region (HPG == 4): thread t scores rows t and t + kSplitThreads of a
+// tile that arrived as 256-row boxes through the summaries' tensor map with 64-byte swizzle
 // (16-byte chunk k of row r sits at chunk k ^ ((r >> 1) & 3)), so the 8 rows a quarter
 // warp reads at once fall in 8 different bank groups.  Rows at or past nreg are skipped
 // a warp at a time.
 __device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, const float4* q4,
                                                 const float (&w)[4], float* scores, float* keep,
                                                 uint32_t* s_hist) {
-    const int t = threadIdx.x;  // 0..255
+    const int t = threadIdx.x;
     const int wbase = t & ~31;
     if (wbase >= nreg) return;
     const int sw = (t >> 1) & 3;
     const uint4* ra = reinterpret_cast<const uint4*>(tile + t * 64);
     uint4 a[4];
-    if (wbase + 256 < nreg) {
-        const uint4* rb = reinterpret_cast<const uint4*>(tile + 16384 + t * 64);
+    if (wbase + kSplitThreads < nreg) {
+        const uint4* rb = reinterpret_cast<const uint4*>(tile + kSplitThreads * 64 + t * 64);
         uint4 b[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -729,12 +734,12 @@ __device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, c
         }
         float sa, sb;
         score_rows2(a, b, q4, w, sa, sb);
-        scores[t] = sa;  // t < 256 < nreg
+        scores[t] = sa;  // t < kSplitThreads < nreg
         if (keep) keep[t] = sa;
         atomicAdd(&s_hist[desc_key(sa) >> (32 - kHistBits)], 1u);
-        if (t + 256 < nreg) {
-            scores[t + 256] = sb;
-            if (keep) keep[t + 256] = sb;
+        if (t + kSplitThreads < nreg) {
+            scores[t + kSplitThreads] = sb;
+            if (keep) keep[t + kSplitThreads] = sb;
             atomicAdd(&s_hist[desc_key(sb) >> (32 - kHistBits)], 1u);
         }
     } else {
@@ -784,14 +789,14 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_w, u
 }
 
 // Fine bin holding the K-th smallest key of a (row, group) with R regions, from its
-// whole fine histogram (one 16 KB read shared by the block: each thread owns 16
-// consecutive bins); kHistBins - 1 when R <= K or the histogram counts fewer than K
+// whole histogram (one 16 KB read shared by the block: each thread owns kBinsPerThread
+// consecutive bins, h); kHistBins - 1 when R <= K or the histogram counts fewer than K
 // keys.  Called by the whole block; the result lands in *s_out.
-__device__ void block_threshold(const uint4 (&h)[4], int R, int K, uint32_t* s_w, int* s_out) {
+__device__ void block_threshold(const uint4 (&h)[kBinsPerThread / 4], int R, int K, uint32_t* s_w, int* s_out) {
     if (threadIdx.x == 0) *s_out = kHistBins - 1;
-    uint32_t loc[16];
+    uint32_t loc[kBinsPerThread];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kBinsPerThread / 4; ++q) {
         loc[4 * q] = h[q].x;
         loc[4 * q + 1] = h[q].y;
         loc[4 * q + 2] = h[q].z;
@@ -799,18 +804,18 @@ __device__ void block_threshold(const uint4 (&h)[4], int R, int K, uint32_t* s_w
     }
     uint32_t sum = 0;
 #pragma unroll
-    for (int q = 0; q < 16; ++q) sum += loc[q];
+    for (int q = 0; q < kBinsPerThread; ++q) sum += loc[q];
     uint32_t tot = 0;
     const uint32_t before = block_excl_scan(sum, s_w, &tot);  // synchronises (after the default)
     if (R > K && before < (uint32_t)K && (uint32_t)K <= before + sum) {
         uint32_t c = before;
-        int bin = 15;
+        int bin = kBinsPerThread - 1;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            if (bin == 15 && c + loc[q] >= (uint32_t)K) bin = q;
+        for (int q = 0; q < kBinsPerThread; ++q) {
+            if (bin == kBinsPerThread - 1 && c + loc[q] >= (uint32_t)K) bin = q;
             c += loc[q];
         }
-        *s_out = threadIdx.x * 16 + bin;
+        *s_out = threadIdx.x * kBinsPerThread + bin;
     }
     __syncthreads();
 }
@@ -870,16 +875,16 @@ __device__ __forceinline__ bool wait_gen(const uint32_t* word, uint32_t gen) {
 // release semantics.
 __device__ void publish_threshold(const ScoreParams& p, int ng, uint32_t gen, uint32_t* s_w, int* s_tmp) {
     const int tid = threadIdx.x;
-    uint4* gh = reinterpret_cast<uint4*>(p.hist + (int64_t)ng * kHistBins) + tid * 4;
-    uint4 h[4];
+    uint4* gh = reinterpret_cast<uint4*>(p.hist + (int64_t)ng * kHistBins) + tid * (kBinsPerThread / 4);
+    uint4 h[kBinsPerThread / 4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) h[q] = __ldcg(gh + q);
+    for (int q = 0; q < kBinsPerThread / 4; ++q) h[q] = __ldcg(gh + q);
     int b, pos;
     int R = row_regions(p, ng / p.G, b, pos);
     if (R < 0) R = 0;
     block_threshold(h, R, p.top_k, s_w, s_tmp);  // ends with a __syncthreads
 #pragma unroll
-    for (int q = 0; q < 4; ++q) gh[q] = make_uint4(0, 0, 0, 0);
+    for (int q = 0; q < kBinsPerThread / 4; ++q) gh[q] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     if (tid == 0) {
         p.arrive1[ng] = 0;
@@ -900,7 +905,7 @@ __device__ int wait_threshold(const ScoreParams& p, int ng, uint32_t gen) {
 
 // Ranks of the candidates of (row, group) ng, after every candidate is written: block
 // `sub` of the nb blocks covering it takes chunks of 32 candidates (one per lane), and
-// each warp counts the smaller keys in its eighth of the list; a candidate ranked below
+// each warp counts the smaller keys in its share of the list; a candidate ranked below
 // K is written at its rank.  Block 0 writes the padding and the count, or, when the
 // list overflowed, selects from every score of the row.
 __device__ void rank_segment(const ScoreParams& p, int ng, int sub, int nb, uint8_t* ring, uint32_t* s_w) {
@@ -909,7 +914,7 @@ __device__ void rank_segment(const ScoreParams& p, int ng, int sub, int nb, uint
     const int n = ng / p.G;
     // the count and the first slots of the list are requested at once
     const uint64_t* cl = p.cand + (int64_t)ng * kCandCap;
-    constexpr int kSpec = 4;  // slots per thread read before the count is known
+    constexpr int kSpec = kCandCap / kSplitThreads;  // slots per thread read before the count is known
     uint64_t cv[kSpec];
     const bool works = sub * 32 < kCandCap;
 #pragma unroll
@@ -939,7 +944,7 @@ __device__ void rank_segment(const ScoreParams& p, int ng, int sub, int nb, uint
             if (u * kSplitThreads + tid < C) s_keys[u * kSplitThreads + tid] = cv[u];
         for (int i = kSpec * kSplitThreads + tid; i < C; i += kSplitThreads) s_keys[i] = __ldcg(cl + i);
         __syncthreads();
-        const int j0 = (int)((int64_t)C * warp / 8), j1 = (int)((int64_t)C * (warp + 1) / 8);
+        const int j0 = (int)((int64_t)C * warp / kSplitWarps), j1 = (int)((int64_t)C * (warp + 1) / kSplitWarps);
         for (int c0 = sub * 32; c0 < C; c0 += nb * 32) {
             const int idx = c0 + lane;
             const uint64_t key = idx < C ? s_keys[idx] : ~0ull;
@@ -950,7 +955,7 @@ __device__ void rank_segment(const ScoreParams& p, int ng, int sub, int nb, uint
             if (warp == 0 && idx < C) {
                 uint32_t rank = 0;
 #pragma unroll
-                for (int w = 0; w < 8; ++w) rank += s_w[w * 32 + lane];
+                for (int w = 0; w < kSplitWarps; ++w) rank += s_w[w * 32 + lane];
                 if (rank < (uint32_t)K) {
                     ids[rank] = (int32_t)(uint32_t)(key & 0xffffffffu);
                     if (ss) ss[rank] = score_of_desc_key((uint32_t)(key >> 32));
@@ -969,9 +974,9 @@ __device__ void rank_segment(const ScoreParams& p, int ng, int sub, int nb, uint
     }
 }
 
-constexpr int kKeep = 2048;                      // scores of a block's range kept on chip
+constexpr int kKeep = 4096;                      // scores of a block's range kept on chip
 constexpr int kMaxShareSegs = 32;                // (row, group)s one block's share may cover
-constexpr int kKeepPer = kKeep / kSplitThreads;  // 8 per thread
+constexpr int kKeepPer = kKeep / kSplitThreads;
 constexpr int kRankWarps = kSplitThreads / 32;
 
 // Split path, one persistent launch (every block resident):
@@ -986,7 +991,7 @@ constexpr int kRankWarps = kSplitThreads / 32;
 // generations, so nothing needs clearing between calls.  A share covers at most
 // kMaxShareSegs (row, group)s (the host launches row batches).
 template <int HPG>
-__global__ void __launch_bounds__(kSplitThreads, 2) score_select_kernel(const __grid_constant__ CUtensorMap smap,
+__global__ void __launch_bounds__(kSplitThreads, 1) score_select_kernel(const __grid_constant__ CUtensorMap smap,
                                                                         ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = align_smem(smem_raw, 1024);
@@ -1009,7 +1014,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_select_kernel(const __
     for (int i = tid; i < kHistBins; i += kSplitThreads) s_hist[i] = 0;
     STEP5_STAMP(1, 0);
     __syncthreads();
-    pdl_wait();
+    // With overlap_prologue the launch before this one writes none of the query,
+    // weight, row and rope inputs, so they are read before waiting for it (only the
+    // summaries are); otherwise every read waits.
+    if (!p.overlap_prologue) pdl_wait();
     STEP5_STAMP(1, 1);
     // this block's even share of the flattened (row, group, region) space
     const int NG = p.N * p.G;
@@ -1042,11 +1050,12 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_select_kernel(const __
     auto issue = [&](const Tile& x, int st) {
         if (tid == 0) {
             if constexpr (HPG == 4) {
-                // two full boxes (rows past the tensor end arrive as zeros)
+                // full boxes (rows past the tensor end arrive as zeros)
                 const int y = (int)(((int64_t)x.b * p.G + x.g) * p.r_cap + x.c0);
                 mbar_arrive_expect_tx(&s_bar[st], (uint32_t)kTileBytes);
-                tma_load_2d(ring + st * kTileBytes, &smap, &s_bar[st], 0, y);
-                tma_load_2d(ring + st * kTileBytes + kTileBytes / 2, &smap, &s_bar[st], 0, y + kTileRegions / 2);
+#pragma unroll
+                for (int k = 0; k < kTileRegions / kBoxRows; ++k)
+                    tma_load_2d(ring + st * kTileBytes + k * kBoxRows * 64, &smap, &s_bar[st], 0, y + k * kBoxRows);
             } else {
                 const uint32_t bytes = (uint32_t)(x.c1 - x.c0) * 64u;
                 mbar_arrive_expect_tx(&s_bar[st], bytes);
@@ -1055,11 +1064,18 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_select_kernel(const __
             }
         }
     };
-    // two tiles in flight: `cur` in stage st, `nxt` in stage st ^ 1
-    Tile cur = next_tile(p, wk);
-    if (cur.valid) issue(cur, 0);
-    Tile nxt = next_tile(p, wk);
-    if (nxt.valid) issue(nxt, 1);
+    // Thread 0 walks the share; the descriptors of the tiles in the two stages live in
+    // shared memory (the other threads only read them).
+    __shared__ Tile s_tile[kScoreStages];
+    if (tid == 0) {
+        s_tile[0] = next_tile(p, wk);
+        s_tile[1] = next_tile(p, wk);
+    }
+    if (p.overlap_prologue) pdl_wait();
+    if (tid == 0) {
+        if (s_tile[0].valid) issue(s_tile[0], 0);
+        if (s_tile[1].valid) issue(s_tile[1], 1);
+    }
     finish_query<HPG>(p, r0, o0, s_qb[0]);
     if (staged1 >= 0) finish_query<HPG>(p, r1, o1, s_qb[1]);
     __syncthreads();  // staged queries visible
@@ -1093,7 +1109,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_select_kernel(const __
     auto flush_hist = [&](int ng) {
         __syncthreads();
         uint32_t* gh = p.hist + (int64_t)ng * kHistBins;
-        // each thread flushes kHistBins / 256 = 16 consecutive bins
+        // each thread flushes its kBinsPerThread consecutive bins
 #pragma unroll
         for (int i = 0; i < kHistBins / kSplitThreads; ++i) {
             const int bin = tid * (kHistBins / kSplitThreads) + i;
@@ -1106,7 +1122,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_select_kernel(const __
     uint32_t ph0 = 0, ph1 = 0;
     int st = 0, ntile = 0;
     bool ok = true;
-    while (cur.valid) {
+    for (;;) {
+        const Tile cur = s_tile[st];
+        if (!cur.valid) break;
         if (cur.ng != seg_ng) {
             if (seg_ng >= 0) {
                 flush_hist(seg_ng);
@@ -1142,11 +1160,13 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_select_kernel(const __
                 score_tile<HPG, false>(f, tile, nreg, scores, keep, s_hist, qd, slot);
         }
         __syncthreads();  // every thread is done with this stage before it is refilled
-        cur = nxt;
-        nxt = next_tile(p, wk);
-        if (nxt.valid) {
-            if (tid == 0) fence_proxy_async();
-            issue(nxt, st);
+        if (tid == 0) {
+            const Tile nx = next_tile(p, wk);
+            s_tile[st] = nx;
+            if (nx.valid) {
+                fence_proxy_async();
+                issue(nx, st);
+            }
         }
         st ^= 1;
     }
@@ -1154,8 +1174,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) score_select_kernel(const __
         if (tid == 0) {
             raise_status(p.status, kDevTimeout);
             // give copies still in flight a bounded chance to land before the block exits
-            if (cur.valid) mbar_wait(&s_bar[st], st ? ph1 : ph0);
-            if (nxt.valid) mbar_wait(&s_bar[st ^ 1], st ? ph0 : ph1);
+            if (s_tile[st].valid) mbar_wait(&s_bar[st], st ? ph1 : ph0);
+            if (s_tile[st ^ 1].valid) mbar_wait(&s_bar[st ^ 1], st ? ph0 : ph1);
         }
         return;
     }
@@ -1370,8 +1390,8 @@ cudaError_t launch_map(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 template <int HPG>
 cudaError_t split_for(const ScoreParams& p_in, const CUtensorMap& smap, cudaStream_t stream, bool pdl) {
-    // one persistent launch with every block resident: as many blocks as fit at once
-    // (two per SM), at most one per tile
+    // one persistent launch with every block resident: one block per SM, at most one per
+    // tile
     static int per_sm = 0;
     if (per_sm == 0) {
         cudaError_t e0 = cudaFuncSetAttribute(score_select_kernel<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1381,7 +1401,7 @@ cudaError_t split_for(const ScoreParams& p_in, const CUtensorMap& smap, cudaStre
         e0 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, score_select_kernel<HPG>, kSplitThreads, kScoreSmem);
         if (e0 != cudaSuccess) return e0;
         if (b < 1) return cudaErrorInvalidConfiguration;
-        per_sm = b < 2 ? b : 2;
+        per_sm = 1;
     }
     // rows in batches small enough that a block's share covers at most kMaxShareSegs
     // (row, group)s
@@ -1406,8 +1426,12 @@ cudaError_t split_for(const ScoreParams& p_in, const CUtensorMap& smap, cudaStre
         p.arrive1 = p_in.arrive1 + g0;
         p.thr = p_in.thr + g0;
         p.bar2 = p_in.bar2 + g0;
+        // at most one block per tile, but enough blocks that no share covers more than
+        // kMaxShareSegs - 2 (row, group)s (short rows)
         const int64_t tiles = ((int64_t)p.N * p.G * p.r_cap + kTileRegions - 1) / kTileRegions;
-        const int64_t grid = full_grid < tiles ? full_grid : tiles;
+        const int64_t need = ((int64_t)p.N * p.G + kMaxShareSegs - 3) / (kMaxShareSegs - 2);
+        int64_t grid = tiles > need ? tiles : need;
+        if (grid > full_grid) grid = full_grid;
         cudaError_t e = launch_map(score_select_kernel<HPG>, dim3((unsigned)grid), dim3(kSplitThreads), kScoreSmem,
                                    stream, pdl && n0 == 0, smap, p);
         if (e != cudaSuccess) return e;

@@ -17,6 +17,7 @@ namespace {
 __device__ uint32_t g_status_word;
 
 int32_t g_select_path = 0;  // 0 auto, 1 fused, 2 split
+int32_t g_overlap_prologue = 0;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -206,7 +207,6 @@ bool cache_maps(const void* kptr, const void* vptr, uint64_t rows, CUtensorMap* 
 
 bool use_pdl() { return true; }
 
-constexpr uint64_t kTileRegionsHost = 512;  // regions per scoring tile (score_select.cu)
 
 
 // Fused (one block per (row, group), keys in shared memory) when there are many rows or
@@ -256,6 +256,12 @@ const char* step5_status_string(step5_status s) {
         case STEP5_ERR_TIMEOUT: return "device wait timed out";
     }
     return "unknown status";
+}
+
+int32_t step5_set_prologue_overlap(int32_t enable) {
+    const int32_t prev = g_overlap_prologue;
+    if (enable == 0 || enable == 1) g_overlap_prologue = enable;
+    return prev;
 }
 
 int32_t step5_set_select_path(int32_t mode) {
@@ -382,6 +388,7 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     p.thr = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.thr);
     p.bar2 = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.bar2);
     p.num_sms = num_sms();
+    p.overlap_prologue = g_overlap_prologue;
     p.status = st;
     p.N = N;
     p.B = B;
@@ -398,7 +405,7 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     } else {
         CUtensorMap smap;
         const uint64_t srows = (uint64_t)B * G * r_cap;
-        if (srows > (uint64_t)INT32_MAX - kTileRegionsHost) return STEP5_ERR_INVALID_ARGUMENT;
+        if (srows > (uint64_t)INT32_MAX - kSplitTileRegions) return STEP5_ERR_INVALID_ARGUMENT;
         if (!cache_summary_map(summaries_e4m3, srows, &smap)) return STEP5_ERR_CUDA;
         e = launch_score_split(p, smap, (cudaStream_t)stream, use_pdl());
     }

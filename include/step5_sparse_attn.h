@@ -190,6 +190,17 @@ step5_status step5_device_status(uint32_t* flags_out, step5_stream_t stream);
  * tuning and testing switch.  Returns the previous value. */
 int32_t step5_set_select_path(int32_t mode);
 
+/* Opt-in overlap of the scoring prologue with the launch before it (no counterpart in
+ * the pages: a launch-scheduling contract of this library).  With enable = 1,
+ * step5_index_score_topk's split-path kernel reads idx_q, w, row_seq, row_pos and the
+ * rope tables before waiting for the kernel launched just before it on the stream
+ * (programmatic dependent launch); only the summaries are read after the wait.  The
+ * caller must then guarantee that this preceding kernel writes none of those inputs,
+ * as step5_region_summarize does (it writes only summaries).  Default 0: every read
+ * waits.  Process-wide, read when a call is enqueued; values other than 0 and 1 are
+ * ignored.  Returns the previous value. */
+int32_t step5_set_prologue_overlap(int32_t enable);
+
 /* The selection path step5_index_score_topk takes for this geometry, N and r_cap under
  * the current step5_set_select_path setting: 1 (fused, one kernel) or 2 (split, three
  * kernels: score + histogram, filter, final select); 0 for an unsupported geometry. */

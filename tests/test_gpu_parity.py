@@ -291,3 +291,46 @@ def test_out_of_range_row_sets_status_and_touches_nothing_else(s5):
     assert np.array_equal(good["out"][1], bad["out"][1])
     assert np.array_equal(good["sel_ids"][1], bad["sel_ids"][1])
     assert s5.step5_device_status() == 0
+
+
+def test_prologue_overlap_gives_identical_results(s5):
+    """The opt-in overlap of the scoring prologue with the summary launch changes when
+    inputs are read, never what is computed."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [30000, 41000, 4100, 70], "B": 3}, seed=23)
+    t = S.materialize(w, device="cuda")
+    dev = t["q"].device
+    res = []
+    for overlap in (0, 1):
+        ws = s5.Workspace.create(geom, w.N, w.r_cap, device=dev)
+        sel_ids = torch.empty((w.N, 4, 512), dtype=torch.int32, device=dev)
+        sel_count = torch.empty((w.N, 4), dtype=torch.int32, device=dev)
+        prev_path = s5.step5_set_select_path(2)
+        s5.step5_region_summarize(geom, t["idx_k"], t["idx_z"], t["cos"], t["sin"], t["sum_begin"],
+                                  t["sum_end"], t["summaries"], max_regions_per_seq=w.max_span)
+        prev = s5.step5_set_prologue_overlap(overlap)
+        s5.step5_index_score_topk(geom, t["idx_q"], t["w"], t["row_seq"], t["row_pos"], t["cos"],
+                                  t["sin"], t["summaries"], sel_ids, sel_count, ws.tensor,
+                                  t_cap=t["idx_k"].shape[2])
+        s5.step5_set_prologue_overlap(prev)
+        s5.step5_set_select_path(prev_path)
+        torch.cuda.synchronize()
+        res.append((sel_ids.cpu(), sel_count.cpu()))
+    assert s5.step5_device_status() == 0
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+    assert s5.step5_set_prologue_overlap(7) in (0, 1)  # out-of-range values are ignored
+
+
+@pytest.mark.parametrize("positions,B", [
+    ([100] * 150 + [9, 17], 5),   # many short rows: one block's share spans many (row, group)s
+    ([20000] * 70 + [20007], 2),  # long shares: more regions per block than it keeps on chip
+])
+def test_split_path_share_shapes(s5, positions, B):
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": positions, "B": B}, seed=29)
+    t = S.materialize(w, device="cuda")
+    a = run_path(s5, geom, w, t, path=1)
+    b = run_path(s5, geom, w, t, path=2)
+    assert a["status"] == 0 and b["status"] == 0
+    for k in ("sel_ids", "sel_count", "sel_scores", "out"):
+        assert np.array_equal(a[k], b[k]), k
