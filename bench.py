@@ -43,7 +43,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=4, help="headline workload (2 or 4)")
+    ap.add_argument("--workload", type=int, default=4, choices=[0, 1, 2, 3, 4],
+                    help="workload: 4 (headline, 1 row at 1M), 2 (4 rows at 128K), 0, 1, 3")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -187,6 +188,11 @@ def run_ours(args, rank, world, local_rank):
         w = S.workload(cfg, seed=17)
         t = S.materialize(w, device=dev)
         N, G = w.N, geom.num_kv_groups
+        pre_span = int((w.pre_end - w.pre_begin).max())
+        if pre_span > 0:  # summaries of the regions completed before the step (set-up)
+            s5.step5_region_summarize(geom, t["idx_k"], t["idx_z"], t["cos"], t["sin"], t["pre_begin"],
+                                      t["pre_end"], t["summaries"], max_regions_per_seq=pre_span)
+            torch.cuda.synchronize()
         ws = s5.Workspace.create(geom, N, w.r_cap, device=dev)
         sel_ids = torch.empty((N, G, geom.top_k), dtype=torch.int32, device=dev)
         sel_count = torch.empty((N, G), dtype=torch.int32, device=dev)
@@ -437,6 +443,10 @@ def oracle_inputs(cfg):
     kshape = (w.B, G, w.t_cap, g.idx_dim)
     h["idx_k"] = S.normal_bf16_rows(kshape, rows, w.seed, S.S_IK)
     h["idx_z"] = S.normal_bf16_rows(kshape, rows, w.seed, S.S_IZ)
+    if int((w.pre_end - w.pre_begin).max()) > 0:  # set-up summaries (untimed)
+        import oracle
+        oracle.summarize_batch(h["idx_k"], h["idx_z"], h["cos"], h["sin"], w.pre_begin, w.pre_end, w.r_cap,
+                               g.rope_dims, summ=h["summaries"])
     return w, h
 
 

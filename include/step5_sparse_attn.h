@@ -172,10 +172,12 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
  * Returns 0 for an unsupported geometry. */
 size_t step5_workspace_bytes(const step5_geometry* geom, int32_t N, int32_t r_cap);
 
-/* Zero-fills a workspace (enqueued on stream).  The workspace must be zero when a call
- * begins; every call that completes leaves it zero again.  Zero it once after
- * allocating it, again whenever N, the geometry or r_cap change between calls on it,
- * and after any call whose device status reported an error. */
+/* Zero-fills a workspace (enqueued on stream).  A zeroed workspace is ready for a call,
+ * and every call that completes leaves it ready for the next one with the same N,
+ * geometry and r_cap (its synchronisation words carry generation numbers, so they are
+ * not cleared).  Zero it once after allocating it, again whenever N, the geometry or
+ * r_cap change between calls on it, and after any call whose device status reported an
+ * error (a bounded wait that gave up leaves the counters inconsistent). */
 step5_status step5_workspace_init(void* workspace, size_t workspace_bytes, step5_stream_t stream);
 
 /* Reads and clears the device status word of the current device: a bit mask of
@@ -202,8 +204,10 @@ int32_t step5_set_select_path(int32_t mode);
 int32_t step5_set_prologue_overlap(int32_t enable);
 
 /* The selection path step5_index_score_topk takes for this geometry, N and r_cap under
- * the current step5_set_select_path setting: 1 (fused, one kernel) or 2 (split, three
- * kernels: score + histogram, filter, final select); 0 for an unsupported geometry. */
+ * the current step5_set_select_path setting: 1 (fused: one block per (row, group)) or 2
+ * (split: one persistent launch whose blocks share each (row, group)'s regions, publish
+ * a histogram threshold, and rank the candidates together); 0 for an unsupported
+ * geometry. */
 int32_t step5_select_path_for(const step5_geometry* geom, int32_t N, int32_t r_cap);
 
 /* Human-readable name of a status code (static string). */

@@ -206,6 +206,8 @@ def workload(cfg, seed: int = 17, geom: Optional[Geometry] = None) -> Workload:
     cfg: 0..4, or a dict {"positions": [...], "B": b (rows assigned round-robin)}.
       0: 1 decode row at context 4,608 (576 completed regions).
       1: 16 decode rows, one per sequence, contexts uniform on [16,384, 32,768].
+      Configs 0 and 1 build the summaries of their earlier regions at set-up (pre_begin,
+      pre_end) and summarise in the step only the region the previous token completed.
       2: 4 decode rows at 131,072 (16,384 regions), e4m3 summaries drawn directly,
          indexer q scaled by 4, 5% of regions per (sequence, group) copied from another
          region (exact score ties).
@@ -235,17 +237,23 @@ def workload(cfg, seed: int = 17, geom: Optional[Geometry] = None) -> Workload:
     if cfg == 0:
         p = 4608
         t_cap = _align8(p + 1)
+        R = p // rt
         return Workload("decode_1x4608", g, 1, 1, t_cap, t_cap // rt, np.zeros(1, np.int32),
-                        np.array([p], np.int32), np.array([0], np.int32),
-                        np.array([p // rt], np.int32), np.zeros(1, np.int32),
-                        np.zeros(1, np.int32), False, seed=seed)
+                        np.array([p], np.int32), np.array([R - 1], np.int32),
+                        np.array([R], np.int32), np.zeros(1, np.int32),
+                        np.array([R - 1], np.int32), False, seed=seed)
     if cfg == 1:
         pos = randint_at(16, 16384, 32768, seed, S_POS)
         t_cap = _align8(int(pos.max()) + 1)
+        R = pos // rt
+        # the step summarises the region the previous token completed (p a multiple of 8);
+        # every earlier region is summarised at set-up
+        done = (pos % rt == 0)
+        sb = np.where(done, R - 1, R)
         return Workload("decode_16x16k-32k", g, 16, 16, t_cap, t_cap // rt,
                         np.arange(16, dtype=np.int32), pos.astype(np.int32),
-                        np.zeros(16, np.int32), (pos // rt).astype(np.int32),
-                        np.zeros(16, np.int32), np.zeros(16, np.int32), False, seed=seed)
+                        sb.astype(np.int32), R.astype(np.int32),
+                        np.zeros(16, np.int32), sb.astype(np.int32), False, seed=seed)
     if cfg == 2:
         p = 131072
         t_cap = _align8(p + 1)
