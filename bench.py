@@ -216,15 +216,8 @@ def run_ours(args, rank, world, local_rank):
                                  sel_ids, sel_count, out, ws.tensor)
 
         def step():
-            call_sum()
-            # the summary kernel is the launch just before the scoring call: the scoring
-            # prologue may read its other inputs before waiting for it
-            prev = s5.step5_set_prologue_overlap(1)
-            try:
-                call_score()
-            finally:
-                s5.step5_set_prologue_overlap(prev)
-            call_attn()
+            # the whole step in one C-ABI call (summaries, score + select, attention)
+            s5.step5_decode_step(geom, t, ws, sel_ids, sel_count, out, max_regions_per_seq=span)
 
         # eager warm-up (sets kernel attributes, TMA descriptors), then the step and each
         # call captured as CUDA graphs: a replay issues the whole step at once, so the
@@ -380,7 +373,7 @@ def run_ours(args, rank, world, local_rank):
                          "score_select": round(head["per_score"] * 1e3, 2),
                          "attention": round(head["per_attn"] * 1e3, 2),
                          "how": head["breakdown_how"]},
-        "roofline": {"kernel": "step5_index_score_topk (one persistent score + select kernel)",
+        "roofline": {"kernel": "score_select_kernel (step5_index_score_topk, split path)",
                      "bound": "hbm", "achieved": round(score_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(score_gbs / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "algorithmic_bytes_per_launch": head["bytes_score"],
@@ -388,7 +381,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(rows / (head["e2e_ms"] / 1e3), 2), "unit": UNIT,
                 "ms_per_step": round(head["e2e_ms"], 5), "h2d_bytes_per_step": head["h2d"],
                 "d2h_bytes_per_step": head["d2h"],
-                "how": "pinned host inputs copied in, the three C-ABI calls issued eagerly, output copied out",
+                "how": "pinned host inputs copied in, step5_decode_step (one C-ABI call) issued eagerly, output copied out",
                 "graph_value": round(rows / (head["e2e_graph_ms"] / 1e3), 2),
                 "graph_ms_per_step": round(head["e2e_graph_ms"], 5)},
         "gpu_launches": head["launches"],

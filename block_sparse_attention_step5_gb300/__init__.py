@@ -28,7 +28,7 @@ __all__ = [
     "step5_region_summarize", "step5_index_score_topk", "step5_sparse_attn",
     "step5_index_score_topk_noalloc",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
-    "step5_set_select_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_status_string", "step5_convert_bf16_to_e4m3",
+    "step5_set_select_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
     "Workspace", "decode_step",
 ]
 
@@ -90,6 +90,8 @@ def load():
         "step5_index_score_topk": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P,
                                          P, sz, P]),
         "step5_sparse_attn": (i32, [G, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]),
+        "step5_decode_step": (i32, [G, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                    P, P, P, P, sz, P]),
         "step5_index_score_topk_noalloc": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P,
                                                  P, P, P]),
         "step5_workspace_bytes": (sz, [G, i32, i32]),
@@ -223,6 +225,23 @@ def step5_sparse_attn(geom, q, k_cache, v_cache, row_seq, row_pos, sel_ids, sel_
         ctypes.byref(Geometry.of(geom)), N, B, t_cap, _ptr(q), _ptr(k_cache), _ptr(v_cache),
         _ptr(row_seq), _ptr(row_pos), _ptr(sel_ids), _ptr(sel_count), _ptr(out), _ptr(workspace),
         ws_bytes, _stream(stream)))
+
+
+def step5_decode_step(geom, t: dict, ws, sel_ids, sel_count, out, max_regions_per_seq, stream=None):
+    """The whole step in one C-ABI call (summaries of [sum_begin, sum_end), score +
+    select, attention), over the tensors of ``t`` (keys as produced by the synthetic
+    workload module).  Same results as the three calls."""
+    B, G, t_cap, _ = t["idx_k"].shape
+    r_cap = t["summaries"].shape[2]
+    N = t["idx_q"].shape[0]
+    ws_t = None if ws is None else (ws.tensor if isinstance(ws, Workspace) else ws)
+    ws_bytes = 0 if ws_t is None else ws_t.numel() * ws_t.element_size()
+    _check("step5_decode_step", load().step5_decode_step(
+        ctypes.byref(Geometry.of(geom)), N, B, t_cap, r_cap, int(max_regions_per_seq),
+        _ptr(t["idx_k"]), _ptr(t["idx_z"]), _ptr(t["cos"]), _ptr(t["sin"]), _ptr(t["sum_begin"]),
+        _ptr(t["sum_end"]), _ptr(t["summaries"]), _ptr(t["idx_q"]), _ptr(t["w"]), _ptr(t["row_seq"]),
+        _ptr(t["row_pos"]), _ptr(t["q"]), _ptr(t["k_cache"]), _ptr(t["v_cache"]), _ptr(sel_ids),
+        _ptr(sel_count), _ptr(out), _ptr(ws_t), ws_bytes, _stream(stream)))
 
 
 @dataclass

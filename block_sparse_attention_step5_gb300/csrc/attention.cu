@@ -382,16 +382,18 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     // ---- block 0: merge the C slots in rank order, from its own shared memory: the
     // weight of every (slot, row) once (lane groups of C per row), then dim d of each row
     __shared__ float s_csc[kMaxCluster][16];
-    if (tid < ((hq_g * C + 31) & ~31)) {
-        const bool ok = tid < hq_g * C;
-        const int r = tid / C, c = tid - r * C;
+    int cp = 1;  // lane-group size: C rounded up to a power of two (padding lanes add nothing)
+    while (cp < C) cp <<= 1;
+    if (tid < ((hq_g * cp + 31) & ~31)) {
+        const int r = tid / cp, c = tid - r * cp;
+        const bool ok = r < hq_g && c < C;
         const float* sl = slots + ((size_t)c * hq_g + r) * kSlotFloats;
         const float m = ok ? sl[0] : -INFINITY;
         float M = m;
-        for (int o = 1; o < C; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        for (int o = 1; o < cp; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         const float sc = exp2f(m - ((M == -INFINITY) ? 0.0f : M));
         float L = ok ? sl[1] * sc : 0.0f;
-        for (int o = 1; o < C; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        for (int o = 1; o < cp; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
         if (ok) {
             s_csc[c][r] = sc;
             if (c == 0) s_L[r] = L;

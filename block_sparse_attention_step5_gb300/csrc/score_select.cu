@@ -519,7 +519,7 @@ __device__ __forceinline__ Walk walk_start(const ScoreParams& p, int64_t x, int6
 
 // The next tile of the walk: at most kTileRegions consecutive candidate regions of one
 // (row, group).  Regions past a row's R, and rows out of range, are skipped.
-__device__ __forceinline__ Tile next_tile(const ScoreParams& p, Walk& k) {
+__device__ __forceinline__ Tile next_tile(const ScoreParams& p, Walk& k, int limit = kTileRegions) {
     Tile t;
     t.valid = 0;
     while (k.left > 0) {
@@ -535,7 +535,7 @@ __device__ __forceinline__ Tile next_tile(const ScoreParams& p, Walk& k) {
             k.r = 0;
             continue;
         }
-        int c1 = min(k.cR, k.r + kTileRegions);
+        int c1 = min(k.cR, k.r + limit);
         if ((int64_t)(c1 - k.r) > k.left) c1 = k.r + (int)k.left;
         t.valid = 1;
         t.ng = k.ng;
@@ -903,6 +903,21 @@ __device__ int wait_threshold(const ScoreParams& p, int ng, uint32_t gen) {
     return -1;
 }
 
+// The selection of (row, group) ng from every score of its row, by one block (the
+// candidate list overflowed): radix descent + bitonic sort.  Out of line: rarely run.
+__device__ __noinline__ void select_all_scores(const ScoreParams& p, int ng, uint8_t* ring) {
+    const int n = ng / p.G;
+    int b, pos;
+    int R = row_regions(p, n, b, pos);
+    if (R < 0) R = 0;
+    int P2 = 32;
+    while (P2 < p.top_k) P2 <<= 1;
+    uint64_t* s_sel = reinterpret_cast<uint64_t*>(ring);
+    TopkSmem& ts = *reinterpret_cast<TopkSmem*>(ring + kMaxTopK * 8);
+    const int take = block_topk<kSplitThreads>(ScoreKeys{p.scores + (int64_t)ng * p.r_cap}, R, p.top_k, P2, s_sel, ts);
+    write_selection<kSplitThreads>(p, n, ng - n * p.G, take, s_sel);
+}
+
 // Ranks of the candidates of (row, group) ng, after every candidate is written: block
 // `sub` of the nb blocks covering it takes chunks of 32 candidates (one per lane), and
 // each warp counts the smaller keys in its share of the list; a candidate ranked below
@@ -911,7 +926,6 @@ __device__ int wait_threshold(const ScoreParams& p, int ng, uint32_t gen) {
 __device__ void rank_segment(const ScoreParams& p, int ng, int sub, int nb, uint8_t* ring, uint32_t* s_w) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = p.top_k;
-    const int n = ng / p.G;
     // the count and the first slots of the list are requested at once
     const uint64_t* cl = p.cand + (int64_t)ng * kCandCap;
     constexpr int kSpec = kCandCap / kSplitThreads;  // slots per thread read before the count is known
@@ -923,18 +937,7 @@ __device__ void rank_segment(const ScoreParams& p, int ng, int sub, int nb, uint
     int32_t* ids = p.sel_ids + (int64_t)ng * K;
     float* ss = p.sel_scores ? p.sel_scores + (int64_t)ng * K : nullptr;
     if (C > kCandCap) {
-        if (sub == 0) {
-            int b, pos;
-            int R = row_regions(p, n, b, pos);
-            if (R < 0) R = 0;
-            int P2 = 32;
-            while (P2 < K) P2 <<= 1;
-            uint64_t* s_sel = reinterpret_cast<uint64_t*>(ring);
-            TopkSmem& ts = *reinterpret_cast<TopkSmem*>(ring + kMaxTopK * 8);
-            const int take =
-                block_topk<kSplitThreads>(ScoreKeys{p.scores + (int64_t)ng * p.r_cap}, R, K, P2, s_sel, ts);
-            write_selection<kSplitThreads>(p, n, ng - n * p.G, take, s_sel);
-        }
+        if (sub == 0) select_all_scores(p, ng, ring);
         return;
     }
     if (sub * 32 < C) {
@@ -1050,11 +1053,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) score_select_kernel(const __
     auto issue = [&](const Tile& x, int st) {
         if (tid == 0) {
             if constexpr (HPG == 4) {
-                // full boxes (rows past the tensor end arrive as zeros)
+                // the boxes that hold the tile's regions (rows past the tensor end arrive
+                // as zeros)
                 const int y = (int)(((int64_t)x.b * p.G + x.g) * p.r_cap + x.c0);
-                mbar_arrive_expect_tx(&s_bar[st], (uint32_t)kTileBytes);
-#pragma unroll
-                for (int k = 0; k < kTileRegions / kBoxRows; ++k)
+                const int nbox = (x.c1 - x.c0 + kBoxRows - 1) / kBoxRows;
+                mbar_arrive_expect_tx(&s_bar[st], (uint32_t)(nbox * kBoxRows * 64));
+                for (int k = 0; k < nbox; ++k)
                     tma_load_2d(ring + st * kTileBytes + k * kBoxRows * 64, &smap, &s_bar[st], 0, y + k * kBoxRows);
             } else {
                 const uint32_t bytes = (uint32_t)(x.c1 - x.c0) * 64u;
@@ -1068,7 +1072,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1) score_select_kernel(const __
     // shared memory (the other threads only read them).
     __shared__ Tile s_tile[kScoreStages];
     if (tid == 0) {
-        s_tile[0] = next_tile(p, wk);
+        // a short first tile, so that every SM starts scoring before the first requests
+        // of all SMs have drained
+        s_tile[0] = next_tile(p, wk, kBoxRows);
         s_tile[1] = next_tile(p, wk);
     }
     if (p.overlap_prologue) pdl_wait();

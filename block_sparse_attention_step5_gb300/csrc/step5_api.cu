@@ -69,9 +69,10 @@ int num_sms() {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // How step (4) splits a row's (top_k + 1)-entry key list: with fewer (row, group) pairs
-// than SMs, each pair gets a cluster of `cluster` blocks (a power of two up to 16, one
-// block per SM) whose shared memory fits and whose whole grid is resident at once;
-// otherwise one block per pair.  Each block takes `eps` entries (whole pairs).
+// than SMs, each pair gets a cluster of `cluster` blocks (1 to 16, one block per SM), the
+// largest whose shared memory fits and whose clusters are all resident at once (the
+// gather of each block runs at a per-SM rate, so the more SMs the better); otherwise one
+// block per pair.  Each block takes `eps` entries (whole pairs).
 void attn_plan(const step5_geometry* g, int N, int* cluster_out, int* eps_out, bool query_device) {
     const int E = g->top_k + 1;
     const int64_t items = (int64_t)N * g->num_kv_groups;
@@ -79,11 +80,11 @@ void attn_plan(const step5_geometry* g, int N, int* cluster_out, int* eps_out, b
     const int sms = query_device ? num_sms() : 152;
     int cluster = 1;
     if (items < sms) {
-        const int per_item = (int)(sms / items);
-        while (cluster * 2 <= kMaxCluster && cluster * 2 <= per_item) cluster *= 2;
-        while (cluster > 1 && attention_smem_bytes(cluster, hq_g) + kAttnStaticSmem > 232448) cluster /= 2;
+        cluster = (int)(sms / items);
+        if (cluster > kMaxCluster) cluster = kMaxCluster;
+        while (cluster > 1 && attention_smem_bytes(cluster, hq_g) + kAttnStaticSmem > 232448) --cluster;
         if (query_device)
-            while (cluster > 1 && attention_max_active_clusters(cluster, hq_g) < items) cluster /= 2;
+            while (cluster > 1 && attention_max_active_clusters(cluster, hq_g) < items) --cluster;
     }
     int eps = (E + cluster - 1) / cluster;
     eps = (eps + 1) / 2 * 2;
@@ -306,11 +307,17 @@ step5_status step5_convert_bf16_to_e4m3(const void* in_bf16, uint8_t* out_e4m3, 
     return STEP5_OK;
 }
 
-step5_status step5_region_summarize(const step5_geometry* geom, int32_t B, int32_t t_cap, int32_t r_cap,
-                                    int32_t max_regions_per_seq, const void* idx_k_bf16, const void* idx_z_bf16,
-                                    const void* rope_cos_bf16, const void* rope_sin_bf16,
-                                    const int32_t* region_begin, const int32_t* region_end,
-                                    uint8_t* summaries_e4m3, float* summaries_f32_or_null, step5_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The three calls, each as validation (launch = false: returns the status the call would
+// return for its arguments, enqueues nothing) or validation + launch.
+step5_status summarize_impl(const step5_geometry* geom, int32_t B, int32_t t_cap, int32_t r_cap,
+                            int32_t max_regions_per_seq, const void* idx_k_bf16, const void* idx_z_bf16,
+                            const void* rope_cos_bf16, const void* rope_sin_bf16, const int32_t* region_begin,
+                            const int32_t* region_end, uint8_t* summaries_e4m3, float* summaries_f32_or_null,
+                            step5_stream_t stream, bool launch) {
     step5_status s = check_geometry(geom);
     if (s != STEP5_OK) return s;
     if (B <= 0 || t_cap <= 0 || r_cap <= 0 || max_regions_per_seq < 0) return STEP5_ERR_INVALID_ARGUMENT;
@@ -322,7 +329,7 @@ step5_status step5_region_summarize(const step5_geometry* geom, int32_t B, int32
         !aligned16(summaries_f32_or_null) || !aligned16(rope_cos_bf16) || !aligned16(rope_sin_bf16))
         return STEP5_ERR_INVALID_ARGUMENT;
     if ((int64_t)B * geom->num_kv_groups * t_cap > INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
-    if (max_regions_per_seq == 0) return STEP5_OK;
+    if (max_regions_per_seq == 0 || !launch) return STEP5_OK;
     uint32_t* st = status_ptr();
     if (!st) return STEP5_ERR_CUDA;
     SummarizeParams p;
@@ -344,12 +351,12 @@ step5_status step5_region_summarize(const step5_geometry* geom, int32_t B, int32
     return STEP5_OK;
 }
 
-step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
-                                    const void* idx_q_bf16, const float* w, const int32_t* row_seq,
-                                    const int32_t* row_pos, const void* rope_cos_bf16, const void* rope_sin_bf16,
-                                    const uint8_t* summaries_e4m3, int32_t* sel_ids, int32_t* sel_count,
-                                    float* scores_or_null, float* sel_scores_or_null, void* workspace,
-                                    size_t workspace_bytes, step5_stream_t stream) {
+step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
+                        const void* idx_q_bf16, const float* w, const int32_t* row_seq, const int32_t* row_pos,
+                        const void* rope_cos_bf16, const void* rope_sin_bf16, const uint8_t* summaries_e4m3,
+                        int32_t* sel_ids, int32_t* sel_count, float* scores_or_null, float* sel_scores_or_null,
+                        void* workspace, size_t workspace_bytes, step5_stream_t stream, int overlap,
+                        bool launch) {
     step5_status s = check_geometry(geom);
     if (s != STEP5_OK) return s;
     if (N <= 0 || B <= 0 || t_cap <= 0 || r_cap <= 0) return STEP5_ERR_INVALID_ARGUMENT;
@@ -365,7 +372,9 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     if (!fused) {
         if (workspace == nullptr) return STEP5_ERR_WORKSPACE;
         if (workspace_bytes < L.end) return STEP5_ERR_WORKSPACE;
+        if ((uint64_t)B * G * r_cap > (uint64_t)INT32_MAX - kSplitTileRegions) return STEP5_ERR_INVALID_ARGUMENT;
     }
+    if (!launch) return STEP5_OK;
     uint32_t* st = status_ptr();
     if (!st) return STEP5_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -388,7 +397,7 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     p.thr = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.thr);
     p.bar2 = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.bar2);
     p.num_sms = num_sms();
-    p.overlap_prologue = g_overlap_prologue;
+    p.overlap_prologue = overlap;
     p.status = st;
     p.N = N;
     p.B = B;
@@ -405,17 +414,16 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
     } else {
         CUtensorMap smap;
         const uint64_t srows = (uint64_t)B * G * r_cap;
-        if (srows > (uint64_t)INT32_MAX - kSplitTileRegions) return STEP5_ERR_INVALID_ARGUMENT;
         if (!cache_summary_map(summaries_e4m3, srows, &smap)) return STEP5_ERR_CUDA;
         e = launch_score_split(p, smap, (cudaStream_t)stream, use_pdl());
     }
     return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
 }
 
-step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, const void* q_bf16,
-                               const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
-                               const int32_t* row_pos, const int32_t* sel_ids, const int32_t* sel_count,
-                               void* out_bf16, void* workspace, size_t workspace_bytes, step5_stream_t stream) {
+step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, const void* q_bf16,
+                       const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
+                       const int32_t* row_pos, const int32_t* sel_ids, const int32_t* sel_count, void* out_bf16,
+                       step5_stream_t stream, bool launch) {
     step5_status s = check_geometry(geom);
     if (s != STEP5_OK) return s;
     if (N <= 0 || B <= 0 || t_cap <= 0 || (t_cap % geom->region_tokens)) return STEP5_ERR_INVALID_ARGUMENT;
@@ -428,6 +436,7 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
     const uint64_t rows = (uint64_t)B * G * t_cap;
     if (rows > (uint64_t)INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
     const int hq_g = geom->num_q_heads / G;
+    if (!launch) return STEP5_OK;
 
     uint32_t* st = status_ptr();
     if (!st) return STEP5_ERR_CUDA;
@@ -435,8 +444,6 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
     attn_plan(geom, N, &cluster, &eps, true);
     CUtensorMap kmap, vmap;
     if (!cache_maps(k_cache_bf16, v_cache_bf16, rows, &kmap, &vmap)) return STEP5_ERR_CUDA;
-    (void)workspace;
-    (void)workspace_bytes;
     AttnParams p;
     p.q = static_cast<const uint16_t*>(q_bf16);
     p.row_seq = row_seq;
@@ -458,6 +465,74 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
     p.scale_log2 = geom->softmax_scale * 1.4426950408889634f;
     cudaError_t e = launch_attention(p, kmap, vmap, (cudaStream_t)stream, use_pdl());
     return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+step5_status step5_region_summarize(const step5_geometry* geom, int32_t B, int32_t t_cap, int32_t r_cap,
+                                    int32_t max_regions_per_seq, const void* idx_k_bf16, const void* idx_z_bf16,
+                                    const void* rope_cos_bf16, const void* rope_sin_bf16,
+                                    const int32_t* region_begin, const int32_t* region_end,
+                                    uint8_t* summaries_e4m3, float* summaries_f32_or_null, step5_stream_t stream) {
+    return summarize_impl(geom, B, t_cap, r_cap, max_regions_per_seq, idx_k_bf16, idx_z_bf16, rope_cos_bf16,
+                          rope_sin_bf16, region_begin, region_end, summaries_e4m3, summaries_f32_or_null, stream,
+                          true);
+}
+
+step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
+                                    const void* idx_q_bf16, const float* w, const int32_t* row_seq,
+                                    const int32_t* row_pos, const void* rope_cos_bf16, const void* rope_sin_bf16,
+                                    const uint8_t* summaries_e4m3, int32_t* sel_ids, int32_t* sel_count,
+                                    float* scores_or_null, float* sel_scores_or_null, void* workspace,
+                                    size_t workspace_bytes, step5_stream_t stream) {
+    return score_impl(geom, N, B, t_cap, r_cap, idx_q_bf16, w, row_seq, row_pos, rope_cos_bf16, rope_sin_bf16,
+                      summaries_e4m3, sel_ids, sel_count, scores_or_null, sel_scores_or_null, workspace,
+                      workspace_bytes, stream, g_overlap_prologue, true);
+}
+
+step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, const void* q_bf16,
+                               const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
+                               const int32_t* row_pos, const int32_t* sel_ids, const int32_t* sel_count,
+                               void* out_bf16, void* workspace, size_t workspace_bytes, step5_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    return attn_impl(geom, N, B, t_cap, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count,
+                     out_bf16, stream, true);
+}
+
+step5_status step5_decode_step(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
+                               int32_t max_regions_per_seq, const void* idx_k_bf16, const void* idx_z_bf16,
+                               const void* rope_cos_bf16, const void* rope_sin_bf16, const int32_t* region_begin,
+                               const int32_t* region_end, uint8_t* summaries_e4m3, const void* idx_q_bf16,
+                               const float* w, const int32_t* row_seq, const int32_t* row_pos, const void* q_bf16,
+                               const void* k_cache_bf16, const void* v_cache_bf16, int32_t* sel_ids,
+                               int32_t* sel_count, void* out_bf16, void* workspace, size_t workspace_bytes,
+                               step5_stream_t stream) {
+    // every argument is checked before anything is enqueued
+    step5_status s = summarize_impl(geom, B, t_cap, r_cap, max_regions_per_seq, idx_k_bf16, idx_z_bf16,
+                                    rope_cos_bf16, rope_sin_bf16, region_begin, region_end, summaries_e4m3,
+                                    nullptr, stream, false);
+    if (s != STEP5_OK) return s;
+    s = score_impl(geom, N, B, t_cap, r_cap, idx_q_bf16, w, row_seq, row_pos, rope_cos_bf16, rope_sin_bf16,
+                   summaries_e4m3, sel_ids, sel_count, nullptr, nullptr, workspace, workspace_bytes, stream, 0,
+                   false);
+    if (s != STEP5_OK) return s;
+    s = attn_impl(geom, N, B, t_cap, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count,
+                  out_bf16, stream, false);
+    if (s != STEP5_OK) return s;
+    s = summarize_impl(geom, B, t_cap, r_cap, max_regions_per_seq, idx_k_bf16, idx_z_bf16, rope_cos_bf16,
+                       rope_sin_bf16, region_begin, region_end, summaries_e4m3, nullptr, stream, true);
+    if (s != STEP5_OK) return s;
+    // the summary kernel (when launched) writes only summaries: the scoring prologue may
+    // read the other scoring inputs before waiting for it
+    s = score_impl(geom, N, B, t_cap, r_cap, idx_q_bf16, w, row_seq, row_pos, rope_cos_bf16, rope_sin_bf16,
+                   summaries_e4m3, sel_ids, sel_count, nullptr, nullptr, workspace, workspace_bytes, stream,
+                   max_regions_per_seq > 0 ? 1 : 0, true);
+    if (s != STEP5_OK) return s;
+    return attn_impl(geom, N, B, t_cap, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count,
+                     out_bf16, stream, true);
 }
 
 }  // extern "C"

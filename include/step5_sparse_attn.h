@@ -167,6 +167,26 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
                                void* out_bf16, void* workspace, size_t workspace_bytes,
                                step5_stream_t stream);
 
+/* One whole step: step5_region_summarize, then step5_index_score_topk, then
+ * step5_sparse_attn, on one stream, with the same arguments and the same results as the
+ * three calls (no counterpart in the pages: a composition for serving loops).  Every
+ * argument is checked before anything is enqueued; then:
+ *  - summaries of regions [region_begin[b], region_end[b]) are written (skipped when
+ *    max_regions_per_seq is 0; the summary inputs must still be valid pointers);
+ *  - the scoring kernel reads its non-summary inputs before waiting for the summary
+ *    kernel (the step5_set_prologue_overlap contract holds by construction here).
+ * Layouts, ownership and errors are those of the three calls (scores and picked scores
+ * are not exported).  workspace: as for step5_index_score_topk. */
+step5_status step5_decode_step(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
+                               int32_t max_regions_per_seq, const void* idx_k_bf16, const void* idx_z_bf16,
+                               const void* rope_cos_bf16, const void* rope_sin_bf16,
+                               const int32_t* region_begin, const int32_t* region_end,
+                               uint8_t* summaries_e4m3, const void* idx_q_bf16, const float* w,
+                               const int32_t* row_seq, const int32_t* row_pos, const void* q_bf16,
+                               const void* k_cache_bf16, const void* v_cache_bf16, int32_t* sel_ids,
+                               int32_t* sel_count, void* out_bf16, void* workspace, size_t workspace_bytes,
+                               step5_stream_t stream);
+
 /* Bytes of device workspace that step5_index_score_topk needs for N rows and r_cap
  * summary slots (the same buffer may be passed to step5_sparse_attn, which ignores it).
  * Returns 0 for an unsupported geometry. */

@@ -334,3 +334,35 @@ def test_split_path_share_shapes(s5, positions, B):
     assert a["status"] == 0 and b["status"] == 0
     for k in ("sel_ids", "sel_count", "sel_scores", "out"):
         assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("cfg", [{"positions": [30000, 41000, 4100, 70], "B": 3}, 4])
+def test_decode_step_entry_matches_the_three_calls(s5, cfg):
+    """step5_decode_step (one call: overlapped prologue, K/V requested into L2 by the
+    selection) gives the same selection and output as the three calls."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload(cfg, seed=31)
+    dev = torch.device("cuda")
+    res = []
+    for fused_entry in (False, True):
+        t = S.materialize(w, device=dev)
+        pre = int((w.pre_end - w.pre_begin).max())
+        if pre > 0:
+            s5.step5_region_summarize(geom, t["idx_k"], t["idx_z"], t["cos"], t["sin"], t["pre_begin"],
+                                      t["pre_end"], t["summaries"], max_regions_per_seq=pre)
+        ws = s5.Workspace.create(geom, w.N, w.r_cap, device=dev)
+        sel_ids = torch.empty((w.N, 4, 512), dtype=torch.int32, device=dev)
+        sel_count = torch.empty((w.N, 4), dtype=torch.int32, device=dev)
+        out = torch.empty((w.N, 32, 128), dtype=torch.bfloat16, device=dev)
+        for _ in range(2):  # twice: the second call reuses the workspace
+            if fused_entry:
+                s5.step5_decode_step(geom, t, ws, sel_ids, sel_count, out, max_regions_per_seq=w.max_span)
+            else:
+                s5.decode_step(geom, t, ws, sel_ids, sel_count, out, max_regions_per_seq=w.max_span)
+        torch.cuda.synchronize()
+        assert s5.step5_device_status() == 0
+        res.append((sel_ids.cpu(), sel_count.cpu(), out.cpu(), S.codes8(t["summaries"])))
+        del t
+    for a, b in zip(res[0][:3], res[1][:3]):
+        assert torch.equal(a, b)
+    assert np.array_equal(res[0][3], res[1][3])
