@@ -7,11 +7,11 @@
 // order ("one simdgroup walking every key alone left decode waiting on loads").
 //
 // Design (sm_103a):
-//  * one thread-block cluster per (row, KV group): its C blocks (1..16) split the row's
-//    key list (picked regions in selection order, then the own region) into runs of
-//    whole 16-token pairs; 8 warps per block, each warp with its own pipeline of 2
-//    pair buffers (warp 0: 3, so that the 17 pairs of a block's share of a 513-entry
-//    list split 16 ways are all requested at once).
+//  * S blocks per (row, KV group) (S = 1..64, as many as the SMs allow: one SM gathers
+//    scattered 2 KB regions at only ~35-65 GB/s, so the gather needs many SMs) split
+//    the row's key list (picked regions in selection order, then the own region) into
+//    runs of whole 16-token pairs; 8 warps per block, each warp with its own pipeline of
+//    2 pair buffers (warp 0: 3).
 //  * a region is a contiguous 2 KB tile of the [B][G][t_cap][128] cache; it is fetched
 //    with one TMA box of a 3-D view (64 dims x 8 rows x 2 row halves) into two
 //    128-byte-swizzled half tiles, so the ldmatrix reads below hit 8 distinct bank
@@ -19,10 +19,10 @@
 //  * S = Q K^T and O += P V run on bf16 mma.sync (m16n8k16, fp32 accumulate) with the
 //    group's query heads as the 16-row left operand (4, 8 or 16 heads; unused rows are
 //    zero); P is rounded to bf16 for the PV product, the softmax state is fp32.
-//  * the warps merge through shared memory; every block then pushes its state into a
-//    slot of block 0's shared memory with remote (distributed shared memory) stores,
-//    one cluster barrier publishes them, and block 0 merges the slots in rank order, so
-//    the result does not depend on timing and nothing goes through global memory.
+//  * the warps merge through shared memory (weights once per (warp, head)); with S > 1
+//    every block writes its state (m, l, o per head) to the workspace, the (row, group)'s
+//    blocks meet at a barrier word, and each block then merges a slice of the outputs
+//    over all S states in split order, so the result does not depend on timing.
 #include "kernels.cuh"
 
 namespace step5 {
@@ -36,14 +36,14 @@ constexpr int kPairBufs = kAttnWarps * kAttnStages + 1;  // warp 0 has one more
 constexpr int kStageBytes = kPairBufs * kPairBytes;
 constexpr int kMergeFloatsPerWarp = 16 * 128 + 32;    // O[16][128], m[16], l[16]
 constexpr int kBarBytes = kPairBufs * 8;
-constexpr int kSlotFloats = 130;                      // m, l, o[128] of one head row
+constexpr int kSlotFloats = kAttnSlotFloats;         // m, l, o[128] of one head row
 static_assert(kAttnWarps * kMergeFloatsPerWarp * 4 <= kStageBytes, "warp merge area must fit");
-static_assert((kMaxTopK + 1) * 4 + (kAttnWarps + kMaxCluster + 2) * 16 * 4 <= kAttnStaticSmem, "static shared memory");
+static_assert((16 * 128 + kAttnMaxSplits) * 4 <= kStageBytes, "split merge area must fit");
+static_assert((kMaxTopK + 2) * 4 + (kAttnWarps * 16 + 32 + 16 * kAttnMaxSplits + 16) * 4 <= kAttnStaticSmem,
+              "static shared memory");
 
-// Dynamic shared memory: [stage area | barriers | push slots C x hq_g x 130 floats]
-size_t attn_smem_bytes(int cluster, int hq_g) {
-    return 1024 + kStageBytes + kBarBytes + (cluster > 1 ? (size_t)cluster * hq_g * kSlotFloats * 4 : 0);
-}
+// Dynamic shared memory: [stage area | barriers]
+size_t attn_smem_bytes() { return 1024 + kStageBytes + kBarBytes; }
 
 // Shared-memory byte offset of (token row t, 16-byte chunk c16 of the 256-byte row) in a
 // region tile written by two 64-dim TMA boxes with 128-byte swizzle.
@@ -52,23 +52,18 @@ __device__ __forceinline__ uint32_t tile_off(int t, int c16) {
     return (uint32_t)(half * 1024 + t * 128 + ((c ^ t) << 4));
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_smem(smem_raw, 1024);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageBytes);
-    float* slots = reinterpret_cast<float*>(smem + kStageBytes + kBarBytes);  // [C][hq_g][130]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, g = blockIdx.y, n = blockIdx.z;
     const int64_t ng = (int64_t)n * p.G + g;
     const int hq_g = p.hq_g;
-    const int C = p.cluster;
+    const int S = p.splits;
 
     if (tid == 0) {
         prefetch_tmap(&kmap);
@@ -81,7 +76,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
 
     // the row's position, pick count and every picked id of this block's run, in one
     // round trip
-    __shared__ int32_t s_ids[kMaxTopK + 1];
+    __shared__ int32_t s_ids[kMaxTopK + 2];  // eps <= top_k + 2 (whole pairs)
     const int32_t* ids = p.sel_ids + ng * p.top_k;
     const int e0 = split * p.entries_per_split;
     for (int i = tid; i < p.entries_per_split; i += kThreads)
@@ -92,7 +87,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     __syncthreads();
     STEP5_STAMP(4, 8);
     if (b < 0 || b >= p.B || pos < 0 || pos >= p.t_cap) {
-        // the same for every block of the cluster: all leave before any cluster barrier
+        // the same for every block of the (row, group): all leave before its barrier
         if (split == 0) {
             if (tid == 0) raise_status(p.status, kDevRange);
             for (int i = tid; i < hq_g * 128; i += kThreads)
@@ -356,57 +351,100 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         }
     }
     __syncthreads();
-    const uint32_t my_slot = smem_u32(slots + (size_t)cluster_ctarank() * hq_g * kSlotFloats);
-    for (int r = rpar; r < hq_g; r += 2) {
-        float O = 0.0f;
+    if (S == 1) {
+        for (int r = rpar; r < hq_g; r += 2) {
+            float O = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * 128 + d] * s_wsc[w][r];
-        if (C == 1) {
+            for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * 128 + d] * s_wsc[w][r];
             p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / s_L[r]);
-        } else {
-            // push into block 0's slot for this block (remote stores, no waiting)
-            const uint32_t a = map_cluster(my_slot + (uint32_t)(r * kSlotFloats) * 4u, 0u);
+        }
+        return;
+    }
+
+    // ---- S blocks per (row, group): this block's state into the workspace
+    const float* pall = p.part + ng * S * hq_g * kSlotFloats;  // [S][hq_g][130]
+    {
+        float* mine = p.part + (ng * S + split) * hq_g * kSlotFloats;
+        for (int r = rpar; r < hq_g; r += 2) {
+            float O = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * 128 + d] * s_wsc[w][r];
+            mine[r * kSlotFloats + 2 + d] = O;
             if (d == 0) {
-                st_cluster_f32(a, s_M[r]);
-                st_cluster_f32(a + 4, s_L[r]);
+                mine[r * kSlotFloats] = s_M[r];
+                mine[r * kSlotFloats + 1] = s_L[r];
             }
-            st_cluster_f32(a + (uint32_t)(2 + d) * 4u, O);
         }
     }
-    if (C == 1) return;
     STEP5_STAMP(4, 11);
-    cluster_sync();  // every push is visible to block 0
+    // every state of the (row, group) is written once all its blocks have arrived
+    __syncthreads();
+    bool ok = true;
+    if (tid == 0) ok = wait_gen(p.bar + ng, arrive_gen(p.bar + ng, (uint32_t)S));
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) raise_status(p.status, kDevTimeout);
+        return;
+    }
     STEP5_STAMP(4, 6);
-    if (cluster_ctarank() != 0) return;
 
-    // ---- block 0: merge the C slots in rank order, from its own shared memory: the
-    // weight of every (slot, row) once (lane groups of C per row), then dim d of each row
-    __shared__ float s_csc[kMaxCluster][16];
-    int cp = 1;  // lane-group size: C rounded up to a power of two (padding lanes add nothing)
-    while (cp < C) cp <<= 1;
-    if (tid < ((hq_g * cp + 31) & ~31)) {
-        const int r = tid / cp, c = tid - r * cp;
-        const bool ok = r < hq_g && c < C;
-        const float* sl = slots + ((size_t)c * hq_g + r) * kSlotFloats;
-        const float m = ok ? sl[0] : -INFINITY;
-        float M = m;
-        for (int o = 1; o < cp; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        const float sc = exp2f(m - ((M == -INFINITY) ? 0.0f : M));
-        float L = ok ? sl[1] * sc : 0.0f;
-        for (int o = 1; o < cp; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (ok) {
-            s_csc[c][r] = sc;
-            if (c == 0) s_L[r] = L;
+    // ---- this block's slice [e_lo, e_hi) of the hq_g * 128 outputs, merged over the S
+    // states in split order.  Every (split, output) value of the slice (at most
+    // EO + S) is requested at once: item j = tid + kThreads * u -> split j / nout, output j % nout.
+    const int EO = hq_g * 128;
+    const int e_lo = EO * split / S, e_hi = EO * (split + 1) / S, nout = e_hi - e_lo;
+    float* s_val = reinterpret_cast<float*>(smem);  // [S][nout], reuses the stage area
+    constexpr int kItems = (16 * 128 + kAttnMaxSplits + kThreads - 1) / kThreads;  // S * nout <= EO + S
+    float v[kItems];
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+        const int j = tid + kThreads * u;
+        v[u] = 0.0f;
+        if (j < S * nout) {
+            const int sp = j / nout, e = e_lo + j - sp * nout;
+            v[u] = __ldcg(pall + ((int64_t)sp * hq_g + (e >> 7)) * kSlotFloats + 2 + (e & 127));
         }
+    }
+    // weights of every split for the rows the slice touches: warp w takes rows
+    // r_lo + w, r_lo + w + 8, ...; lanes take splits
+    __shared__ float s_sw[16][kAttnMaxSplits], s_sL[16];
+    const int r_lo = e_lo >> 7, r_hi = (e_hi - 1) >> 7;
+    for (int r = r_lo + warp; r <= r_hi; r += kAttnWarps) {
+        float m[kAttnMaxSplits / 32], l[kAttnMaxSplits / 32];
+#pragma unroll
+        for (int k = 0; k < kAttnMaxSplits / 32; ++k) {
+            const int sp = lane + 32 * k;
+            m[k] = sp < S ? __ldcg(pall + ((int64_t)sp * hq_g + r) * kSlotFloats) : -INFINITY;
+            l[k] = sp < S ? __ldcg(pall + ((int64_t)sp * hq_g + r) * kSlotFloats + 1) : 0.0f;
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kAttnMaxSplits / 32; ++k) M = fmaxf(M, m[k]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float base = (M == -INFINITY) ? 0.0f : M;
+        float L = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kAttnMaxSplits / 32; ++k) {
+            const int sp = lane + 32 * k;
+            const float sc = exp2f(m[k] - base);
+            if (sp < S) s_sw[r - r_lo][sp] = sc;
+            L += l[k] * sc;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (lane == 0) s_sL[r - r_lo] = L;
+    }
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+        const int j = tid + kThreads * u;
+        if (j < S * nout) s_val[j] = v[u];
     }
     __syncthreads();
-    STEP5_STAMP(4, 10);
-    for (int r = rpar; r < hq_g; r += 2) {
+    for (int t = tid; t < nout; t += kThreads) {
+        const int e = e_lo + t, r = e >> 7;
         float O = 0.0f;
-#pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c)
-            if (c < C) O += slots[((size_t)c * hq_g + r) * kSlotFloats + 2 + d] * s_csc[c][r];
-        p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / s_L[r]);
+        for (int sp = 0; sp < S; ++sp) O += s_val[sp * nout + t] * s_sw[r - r_lo][sp];
+        p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + (e & 127)] = f32_to_bf16_bits(O / s_sL[r - r_lo]);
     }
     STEP5_STAMP(4, 7);
 }
@@ -417,45 +455,14 @@ static cudaError_t ensure_attn_attr() {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)attn_smem_bytes(16, 8));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                                             (int)attn_smem_bytes());
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     return cudaSuccess;
 }
 
-size_t attention_smem_bytes(int cluster, int hq_g) { return attn_smem_bytes(cluster, hq_g); }
-
-int attention_max_active_clusters(int cluster, int hq_g) {
-    static int cache[64][17][17] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cluster < 1 || cluster > 16 || hq_g < 1 ||
-        hq_g > 16)
-        return 0;
-    if (cache[dev][cluster][hq_g] == 0) {
-        int n = -1;
-        if (ensure_attn_attr() == cudaSuccess) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)cluster, 1, 1);
-            cfg.blockDim = dim3(kThreads);
-            cfg.dynamicSmemBytes = attn_smem_bytes(cluster, hq_g);
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = (unsigned)cluster;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int m = 0;
-            if (cudaOccupancyMaxActiveClusters(&m, sparse_attn_kernel, &cfg) == cudaSuccess && m > 0) n = m;
-            cudaGetLastError();  // clear a refused configuration
-        }
-        cache[dev][cluster][hq_g] = n;
-    }
-    return cache[dev][cluster][hq_g] > 0 ? cache[dev][cluster][hq_g] : 0;
-}
+size_t attention_smem_bytes() { return attn_smem_bytes(); }
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream, bool pdl) {
@@ -464,22 +471,13 @@ cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.splits, p.G, p.N);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = attn_smem_bytes(p.cluster, p.hq_g);
+    cfg.dynamicSmemBytes = attn_smem_bytes();
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = (unsigned)p.cluster;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-    if (pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = na;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, sparse_attn_kernel, kmap, vmap, p);
 }
 

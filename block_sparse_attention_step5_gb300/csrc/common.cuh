@@ -202,6 +202,48 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
     return false;
 }
 
+// ---------------------------------------------------------------------------------
+// Global-memory synchronisation between the blocks of one launch (all resident)
+// ---------------------------------------------------------------------------------
+
+constexpr uint32_t kBarrierPolls = 1u << 22;  // polls of a global wait before giving up
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* a) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* a, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+// A barrier word holds a generation number (high 16 bits) and the arrivals of the
+// current barrier (low 16 bits): the last of nb arrivals clears the count and advances
+// the generation with one release add, so the word never needs clearing.
+constexpr uint32_t kArrivedLast = 0x80000000u;
+
+// Arrival (acquire + release): the generation seen, or kArrivedLast for the last
+// arrival (which has released the others).
+__device__ __forceinline__ uint32_t arrive_gen(uint32_t* word, uint32_t nb) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(word) : "memory");
+    if ((old & 0xffffu) == nb - 1u) {
+        asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(word), "r"(0x10000u - nb) : "memory");
+        return kArrivedLast;
+    }
+    return old >> 16;
+}
+
+// Waits until the generation of a barrier word differs from gen (kArrivedLast: no
+// wait); false when the wait gives up.
+__device__ __forceinline__ bool wait_gen(const uint32_t* word, uint32_t gen) {
+    if (gen == kArrivedLast) return true;
+    for (uint32_t it = 0; it < kBarrierPolls; ++it)
+        if ((ld_acquire_u32(word) >> 16) != gen) return true;
+    return false;
+}
+
 // 2-D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_t* bar, int32_t x,
                                             int32_t y) {
@@ -265,6 +307,11 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
 

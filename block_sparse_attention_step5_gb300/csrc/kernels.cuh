@@ -54,6 +54,11 @@ struct ScoreParams {
     int N, B, G, idx_heads, hpg, t_cap, r_cap, rope_dims, top_k;
     int num_sms;             // split path: persistent blocks (one per SM)
     int overlap_prologue;    // split path: read the non-summary inputs before the launch wait
+    // split path with overlap_prologue: the launch before writes only the summaries of
+    // regions [defer_begin[b], defer_end[b]) of each sequence b; tiles clear of those
+    // ranges are fetched before the launch wait (null: wait before the first tile)
+    const int32_t* defer_begin;
+    const int32_t* defer_end;
 };
 cudaError_t launch_score_fused(const ScoreParams& p, cudaStream_t stream, bool pdl);
 // Split path: one persistent launch (score, candidates, ranks) with grid barriers.
@@ -63,8 +68,12 @@ cudaError_t launch_score_split(const ScoreParams& p, const CUtensorMap& smap, cu
 
 // ----------------------------------------------------------------- step (4)
 constexpr int kAttnWarps = 8;
-constexpr int kAttnStages = 2;          // pair buffers per warp
-constexpr int kMaxCluster = 16;         // blocks per (row, group) (non-portable above 8)
+constexpr int kAttnStages = 2;          // pair buffers per warp (warp 0: one more)
+constexpr int kAttnMaxSplits = 64;      // blocks per (row, group)
+constexpr int kAttnMaxBlocks = 256;     // blocks of one launch that share a (row, group) with others
+constexpr int kAttnSlotFloats = 130;    // m, l, o[128] of one head row
+// upper bound of step (4)'s workspace area (barrier words of <= 128 pairs, 256 slots of 16 heads)
+constexpr size_t kAttnAreaMaxBytes = 512 + (size_t)kAttnMaxBlocks * 16 * kAttnSlotFloats * 4;
 
 struct AttnParams {
     const uint16_t* q;       // [N][Hq][128]
@@ -73,16 +82,16 @@ struct AttnParams {
     const int32_t* sel_ids;  // [N][G][top_k]
     const int32_t* sel_count;
     uint16_t* out;           // [N][Hq][128]
+    float* part;             // splits > 1: [N*G][splits][hq_g][130] block states
+    uint32_t* bar;           // splits > 1: [N*G] barrier words (generation | arrivals)
     uint32_t* status;
     int N, B, G, Hq, hq_g, t_cap, top_k;
-    int splits, entries_per_split, cluster;
+    int splits, entries_per_split;  // blocks per (row, group) and the entries each takes
     float scale_log2;        // softmax_scale * log2(e)
 };
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream, bool pdl);
-// Clusters of `cluster` attention blocks that can be resident at once (0 if unknown).
-int attention_max_active_clusters(int cluster, int hq_g);
-size_t attention_smem_bytes(int cluster, int hq_g);  // dynamic part
-constexpr size_t kAttnStaticSmem = (kMaxTopK + 1) * 4 + 4096;  // picked ids + merge weights
+size_t attention_smem_bytes();  // dynamic part
+constexpr size_t kAttnStaticSmem = (kMaxTopK + 2) * 4 + 16384;  // picked ids + merge scratch
 
 }  // namespace step5

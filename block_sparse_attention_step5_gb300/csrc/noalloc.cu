@@ -18,7 +18,8 @@
 namespace step5 {
 namespace {
 
-constexpr size_t kNoallocScratchBytes = (size_t)4 << 20;  // 4 MiB
+// 4 MiB for steps (2)-(3), after the space a workspace keeps for step (4)
+constexpr size_t kNoallocScratchBytes = ((size_t)4 << 20) + kAttnAreaMaxBytes;
 
 // The scratch array: one copy on every device that loads the library, held until exit.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];

@@ -30,8 +30,8 @@ namespace {
 
 template <int HPG>
 struct QFrag {
-    float2 q[HPG][8];  // e4m3 query of head h at dims 16*qd + 2i, 16*qd + 2i + 1
-    float w[HPG];      // w of every head (HPG == 4: w[0] holds head qd's weight)
+    uint32_t q[HPG][8];  // e4m3 query of head h at dims 16*qd + 2i, 16*qd + 2i + 1 (f16 pair)
+    float w[HPG];        // w of every head (HPG == 4: w[0] holds head qd's weight)
 };
 
 // e4m3(bf16(NEOX(q))) of the group's HPG heads, as floats, into s_q[h * 64 + d].  Ends
@@ -69,70 +69,86 @@ __device__ void load_qfrag(const ScoreParams& p, int n, int g, int pos, float* s
     for (int h = 0; h < HPG; ++h) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            f.q[h][i] = make_float2(s_q[h * 64 + 16 * qd + 2 * i], s_q[h * 64 + 16 * qd + 2 * i + 1]);
+            f.q[h][i] = pack_f16x2(s_q[h * 64 + 16 * qd + 2 * i], s_q[h * 64 + 16 * qd + 2 * i + 1]);
     }
 }
 
 // ----------------------------------------------------------------- one thread per region
 //
 // For 4 indexer heads per group: a thread scores whole regions (64 dims, 4 heads), two at
-// a time, so no cross-lane reduction is needed.  The query lives in shared memory as
-// q4[2 * pair + hp] = (q_{2hp}[2 pair], q_{2hp}[2 pair + 1], q_{2hp+1}[2 pair],
-// q_{2hp+1}[2 pair + 1]); every lane reads the same element (broadcast) and one query
+// a time, so no cross-lane reduction is needed.  Both operands of every product are e4m3
+// values, which f16 holds exactly, so the summaries are widened only to f16 (one cvt per
+// two dims) and the products accumulate in fp32 through the mixed-precision fma (f16
+// inputs, fp32 addend and result, one rounding): the same bits as an fp32 fma on the
+// decoded values, at fewer instructions per product than widening every value to fp32.
+// The query lives in shared memory as qh[pair] = 4 words, word h = the f16 pair
+// (q_h[2 pair], q_h[2 pair + 1]); every lane reads the same words (broadcast) and one
 // load serves both regions.
 
-// Rearranges s_q [4][64] into q4 [64]; ends with a __syncthreads.
-__device__ __forceinline__ void build_q4(const float* s_q, float4* q4) {
-    if (threadIdx.x < 64) {
-        const int pr = threadIdx.x >> 1, hp = threadIdx.x & 1;
-        q4[threadIdx.x] = make_float4(s_q[(2 * hp) * 64 + 2 * pr], s_q[(2 * hp) * 64 + 2 * pr + 1],
-                                      s_q[(2 * hp + 1) * 64 + 2 * pr], s_q[(2 * hp + 1) * 64 + 2 * pr + 1]);
+// Packs s_q [4][64] (e4m3-valued floats) into qh [32] uint4; ends with a __syncthreads.
+__device__ __forceinline__ void build_qh(const float* s_q, uint32_t* qh) {
+    if (threadIdx.x < 128) {
+        const int pr = threadIdx.x >> 2, h = threadIdx.x & 3;
+        qh[threadIdx.x] = pack_f16x2(s_q[h * 64 + 2 * pr], s_q[h * 64 + 2 * pr + 1]);
     }
     __syncthreads();
 }
 
-__device__ __forceinline__ float finish_score4(const float2 (&acc)[4], const float (&w)[4]) {
+// Two f16 pairs of e4m3-valued elements, widened from two e4m3 bytes.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+    return h2;
+}
+
+// lo += q.lo * x.lo and hi += q.hi * x.hi (f16 pairs q and x, fp32 accumulators).
+__device__ __forceinline__ void fma_f16x2_f32(float& lo, float& hi, uint32_t q, uint32_t x) {
+    asm("{.reg .f16 q0, q1, x0, x1;\n\t"
+        "mov.b32 {q0, q1}, %2;\n\t"
+        "mov.b32 {x0, x1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, q0, x0, %0;\n\t"
+        "fma.rn.f32.f16 %1, q1, x1, %1;}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(q), "r"(x));
+}
+
+__device__ __forceinline__ float finish_score4(const float (&ev)[4], const float (&od)[4], const float (&w)[4]) {
     float sc = 0.0f;
 #pragma unroll
-    for (int h = 0; h < 4; ++h) sc = fmaf(fmaxf(__fadd_rn(acc[h].x, acc[h].y), 0.0f), w[h], sc);
+    for (int h = 0; h < 4; ++h) sc = fmaf(fmaxf(__fadd_rn(ev[h], od[h]), 0.0f), w[h], sc);
     return __fadd_rn(sc, 0.0f);  // -0 -> +0
 }
 
 // Scores of two regions whose 64 summary bytes are a[0..3] and b[0..3] (dims 16k..16k+15
 // in chunk k).  Each head's dot product is the sum of an even-dim and an odd-dim partial
-// sum, accumulated in dim order.
-__device__ __forceinline__ void score_rows2(const uint4 (&a)[4], const uint4 (&b)[4], const float4* q4,
+// sum, each accumulated in dim order.
+__device__ __forceinline__ void score_rows2(const uint4 (&a)[4], const uint4 (&b)[4], const uint4* qh,
                                             const float (&w)[4], float& sa, float& sb) {
-    float2 A[4], Bc[4];
+    float ae[4], ao[4], be[4], bo[4];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) A[h] = Bc[h] = make_float2(0.0f, 0.0f);
+    for (int h = 0; h < 4; ++h) ae[h] = ao[h] = be[h] = bo[h] = 0.0f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const uint32_t wa[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
         const uint32_t wb[4] = {b[k].x, b[k].y, b[k].z, b[k].w};
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
-            const int p0 = 8 * k + 2 * qq;
 #pragma unroll
-            for (int hw = 0; hw < 2; ++hw) {  // low / high 16 bits: pair p0 / p0 + 1
-                const float2 xa = e4m3x2_to_f32x2((uint16_t)(hw ? wa[qq] >> 16 : wa[qq] & 0xffffu));
-                const float2 xb = e4m3x2_to_f32x2((uint16_t)(hw ? wb[qq] >> 16 : wb[qq] & 0xffffu));
-                const float4 q01 = q4[2 * (p0 + hw)], q23 = q4[2 * (p0 + hw) + 1];
-                const float2 q0 = make_float2(q01.x, q01.y), q1 = make_float2(q01.z, q01.w);
-                const float2 q2 = make_float2(q23.x, q23.y), q3 = make_float2(q23.z, q23.w);
-                A[0] = __ffma2_rn(q0, xa, A[0]);
-                A[1] = __ffma2_rn(q1, xa, A[1]);
-                A[2] = __ffma2_rn(q2, xa, A[2]);
-                A[3] = __ffma2_rn(q3, xa, A[3]);
-                Bc[0] = __ffma2_rn(q0, xb, Bc[0]);
-                Bc[1] = __ffma2_rn(q1, xb, Bc[1]);
-                Bc[2] = __ffma2_rn(q2, xb, Bc[2]);
-                Bc[3] = __ffma2_rn(q3, xb, Bc[3]);
+            for (int hw = 0; hw < 2; ++hw) {  // low / high 16 bits: pair 8k + 2qq + hw
+                const uint32_t xa = e4m3x2_to_f16x2((uint16_t)(hw ? wa[qq] >> 16 : wa[qq] & 0xffffu));
+                const uint32_t xb = e4m3x2_to_f16x2((uint16_t)(hw ? wb[qq] >> 16 : wb[qq] & 0xffffu));
+                const uint4 q = qh[8 * k + 2 * qq + hw];
+                const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    fma_f16x2_f32(ae[h], ao[h], qw[h], xa);
+                    fma_f16x2_f32(be[h], bo[h], qw[h], xb);
+                }
             }
         }
     }
-    sa = finish_score4(A, w);
-    sb = finish_score4(Bc, w);
+    sa = finish_score4(ae, ao, w);
+    sb = finish_score4(be, bo, w);
 }
 
 // Score of the region whose 16 dims [16*qd, 16*qd + 16) this thread holds in v.  All
@@ -146,12 +162,12 @@ __device__ __forceinline__ float score_from_vec(const QFrag<HPG>& f, uint4 v) {
     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const float2 s0 = e4m3x2_to_f32x2((uint16_t)(w4[q] & 0xffffu));
-        const float2 s1 = e4m3x2_to_f32x2((uint16_t)(w4[q] >> 16));
+        const uint32_t s0 = e4m3x2_to_f16x2((uint16_t)(w4[q] & 0xffffu));
+        const uint32_t s1 = e4m3x2_to_f16x2((uint16_t)(w4[q] >> 16));
 #pragma unroll
         for (int h = 0; h < HPG; ++h) {
-            acc[h] = __ffma2_rn(f.q[h][2 * q], s0, acc[h]);
-            acc[h] = __ffma2_rn(f.q[h][2 * q + 1], s1, acc[h]);
+            fma_f16x2_f32(acc[h].x, acc[h].y, f.q[h][2 * q], s0);
+            fma_f16x2_f32(acc[h].x, acc[h].y, f.q[h][2 * q + 1], s1);
         }
     }
     if constexpr (HPG == 4) {
@@ -416,12 +432,12 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
     const uint4* base = reinterpret_cast<const uint4*>(p.summ + ((int64_t)b * p.G + g) * p.r_cap * 64);
     float* exp_scores = p.scores ? p.scores + ((int64_t)n * p.G + g) * p.r_cap : nullptr;
     if constexpr (HPG == 4) {
-        __shared__ float4 s_q4[64];
+        __shared__ uint4 s_qh[32];
         float w[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) w[h] = p.w[(int64_t)n * p.idx_heads + (int64_t)g * 4 + h];
         stage_query<4>(p, n, g, pos, s_q);
-        build_q4(s_q, s_q4);
+        build_qh(s_q, reinterpret_cast<uint32_t*>(s_qh));
         for (int r0 = 0; r0 < R; r0 += 2 * kFusedThreads) {
             const int ra = r0 + threadIdx.x, rb = ra + kFusedThreads;
             uint4 va[4], vb[4];
@@ -431,7 +447,7 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
                 vb[k] = rb < R ? __ldg(base + (int64_t)rb * 4 + k) : make_uint4(0, 0, 0, 0);
             }
             float sa, sb;
-            score_rows2(va, vb, s_q4, w, sa, sb);
+            score_rows2(va, vb, s_qh, w, sa, sb);
             if (ra < R) {
                 s_key[ra] = desc_key(sa);
                 if (exp_scores) exp_scores[ra] = sa;
@@ -474,6 +490,12 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
 // ----------------------------------------------------------------- split path
 
 constexpr int kSplitThreads = 512;                     // one block per SM
+// Registers per thread.  An SM's registers are split over its 4 schedulers (16,384
+// each) and a warp takes its registers from one of them: 4 warps x 32 x 112 leave 2,048
+// per scheduler, room for a warp of a 64-thread summary block of the launch before (at
+// most 48 registers a thread; step (1) of the same decode step), so the scoring block of
+// that SM starts at once instead of after it.
+constexpr int kSplitMaxRegs = 112;
 constexpr int kSplitWarps = kSplitThreads / 32;
 constexpr int kBinsPerThread = kHistBins / kSplitThreads;  // histogram bins a thread owns
 
@@ -630,11 +652,14 @@ __device__ __forceinline__ void load_rope(const ScoreParams& p, int pos, QRope<H
     }
 }
 
-// Shared-memory query buffers of the split scoring kernel.  HPG == 4 keeps the query in
-// the q4 layout of score_rows2; the others as q[h * 64 + d].
+// Shared-memory query buffers of the split scoring kernel.  HPG == 4 keeps the query as
+// the f16 pairs of score_rows2 (qh); the others as q[h * 64 + d].
 template <int HPG>
 struct QBuf {
-    float q[HPG * 64];
+    static constexpr int kQ = HPG == 4 ? 4 : HPG * 64;
+    static constexpr int kQh = HPG == 4 ? HPG * 64 : 8;
+    float q[kQ];
+    __align__(16) uint16_t qh[kQh];
     float w[HPG];
 };
 
@@ -655,7 +680,7 @@ __device__ __forceinline__ void finish_query(const ScoreParams& p, const QRaw<HP
                                  d < half);
             const float v = e4m3x2_to_f32x2(f32_to_e4m3(bf16_to_f32(rb))).x;
             if constexpr (HPG == 4)
-                qb.q[(2 * (d >> 1) + (h >> 1)) * 4 + (h & 1) * 2 + (d & 1)] = v;
+                qb.qh[(d >> 1) * 8 + h * 2 + (d & 1)] = __half_as_ushort(__float2half_rn(v));
             else
                 qb.q[i] = v;
         }
@@ -673,7 +698,7 @@ __device__ __forceinline__ void qfrag_from_smem(const QBuf<HPG>& qb, QFrag<HPG>&
     for (int h = 0; h < HPG; ++h) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            f.q[h][i] = make_float2(qb.q[h * 64 + 16 * qd + 2 * i], qb.q[h * 64 + 16 * qd + 2 * i + 1]);
+            f.q[h][i] = pack_f16x2(qb.q[h * 64 + 16 * qd + 2 * i], qb.q[h * 64 + 16 * qd + 2 * i + 1]);
     }
 }
 
@@ -686,28 +711,26 @@ __device__ __forceinline__ int row_pos_or0(const ScoreParams& p, int n) {
 
 // Score of one region whose 64 summary bytes are a[0..3] (the one-row form of
 // score_rows2, same arithmetic and order).
-__device__ __forceinline__ float score_row1(const uint4 (&a)[4], const float4* q4, const float (&w)[4]) {
-    float2 A[4];
+__device__ __forceinline__ float score_row1(const uint4 (&a)[4], const uint4* qh, const float (&w)[4]) {
+    float ae[4], ao[4];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) A[h] = make_float2(0.0f, 0.0f);
+    for (int h = 0; h < 4; ++h) ae[h] = ao[h] = 0.0f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const uint32_t wa[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
-            const int p0 = 8 * k + 2 * qq;
 #pragma unroll
             for (int hw = 0; hw < 2; ++hw) {
-                const float2 xa = e4m3x2_to_f32x2((uint16_t)(hw ? wa[qq] >> 16 : wa[qq] & 0xffffu));
-                const float4 q01 = q4[2 * (p0 + hw)], q23 = q4[2 * (p0 + hw) + 1];
-                A[0] = __ffma2_rn(make_float2(q01.x, q01.y), xa, A[0]);
-                A[1] = __ffma2_rn(make_float2(q01.z, q01.w), xa, A[1]);
-                A[2] = __ffma2_rn(make_float2(q23.x, q23.y), xa, A[2]);
-                A[3] = __ffma2_rn(make_float2(q23.z, q23.w), xa, A[3]);
+                const uint32_t xa = e4m3x2_to_f16x2((uint16_t)(hw ? wa[qq] >> 16 : wa[qq] & 0xffffu));
+                const uint4 q = qh[8 * k + 2 * qq + hw];
+                const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) fma_f16x2_f32(ae[h], ao[h], qw[h], xa);
             }
         }
     }
-    return finish_score4(A, w);
+    return finish_score4(ae, ao, w);
 }
 
 // One thread per region (HPG == 4): thread t scores rows t and t + kSplitThreads of a
@@ -715,7 +738,7 @@ __device__ __forceinline__ float score_row1(const uint4 (&a)[4], const float4* q
 // (16-byte chunk k of row r sits at chunk k ^ ((r >> 1) & 3)), so the 8 rows a quarter
 // warp reads at once fall in 8 different bank groups.  Rows at or past nreg are skipped
 // a warp at a time.
-__device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, const float4* q4,
+__device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, const uint4* qh,
                                                 const float (&w)[4], float* scores, float* keep,
                                                 uint32_t* s_hist) {
     const int t = threadIdx.x;
@@ -733,7 +756,7 @@ __device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, c
             b[k] = rb[k ^ sw];
         }
         float sa, sb;
-        score_rows2(a, b, q4, w, sa, sb);
+        score_rows2(a, b, qh, w, sa, sb);
         scores[t] = sa;  // t < kSplitThreads < nreg
         if (keep) keep[t] = sa;
         atomicAdd(&s_hist[desc_key(sa) >> (32 - kHistBits)], 1u);
@@ -745,7 +768,7 @@ __device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, c
     } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k) a[k] = ra[k ^ sw];
-        const float sa = score_row1(a, q4, w);
+        const float sa = score_row1(a, qh, w);
         if (t < nreg) {
             scores[t] = sa;
             if (keep) keep[t] = sa;
@@ -755,14 +778,6 @@ __device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, c
 }
 
 // ----------------------------------------------------------------- grid-wide steps
-
-constexpr uint32_t kBarrierPolls = 1u << 22;  // polls of a grid barrier before giving up
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* a) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
-    return v;
-}
 
 // Block-wide exclusive scan of one count per thread; returns the thread's offset and
 // leaves the block total in *total.  s_w: kSplitThreads / 32 words of scratch.
@@ -834,10 +849,6 @@ __device__ __forceinline__ bool arrive_last(uint32_t* ctr, uint32_t nblocks) {
     return old == nblocks - 1u;
 }
 
-__device__ __forceinline__ void st_release_u32(uint32_t* a, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
-}
-
 // Per-(row, group) synchronisation words of the split path.  Each is a generation
 // number (high bits) with a payload, so none needs clearing between calls:
 //  * thr[ng] = gen << 12 | bin: the threshold bin, published by the last block to add
@@ -845,34 +856,12 @@ __device__ __forceinline__ void st_release_u32(uint32_t* a, uint32_t v) {
 //  * bar2[ng] = gen << 16 | arrivals: a barrier over the (row, group)'s blocks once
 //    their candidates are written; the last arrival clears the count and advances the
 //    generation with one release add.
-constexpr uint32_t kArrivedLast = 0x80000000u;
-
-// Arrival at a count/generation barrier word of nb blocks: the generation seen, or
-// kArrivedLast for the last arrival (which has released the others).
-__device__ __forceinline__ uint32_t arrive_gen(uint32_t* word, uint32_t nb) {
-    uint32_t old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(word) : "memory");
-    if ((old & 0xffffu) == nb - 1u) {
-        asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(word), "r"(0x10000u - nb) : "memory");
-        return kArrivedLast;
-    }
-    return old >> 16;
-}
-
-// Waits until the generation of a barrier word differs from gen (kArrivedLast: no
-// wait); false when the wait gives up.
-__device__ __forceinline__ bool wait_gen(const uint32_t* word, uint32_t gen) {
-    if (gen == kArrivedLast) return true;
-    for (uint32_t it = 0; it < kBarrierPolls; ++it)
-        if ((ld_acquire_u32(word) >> 16) != gen) return true;
-    return false;
-}
 
 // Threshold of one (row, group), by the whole block that added its histogram share
 // last: the fine bin holding the K-th key (block_threshold over the complete
-// histogram).  Clears the histogram, the arrival counter and the candidate counter for
-// the candidates that follow, then publishes thr[ng] = (gen + 1) << 12 | bin with
-// release semantics.
+// histogram).  Clears the arrival counter and the candidate counter for the candidates
+// that follow, publishes thr[ng] = (gen + 1) << 12 | bin with release semantics, then
+// clears the histogram.
 __device__ void publish_threshold(const ScoreParams& p, int ng, uint32_t gen, uint32_t* s_w, int* s_tmp) {
     const int tid = threadIdx.x;
     uint4* gh = reinterpret_cast<uint4*>(p.hist + (int64_t)ng * kHistBins) + tid * (kBinsPerThread / 4);
@@ -883,14 +872,15 @@ __device__ void publish_threshold(const ScoreParams& p, int ng, uint32_t gen, ui
     int R = row_regions(p, ng / p.G, b, pos);
     if (R < 0) R = 0;
     block_threshold(h, R, p.top_k, s_w, s_tmp);  // ends with a __syncthreads
-#pragma unroll
-    for (int q = 0; q < kBinsPerThread / 4; ++q) gh[q] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
     if (tid == 0) {
         p.arrive1[ng] = 0;
         p.cand_count[ng] = 0;
         st_release_u32(p.thr + ng, ((gen + 1u) << 12) | (uint32_t)*s_tmp);
     }
+    // every share has been added, and nothing reads the histogram again in this launch:
+    // it is cleared for the next one after the threshold is out
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread / 4; ++q) gh[q] = make_uint4(0, 0, 0, 0);
 }
 
 // Waits (thread 0) for the threshold of (row, group) ng published after generation
@@ -994,7 +984,7 @@ constexpr int kRankWarps = kSplitThreads / 32;
 // generations, so nothing needs clearing between calls.  A share covers at most
 // kMaxShareSegs (row, group)s (the host launches row batches).
 template <int HPG>
-__global__ void __launch_bounds__(kSplitThreads, 1) score_select_kernel(const __grid_constant__ CUtensorMap smap,
+__global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_constant__ CUtensorMap smap,
                                                                         ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = align_smem(smem_raw, 1024);
@@ -1019,7 +1009,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1) score_select_kernel(const __
     __syncthreads();
     // With overlap_prologue the launch before this one writes none of the query,
     // weight, row and rope inputs, so they are read before waiting for it (only the
-    // summaries are); otherwise every read waits.
+    // summaries are, and thread 0 waits before the first copy that may read them);
+    // otherwise every read waits.
     if (!p.overlap_prologue) pdl_wait();
     STEP5_STAMP(1, 1);
     // this block's even share of the flattened (row, group, region) space
@@ -1040,18 +1031,48 @@ __global__ void __launch_bounds__(kSplitThreads, 1) score_select_kernel(const __
     int staged1 = ngB > ngA ? ngA + 1 : -1;
     QRaw<HPG> r0, r1;
     QRope<HPG> o0, o1;
+    // Thread 0 walks the share; the descriptors of the tiles in the two stages live in
+    // shared memory (the other threads only read them).
+    __shared__ Tile s_tile[kScoreStages];
+    // the deferred summary ranges of up to kSplitThreads sequences, staged with the
+    // first reads so that the first copies wait on one round trip only
+    __shared__ int2 s_def[kSplitThreads];
+    const bool def_staged = p.defer_begin != nullptr && p.B <= kSplitThreads;
     {
         const int n0 = staged0 / p.G;
         const int n1 = staged1 < 0 ? n0 : staged1 / p.G;
         load_query_raw<HPG>(p, n0, staged0 - n0 * p.G, r0);
         if (staged1 >= 0) load_query_raw<HPG>(p, n1, staged1 - n1 * p.G, r1);
+        if (def_staged && tid < p.B) s_def[tid] = make_int2(__ldg(p.defer_begin + tid), __ldg(p.defer_end + tid));
+        if (tid == 0) {
+            // a short first tile, so that every SM starts scoring before the first
+            // requests of all SMs have drained
+            s_tile[0] = next_tile(p, wk, kBoxRows);
+            s_tile[1] = next_tile(p, wk);
+        }
         const int pos0 = row_pos_or0(p, n0);
         const int pos1 = n1 == n0 ? pos0 : row_pos_or0(p, n1);
         load_rope<HPG>(p, pos0, o0);
         if (staged1 >= 0) load_rope<HPG>(p, pos1, o1);
     }
+    __syncthreads();  // s_tile, s_def
+    // thread 0 (the only one that reads summaries, through the copies it issues) waits
+    // for the launch before once a tile may hold summaries that launch writes
+    bool waited = !p.overlap_prologue;
     auto issue = [&](const Tile& x, int st) {
         if (tid == 0) {
+            if (!waited) {
+                bool clear = p.defer_begin != nullptr;
+                if (clear) {
+                    const int2 d = def_staged ? s_def[x.b]
+                                              : make_int2(__ldg(p.defer_begin + x.b), __ldg(p.defer_end + x.b));
+                    clear = x.c1 <= d.x || d.y <= x.c0;
+                }
+                if (!clear) {
+                    pdl_wait();
+                    waited = true;
+                }
+            }
             if constexpr (HPG == 4) {
                 // the boxes that hold the tile's regions (rows past the tensor end arrive
                 // as zeros)
@@ -1068,16 +1089,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1) score_select_kernel(const __
             }
         }
     };
-    // Thread 0 walks the share; the descriptors of the tiles in the two stages live in
-    // shared memory (the other threads only read them).
-    __shared__ Tile s_tile[kScoreStages];
-    if (tid == 0) {
-        // a short first tile, so that every SM starts scoring before the first requests
-        // of all SMs have drained
-        s_tile[0] = next_tile(p, wk, kBoxRows);
-        s_tile[1] = next_tile(p, wk);
-    }
-    if (p.overlap_prologue) pdl_wait();
     if (tid == 0) {
         if (s_tile[0].valid) issue(s_tile[0], 0);
         if (s_tile[1].valid) issue(s_tile[1], 1);
@@ -1156,7 +1167,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) score_select_kernel(const __
         float* keep = keep_all ? s_keep + (int)(x0 - xbeg) : nullptr;
         const int nreg = cur.c1 - cur.c0;
         if constexpr (HPG == 4) {
-            score_tile_rows(ring + st * kTileBytes, nreg, reinterpret_cast<const float4*>(s_qb[qbuf].q), w4,
+            score_tile_rows(ring + st * kTileBytes, nreg, reinterpret_cast<const uint4*>(s_qb[qbuf].qh), w4,
                             scores, keep, s_hist);
         } else {
             const uint4* tile = reinterpret_cast<const uint4*>(ring + st * kTileBytes);

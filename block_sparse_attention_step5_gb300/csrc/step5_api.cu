@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kernels.cuh"
@@ -68,32 +69,53 @@ int num_sms() {
 // ------------------------------------------------------------------ workspace layout
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// How step (4) splits a row's (top_k + 1)-entry key list: with fewer (row, group) pairs
-// than SMs, each pair gets a cluster of `cluster` blocks (1 to 16, one block per SM), the
-// largest whose shared memory fits and whose clusters are all resident at once (the
-// gather of each block runs at a per-SM rate, so the more SMs the better); otherwise one
-// block per pair.  Each block takes `eps` entries (whole pairs).
-void attn_plan(const step5_geometry* g, int N, int* cluster_out, int* eps_out, bool query_device) {
+// Step (4)'s part of the workspace: with fewer (row, group) pairs than half the SMs, a
+// pair's key list is split over several blocks, which need a barrier word per pair and
+// one state slot (m, l, o of each head) per block.  Sized from the geometry and N alone
+// (step5_sparse_attn has no r_cap); zero when no pair can be split.
+struct AttnArea {
+    size_t bar, part, end;
+    int max_blocks;
+};
+
+AttnArea attn_area(const step5_geometry* g, int N) {
+    AttnArea A{0, 0, 0, 0};
+    const int64_t items = (int64_t)N * g->num_kv_groups;
+    const int hq_g = g->num_q_heads / g->num_kv_groups;
+    if (2 * items > kAttnMaxBlocks) return A;
+    const int64_t blocks = std::min<int64_t>(items * kAttnMaxSplits, kAttnMaxBlocks);
+    A.max_blocks = (int)blocks;
+    A.bar = 0;
+    A.part = align256((size_t)items * 4);
+    A.end = align256(A.part + (size_t)blocks * hq_g * kAttnSlotFloats * 4);
+    return A;
+}
+
+// How step (4) splits a row's (top_k + 1)-entry key list: S blocks per (row, group),
+// as many as the SMs allow with one block per SM for the whole launch (the gather of
+// each block runs at a per-SM rate, so the more SMs the better), at most 64 and at least
+// 16 outputs of the final merge per block; S = 1 without a workspace area.  Each block
+// takes `eps` entries (whole pairs).
+void attn_plan(const step5_geometry* g, int N, bool split_area, int* splits_out, int* eps_out, bool query_device) {
     const int E = g->top_k + 1;
     const int64_t items = (int64_t)N * g->num_kv_groups;
     const int hq_g = g->num_q_heads / g->num_kv_groups;
     const int sms = query_device ? num_sms() : 152;
-    int cluster = 1;
-    if (items < sms) {
-        cluster = (int)(sms / items);
-        if (cluster > kMaxCluster) cluster = kMaxCluster;
-        while (cluster > 1 && attention_smem_bytes(cluster, hq_g) + kAttnStaticSmem > 232448) --cluster;
-        if (query_device)
-            while (cluster > 1 && attention_max_active_clusters(cluster, hq_g) < items) --cluster;
+    int64_t S = 1;
+    if (split_area) {
+        const AttnArea A = attn_area(g, N);
+        S = std::min<int64_t>({(int64_t)kAttnMaxSplits, sms / items, (int64_t)(hq_g * 128 + 15) / 16,
+                               (int64_t)A.max_blocks / items});
+        if (S < 1) S = 1;
     }
-    int eps = (E + cluster - 1) / cluster;
+    int eps = (int)((E + S - 1) / S);
     eps = (eps + 1) / 2 * 2;
-    *cluster_out = cluster;
+    *splits_out = (int)S;
     *eps_out = eps;
 }
 
-// Workspace of step (2)-(3).  The zero-maintained parts (histograms and counters) come
-// first.
+// Workspace: step (4)'s area first (its offset depends on the geometry and N only),
+// then step (2)-(3)'s, whose zero-maintained parts (histograms and counters) come first.
 struct Layout {
     size_t hist, cand_count, arrive1, thr, bar2, scores, cand, end;
 };
@@ -102,7 +124,7 @@ Layout layout(const step5_geometry* g, int N, int r_cap) {
     Layout L;
     const int G = g->num_kv_groups;
     const size_t ng = (size_t)N * G;
-    L.hist = 0;
+    L.hist = attn_area(g, N).end;
     L.cand_count = align256(L.hist + ng * kHistBins * 4);
     L.arrive1 = align256(L.cand_count + ng * 4);
     L.thr = align256(L.arrive1 + ng * 4);
@@ -356,7 +378,7 @@ step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_
                         const void* rope_cos_bf16, const void* rope_sin_bf16, const uint8_t* summaries_e4m3,
                         int32_t* sel_ids, int32_t* sel_count, float* scores_or_null, float* sel_scores_or_null,
                         void* workspace, size_t workspace_bytes, step5_stream_t stream, int overlap,
-                        bool launch) {
+                        const int32_t* defer_begin, const int32_t* defer_end, bool launch) {
     step5_status s = check_geometry(geom);
     if (s != STEP5_OK) return s;
     if (N <= 0 || B <= 0 || t_cap <= 0 || r_cap <= 0) return STEP5_ERR_INVALID_ARGUMENT;
@@ -398,6 +420,8 @@ step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_
     p.bar2 = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.bar2);
     p.num_sms = num_sms();
     p.overlap_prologue = overlap;
+    p.defer_begin = overlap ? defer_begin : nullptr;
+    p.defer_end = overlap ? defer_end : nullptr;
     p.status = st;
     p.N = N;
     p.B = B;
@@ -423,7 +447,7 @@ step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_
 step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, const void* q_bf16,
                        const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
                        const int32_t* row_pos, const int32_t* sel_ids, const int32_t* sel_count, void* out_bf16,
-                       step5_stream_t stream, bool launch) {
+                       void* workspace, size_t workspace_bytes, step5_stream_t stream, bool launch) {
     step5_status s = check_geometry(geom);
     if (s != STEP5_OK) return s;
     if (N <= 0 || B <= 0 || t_cap <= 0 || (t_cap % geom->region_tokens)) return STEP5_ERR_INVALID_ARGUMENT;
@@ -436,12 +460,15 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     const uint64_t rows = (uint64_t)B * G * t_cap;
     if (rows > (uint64_t)INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
     const int hq_g = geom->num_q_heads / G;
+    const AttnArea A = attn_area(geom, N);
+    const bool use_area = workspace != nullptr && workspace_bytes > 0 && A.end > 0;
+    if (use_area && workspace_bytes < A.end) return STEP5_ERR_WORKSPACE;
     if (!launch) return STEP5_OK;
 
     uint32_t* st = status_ptr();
     if (!st) return STEP5_ERR_CUDA;
-    int cluster, eps;
-    attn_plan(geom, N, &cluster, &eps, true);
+    int splits, eps;
+    attn_plan(geom, N, use_area, &splits, &eps, true);
     CUtensorMap kmap, vmap;
     if (!cache_maps(k_cache_bf16, v_cache_bf16, rows, &kmap, &vmap)) return STEP5_ERR_CUDA;
     AttnParams p;
@@ -459,9 +486,11 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     p.hq_g = hq_g;
     p.t_cap = t_cap;
     p.top_k = geom->top_k;
-    p.splits = cluster;
+    p.splits = splits;
     p.entries_per_split = eps;
-    p.cluster = cluster;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.bar = splits > 1 ? reinterpret_cast<uint32_t*>(ws + A.bar) : nullptr;
+    p.part = splits > 1 ? reinterpret_cast<float*>(ws + A.part) : nullptr;
     p.scale_log2 = geom->softmax_scale * 1.4426950408889634f;
     cudaError_t e = launch_attention(p, kmap, vmap, (cudaStream_t)stream, use_pdl());
     return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
@@ -489,17 +518,15 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
                                     size_t workspace_bytes, step5_stream_t stream) {
     return score_impl(geom, N, B, t_cap, r_cap, idx_q_bf16, w, row_seq, row_pos, rope_cos_bf16, rope_sin_bf16,
                       summaries_e4m3, sel_ids, sel_count, scores_or_null, sel_scores_or_null, workspace,
-                      workspace_bytes, stream, g_overlap_prologue, true);
+                      workspace_bytes, stream, g_overlap_prologue, nullptr, nullptr, true);
 }
 
 step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, const void* q_bf16,
                                const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
                                const int32_t* row_pos, const int32_t* sel_ids, const int32_t* sel_count,
                                void* out_bf16, void* workspace, size_t workspace_bytes, step5_stream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     return attn_impl(geom, N, B, t_cap, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count,
-                     out_bf16, stream, true);
+                     out_bf16, workspace, workspace_bytes, stream, true);
 }
 
 step5_status step5_decode_step(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
@@ -517,22 +544,25 @@ step5_status step5_decode_step(const step5_geometry* geom, int32_t N, int32_t B,
     if (s != STEP5_OK) return s;
     s = score_impl(geom, N, B, t_cap, r_cap, idx_q_bf16, w, row_seq, row_pos, rope_cos_bf16, rope_sin_bf16,
                    summaries_e4m3, sel_ids, sel_count, nullptr, nullptr, workspace, workspace_bytes, stream, 0,
-                   false);
+                   nullptr, nullptr, false);
     if (s != STEP5_OK) return s;
     s = attn_impl(geom, N, B, t_cap, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count,
-                  out_bf16, stream, false);
+                  out_bf16, workspace, workspace_bytes, stream, false);
     if (s != STEP5_OK) return s;
     s = summarize_impl(geom, B, t_cap, r_cap, max_regions_per_seq, idx_k_bf16, idx_z_bf16, rope_cos_bf16,
                        rope_sin_bf16, region_begin, region_end, summaries_e4m3, nullptr, stream, true);
     if (s != STEP5_OK) return s;
-    // the summary kernel (when launched) writes only summaries: the scoring prologue may
-    // read the other scoring inputs before waiting for it
+    // the summary kernel (when launched) writes only the summaries of regions
+    // [region_begin[b], region_end[b]): the scoring kernel reads its other inputs, and
+    // the summary tiles clear of those ranges, before waiting for it
+    const bool sum_launched = max_regions_per_seq > 0;
     s = score_impl(geom, N, B, t_cap, r_cap, idx_q_bf16, w, row_seq, row_pos, rope_cos_bf16, rope_sin_bf16,
                    summaries_e4m3, sel_ids, sel_count, nullptr, nullptr, workspace, workspace_bytes, stream,
-                   max_regions_per_seq > 0 ? 1 : 0, true);
+                   sum_launched ? 1 : 0, sum_launched ? region_begin : nullptr,
+                   sum_launched ? region_end : nullptr, true);
     if (s != STEP5_OK) return s;
     return attn_impl(geom, N, B, t_cap, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count,
-                     out_bf16, stream, true);
+                     out_bf16, workspace, workspace_bytes, stream, true);
 }
 
 }  // extern "C"

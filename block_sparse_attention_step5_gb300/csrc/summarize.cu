@@ -15,9 +15,13 @@ namespace step5 {
 
 namespace {
 
-constexpr int kRegionsPerCta = 4;  // x 64 dims = 256 threads
+// One region (64 dims) per block: a 64-thread block at <= 48 registers a thread fits beside
+// a scoring block (512 threads x 112 registers) on one SM, so in a decode step neither
+// kernel waits for the SMs the other holds.
+constexpr int kRegionsPerCta = 1;
+constexpr int kSumThreads = kRegionsPerCta * 64;
 
-__global__ void __launch_bounds__(256) summarize_kernel(SummarizeParams p) {
+__global__ void __maxnreg__(48) summarize_kernel(SummarizeParams p) {
     const int lr = threadIdx.x >> 6;   // region within the block
     const int d = threadIdx.x & 63;    // dim
     const int g = blockIdx.y;
@@ -87,8 +91,17 @@ __global__ void convert_kernel(const uint16_t* in, uint8_t* out, int64_t n) {
 }  // namespace
 
 cudaError_t launch_summarize(const SummarizeParams& p, int B, cudaStream_t stream) {
+    // the SM's shared-memory split of the scoring kernel that follows, so that blocks of
+    // both fit on one SM without the SM first draining to change it
+    static bool carveout_set = false;
+    if (!carveout_set) {
+        cudaError_t e = cudaFuncSetAttribute(summarize_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        carveout_set = true;
+    }
     dim3 grid((p.max_span + kRegionsPerCta - 1) / kRegionsPerCta, p.G, B);
-    summarize_kernel<<<grid, 256, 0, stream>>>(p);
+    summarize_kernel<<<grid, kSumThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

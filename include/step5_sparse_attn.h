@@ -125,10 +125,11 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
  * this is a deployment variant).  For callers that cannot allocate device memory -- code
  * whose device allocations all belong to a host framework, or a path where no allocator
  * is reachable or allocating would synchronise the device -- this call takes the same
- * inputs and outputs as step5_index_score_topk and keeps its scratch in a fixed 4 MiB
- * array of static device memory inside the library (one per device that loads it,
- * held until the process exits).  It allocates nothing.
- *  - Limit: step5_workspace_bytes(geom, N, r_cap) must be at most 4 MiB (for Step-5's
+ * inputs and outputs as step5_index_score_topk and keeps its scratch in a fixed array
+ * of static device memory inside the library (about 6 MiB: 4 MiB for this call's own
+ * scratch after the ~2 MiB any workspace keeps for step5_sparse_attn; one array per
+ * device that loads the library, held until the process exits).  It allocates nothing.
+ *  - Limit: step5_workspace_bytes(geom, N, r_cap) must fit the array (for Step-5's
  *    geometry about N * r_cap <= 220,000, e.g. one row at 1M tokens or four at 128K);
  *    larger problems return STEP5_ERR_WORKSPACE before anything is enqueued.
  *  - The first call on a device looks up the array's device address (with that device
@@ -157,8 +158,16 @@ step5_status step5_index_score_topk_noalloc(const step5_geometry* geom, int32_t 
  * step5_index_score_topk (ids must be distinct candidates of the row, < o);
  * out_bf16: [N][num_q_heads][head_dim].  Cache rows past p are never read into the
  * result (they may hold anything).  t_cap must be a multiple of region_tokens; pointers
- * 16-byte aligned.  workspace / workspace_bytes: not used by this call (may be NULL / 0);
- * the splits of a row merge on chip. */
+ * 16-byte aligned.
+ * workspace / workspace_bytes: a workspace of step5_workspace_bytes(geom, N, any r_cap)
+ * bytes, zeroed once (step5_workspace_init), or NULL / 0.  With fewer (row, group) pairs
+ * than half the SMs, the call splits each pair's key list over several blocks, which
+ * exchange their partial softmax states through the workspace's first part (a barrier
+ * word per pair and ~8 KB per block, at most ~2 MiB) and merge them in a fixed order;
+ * the result does not depend on the split or on timing.  NULL / 0: one block per pair
+ * (same result, slower when the pairs are few).  A non-NULL workspace smaller than that
+ * part returns STEP5_ERR_WORKSPACE.  A bounded wait that gives up raises
+ * STEP5_DEV_TIMEOUT (re-zero the workspace before the next call). */
 step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
                                int32_t t_cap, const void* q_bf16,
                                const void* k_cache_bf16, const void* v_cache_bf16,
@@ -173,8 +182,10 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
  * argument is checked before anything is enqueued; then:
  *  - summaries of regions [region_begin[b], region_end[b]) are written (skipped when
  *    max_regions_per_seq is 0; the summary inputs must still be valid pointers);
- *  - the scoring kernel reads its non-summary inputs before waiting for the summary
- *    kernel (the step5_set_prologue_overlap contract holds by construction here).
+ *  - the scoring kernel reads its non-summary inputs, and the summaries of regions
+ *    outside [region_begin[b], region_end[b]), before waiting for the summary kernel
+ *    (that kernel writes nothing else, so the step5_set_prologue_overlap contract holds
+ *    by construction here).
  * Layouts, ownership and errors are those of the three calls (scores and picked scores
  * are not exported).  workspace: as for step5_index_score_topk. */
 step5_status step5_decode_step(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
@@ -187,9 +198,9 @@ step5_status step5_decode_step(const step5_geometry* geom, int32_t N, int32_t B,
                                int32_t* sel_count, void* out_bf16, void* workspace, size_t workspace_bytes,
                                step5_stream_t stream);
 
-/* Bytes of device workspace that step5_index_score_topk needs for N rows and r_cap
- * summary slots (the same buffer may be passed to step5_sparse_attn, which ignores it).
- * Returns 0 for an unsupported geometry. */
+/* Bytes of device workspace that step5_index_score_topk and step5_sparse_attn need for
+ * N rows and r_cap summary slots (one buffer serves both: step (4)'s part comes first
+ * and depends on the geometry and N only).  Returns 0 for an unsupported geometry. */
 size_t step5_workspace_bytes(const step5_geometry* geom, int32_t N, int32_t r_cap);
 
 /* Zero-fills a workspace (enqueued on stream).  A zeroed workspace is ready for a call,

@@ -338,8 +338,9 @@ def test_split_path_share_shapes(s5, positions, B):
 
 @pytest.mark.parametrize("cfg", [{"positions": [30000, 41000, 4100, 70], "B": 3}, 4])
 def test_decode_step_entry_matches_the_three_calls(s5, cfg):
-    """step5_decode_step (one call: overlapped prologue, K/V requested into L2 by the
-    selection) gives the same selection and output as the three calls."""
+    """step5_decode_step (one call: the scoring kernel fetches the summary tiles clear of
+    the regions being summarised before waiting for the summary kernel) gives the same
+    selection and output as the three calls."""
     geom = s5.STEP5_GEOMETRY
     w = S.workload(cfg, seed=31)
     dev = torch.device("cuda")
@@ -366,3 +367,50 @@ def test_decode_step_entry_matches_the_three_calls(s5, cfg):
     for a, b in zip(res[0][:3], res[1][:3]):
         assert torch.equal(a, b)
     assert np.array_equal(res[0][3], res[1][3])
+
+
+@pytest.mark.parametrize("cfg", [{"positions": [30000, 41000, 4100, 70], "B": 3}, {"positions": [1016], "B": 1}])
+def test_attention_split_over_blocks_and_single_block(s5, cfg):
+    """With a workspace, few (row, group) pairs split their key list over several blocks
+    that merge through it; without one, one block takes each pair.  Both agree with the
+    oracle on the same selection, and the split result repeats bit for bit."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload(cfg, seed=37)
+    t = S.materialize(w, device="cuda")
+    g = run_path(s5, geom, w, t, path=0)
+    assert g["status"] == 0
+    h = host_inputs(t)
+    ref_out, _ = oracle.attend_batch(h["q"], h["k_cache"], h["v_cache"], w.row_seq, w.row_pos,
+                                     g["sel_ids"], g["sel_count"], geom.softmax_scale)
+    dev = t["q"].device
+    sel_ids = torch.from_numpy(g["sel_ids"]).to(dev)
+    sel_count = torch.from_numpy(g["sel_count"]).to(dev)
+    ws = s5.Workspace.create(geom, w.N, w.r_cap, device=dev)
+    outs = []
+    for workspace in (ws.tensor, None, ws.tensor):
+        out = torch.full((w.N, geom.num_q_heads, geom.head_dim), float("nan"), dtype=torch.bfloat16, device=dev)
+        s5.step5_sparse_attn(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
+                             sel_ids, sel_count, out, workspace)
+        torch.cuda.synchronize()
+        outs.append(out.float().cpu().numpy())
+    assert s5.step5_device_status() == 0
+    for i, o in enumerate(outs):
+        check_out(o, ref_out, where="one block" if i == 1 else "split")
+    assert np.array_equal(outs[0], outs[2])
+
+
+def test_attention_rejects_a_workspace_too_small(s5):
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [4100], "B": 1}, seed=37)
+    t = S.materialize(w, device="cuda")
+    dev = t["q"].device
+    sel_ids = torch.full((1, 4, 512), -1, dtype=torch.int32, device=dev)
+    sel_count = torch.zeros((1, 4), dtype=torch.int32, device=dev)
+    out = torch.zeros((1, geom.num_q_heads, geom.head_dim), dtype=torch.bfloat16, device=dev)
+    tiny = torch.zeros(256, dtype=torch.uint8, device=dev)
+    with pytest.raises(s5.Step5Error) as e:
+        s5.step5_sparse_attn(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
+                             sel_ids, sel_count, out, tiny)
+    assert e.value.status == 3
+    torch.cuda.synchronize()
+    assert (out.cpu() == 0).all()   # nothing was enqueued
