@@ -20,9 +20,10 @@
 //    group's query heads as the 16-row left operand (4, 8 or 16 heads; unused rows are
 //    zero); P is rounded to bf16 for the PV product, the softmax state is fp32.
 //  * the warps merge through shared memory (weights once per (warp, head)); with S > 1
-//    every block writes its state (m, l, o per head) to the workspace, the (row, group)'s
-//    blocks meet at a barrier word, and each block then merges a slice of the outputs
-//    over all S states in split order, so the result does not depend on timing.
+//    every block writes its state (m, l, o per head) to the workspace and raises its flag
+//    (an epoch per (row, group) tells launches apart); once all S flags are up each block
+//    merges a slice of the outputs over all S states in split order, so the result does
+//    not depend on timing.
 #include "kernels.cuh"
 
 namespace step5 {
@@ -34,7 +35,8 @@ constexpr int kRegionBytes = 2048;                    // 8 tokens x 128 dims x b
 constexpr int kPairBytes = 4 * kRegionBytes;          // K (2 regions) + V (2 regions)
 constexpr int kPairBufs = kAttnWarps * kAttnStages + 1;  // warp 0 has one more
 constexpr int kStageBytes = kPairBufs * kPairBytes;
-constexpr int kMergeFloatsPerWarp = 16 * 128 + 32;    // O[16][128], m[16], l[16]
+constexpr int kMergeRow = 136;                        // a row of O: 128 floats + 8 of padding
+constexpr int kMergeFloatsPerWarp = 16 * kMergeRow + 32;  // O[16][kMergeRow], m[16], l[16]
 constexpr int kBarBytes = kPairBufs * 8;
 constexpr int kSlotFloats = kAttnSlotFloats;         // m, l, o[128] of one head row
 static_assert(kAttnWarps * kMergeFloatsPerWarp * 4 <= kStageBytes, "warp merge area must fit");
@@ -84,6 +86,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     const int b = p.row_seq[n];
     const int pos = p.row_pos[n];
     int cnt = p.sel_count[ng];
+    const uint32_t epoch = S > 1 ? __ldcg(p.bar + ng) : 0u;
     __syncthreads();
     STEP5_STAMP(4, 8);
     if (b < 0 || b >= p.B || pos < 0 || pos >= p.t_cap) {
@@ -305,20 +308,24 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     // ---- merge the warps through shared memory (reuses the stage buffers)
     STEP5_STAMP(4, 4);
     __syncthreads();
+    // rows at or past hq_g hold zero queries and are skipped; the padded rows put the 8
+    // rows of one store on 8 different bank groups (float2 stores)
     float* mw = reinterpret_cast<float*>(smem) + warp * kMergeFloatsPerWarp;
+    if (qr < hq_g) {
 #pragma unroll
-    for (int nn = 0; nn < 16; ++nn) {
-        const int dd = nn * 8 + qc;
-        mw[qr * 128 + dd] = o[nn][0];
-        mw[qr * 128 + dd + 1] = o[nn][1];
-        mw[(qr + 8) * 128 + dd] = o[nn][2];
-        mw[(qr + 8) * 128 + dd + 1] = o[nn][3];
+        for (int nn = 0; nn < 16; ++nn)
+            *reinterpret_cast<float2*>(mw + qr * kMergeRow + nn * 8 + qc) = make_float2(o[nn][0], o[nn][1]);
+    }
+    if (qr + 8 < hq_g) {
+#pragma unroll
+        for (int nn = 0; nn < 16; ++nn)
+            *reinterpret_cast<float2*>(mw + (qr + 8) * kMergeRow + nn * 8 + qc) = make_float2(o[nn][2], o[nn][3]);
     }
     if ((lane & 3) == 0) {
-        mw[2048 + qr] = m0;
-        mw[2048 + qr + 8] = m1;
-        mw[2048 + 16 + qr] = l0;
-        mw[2048 + 16 + qr + 8] = l1;
+        mw[16 * kMergeRow + qr] = m0;
+        mw[16 * kMergeRow + qr + 8] = m1;
+        mw[16 * kMergeRow + 16 + qr] = l0;
+        mw[16 * kMergeRow + 16 + qr + 8] = l1;
     }
     __syncthreads();
     STEP5_STAMP(4, 5);
@@ -333,12 +340,12 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         for (int r0 = 0; r0 < hq_g; r0 += 32 / kAttnWarps) {
             const int r = r0 + lane / kAttnWarps, w = lane % kAttnWarps;
             const bool ok = r < hq_g;
-            const float m = ok ? mall[w * kMergeFloatsPerWarp + 2048 + r] : -INFINITY;
+            const float m = ok ? mall[w * kMergeFloatsPerWarp + 16 * kMergeRow + r] : -INFINITY;
             float M = m;
 #pragma unroll
             for (int o = 1; o < kAttnWarps; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
             const float sc = exp2f(m - ((M == -INFINITY) ? 0.0f : M));
-            float L = ok ? mall[w * kMergeFloatsPerWarp + 2048 + 16 + r] * sc : 0.0f;
+            float L = ok ? mall[w * kMergeFloatsPerWarp + 16 * kMergeRow + 16 + r] * sc : 0.0f;
 #pragma unroll
             for (int o = 1; o < kAttnWarps; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
             if (ok) {
@@ -355,7 +362,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         for (int r = rpar; r < hq_g; r += 2) {
             float O = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * 128 + d] * s_wsc[w][r];
+            for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * kMergeRow + d] * s_wsc[w][r];
             p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / s_L[r]);
         }
         return;
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         for (int r = rpar; r < hq_g; r += 2) {
             float O = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * 128 + d] * s_wsc[w][r];
+            for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * kMergeRow + d] * s_wsc[w][r];
             mine[r * kSlotFloats + 2 + d] = O;
             if (d == 0) {
                 mine[r * kSlotFloats] = s_M[r];
@@ -377,14 +384,31 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         }
     }
     STEP5_STAMP(4, 11);
-    // every state of the (row, group) is written once all its blocks have arrived
+    // The exchange: each block raises its flag to the (row, group)'s epoch + 1 (release)
+    // once its state is out, and reads the states after seeing every flag raised
+    // (acquire); block 0 then advances the epoch for the next launch (every block has
+    // read it by then, since each reads it before raising its flag).
     __syncthreads();
+    uint32_t* fl = p.flags + ng * kAttnMaxSplits;
+    if (tid == 0) st_release_u32(fl + split, epoch + 1u);
     bool ok = true;
-    if (tid == 0) ok = wait_gen(p.bar + ng, arrive_gen(p.bar + ng, (uint32_t)S));
+    if (warp == 0) {
+        ok = false;
+        for (uint32_t it = 0; it < kBarrierPolls; ++it) {
+            bool all = true;
+            for (int sp = lane; sp < S; sp += 32) all &= ld_relaxed_u32(fl + sp) == epoch + 1u;
+            if (__all_sync(0xffffffffu, all)) {
+                ok = true;
+                break;
+            }
+        }
+        fence_acquire_gpu();  // the flags' release stores happen before the reads below
+    }
     if (__syncthreads_or(!ok)) {
         if (tid == 0) raise_status(p.status, kDevTimeout);
         return;
     }
+    if (split == 0 && tid == 0) p.bar[ng] = epoch + 1u;
     STEP5_STAMP(4, 6);
 
     // ---- this block's slice [e_lo, e_hi) of the hq_g * 128 outputs, merged over the S

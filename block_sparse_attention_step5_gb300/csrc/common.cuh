@@ -214,6 +214,16 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* a) {
     return v;
 }
 
+// Relaxed (no ordering) load for polling; pair with fence_acquire_gpu once it succeeds.
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* a) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+
+// Acquire side of a release store seen by an earlier relaxed load of this thread.
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void st_release_u32(uint32_t* a, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
 }
@@ -240,7 +250,10 @@ __device__ __forceinline__ uint32_t arrive_gen(uint32_t* word, uint32_t nb) {
 __device__ __forceinline__ bool wait_gen(const uint32_t* word, uint32_t gen) {
     if (gen == kArrivedLast) return true;
     for (uint32_t it = 0; it < kBarrierPolls; ++it)
-        if ((ld_acquire_u32(word) >> 16) != gen) return true;
+        if ((ld_relaxed_u32(word) >> 16) != gen) {
+            fence_acquire_gpu();
+            return true;
+        }
     return false;
 }
 

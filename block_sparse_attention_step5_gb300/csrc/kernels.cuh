@@ -72,8 +72,9 @@ constexpr int kAttnStages = 2;          // pair buffers per warp (warp 0: one mo
 constexpr int kAttnMaxSplits = 64;      // blocks per (row, group)
 constexpr int kAttnMaxBlocks = 256;     // blocks of one launch that share a (row, group) with others
 constexpr int kAttnSlotFloats = 130;    // m, l, o[128] of one head row
-// upper bound of step (4)'s workspace area (barrier words of <= 128 pairs, 256 slots of 16 heads)
-constexpr size_t kAttnAreaMaxBytes = 512 + (size_t)kAttnMaxBlocks * 16 * kAttnSlotFloats * 4;
+// upper bound of step (4)'s workspace area (epochs and flags of <= 128 pairs, 256 slots of 16 heads)
+constexpr size_t kAttnAreaMaxBytes = 512 + (size_t)(kAttnMaxBlocks / 2) * kAttnMaxSplits * 4 +
+                                     (size_t)kAttnMaxBlocks * 16 * kAttnSlotFloats * 4;
 
 struct AttnParams {
     const uint16_t* q;       // [N][Hq][128]
@@ -83,7 +84,8 @@ struct AttnParams {
     const int32_t* sel_count;
     uint16_t* out;           // [N][Hq][128]
     float* part;             // splits > 1: [N*G][splits][hq_g][130] block states
-    uint32_t* bar;           // splits > 1: [N*G] barrier words (generation | arrivals)
+    uint32_t* bar;           // splits > 1: [N*G] epoch of each (row, group)'s state exchange
+    uint32_t* flags;         // splits > 1: [N*G][kAttnMaxSplits] epoch + 1 once a block's state is out
     uint32_t* status;
     int N, B, G, Hq, hq_g, t_cap, top_k;
     int splits, entries_per_split;  // blocks per (row, group) and the entries each takes

@@ -887,8 +887,11 @@ __device__ void publish_threshold(const ScoreParams& p, int ng, uint32_t gen, ui
 // gen; -1 when the wait gives up.
 __device__ int wait_threshold(const ScoreParams& p, int ng, uint32_t gen) {
     for (uint32_t it = 0; it < kBarrierPolls; ++it) {
-        const uint32_t v = ld_acquire_u32(p.thr + ng);
-        if ((v >> 12) != gen) return (int)(v & (kHistBins - 1));
+        const uint32_t v = ld_relaxed_u32(p.thr + ng);
+        if ((v >> 12) != gen) {
+            fence_acquire_gpu();
+            return (int)(v & (kHistBins - 1));
+        }
     }
     return -1;
 }

@@ -70,23 +70,24 @@ int num_sms() {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Step (4)'s part of the workspace: with fewer (row, group) pairs than half the SMs, a
-// pair's key list is split over several blocks, which need a barrier word per pair and
-// one state slot (m, l, o of each head) per block.  Sized from the geometry and N alone
+// pair's key list is split over several blocks, which need an epoch word per pair, a
+// flag per (pair, block) and one state slot (m, l, o of each head) per block.  Sized from the geometry and N alone
 // (step5_sparse_attn has no r_cap); zero when no pair can be split.
 struct AttnArea {
-    size_t bar, part, end;
+    size_t bar, flags, part, end;
     int max_blocks;
 };
 
 AttnArea attn_area(const step5_geometry* g, int N) {
-    AttnArea A{0, 0, 0, 0};
+    AttnArea A{0, 0, 0, 0, 0};
     const int64_t items = (int64_t)N * g->num_kv_groups;
     const int hq_g = g->num_q_heads / g->num_kv_groups;
     if (2 * items > kAttnMaxBlocks) return A;
     const int64_t blocks = std::min<int64_t>(items * kAttnMaxSplits, kAttnMaxBlocks);
     A.max_blocks = (int)blocks;
     A.bar = 0;
-    A.part = align256((size_t)items * 4);
+    A.flags = align256((size_t)items * 4);
+    A.part = align256(A.flags + (size_t)items * kAttnMaxSplits * 4);
     A.end = align256(A.part + (size_t)blocks * hq_g * kAttnSlotFloats * 4);
     return A;
 }
@@ -490,6 +491,7 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     p.entries_per_split = eps;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.bar = splits > 1 ? reinterpret_cast<uint32_t*>(ws + A.bar) : nullptr;
+    p.flags = splits > 1 ? reinterpret_cast<uint32_t*>(ws + A.flags) : nullptr;
     p.part = splits > 1 ? reinterpret_cast<float*>(ws + A.part) : nullptr;
     p.scale_log2 = geom->softmax_scale * 1.4426950408889634f;
     cudaError_t e = launch_attention(p, kmap, vmap, (cudaStream_t)stream, use_pdl());

@@ -162,10 +162,11 @@ step5_status step5_index_score_topk_noalloc(const step5_geometry* geom, int32_t 
  * workspace / workspace_bytes: a workspace of step5_workspace_bytes(geom, N, any r_cap)
  * bytes, zeroed once (step5_workspace_init), or NULL / 0.  With fewer (row, group) pairs
  * than half the SMs, the call splits each pair's key list over several blocks, which
- * exchange their partial softmax states through the workspace's first part (a barrier
- * word per pair and ~8 KB per block, at most ~2 MiB) and merge them in a fixed order;
- * the result does not depend on the split or on timing.  NULL / 0: one block per pair
- * (same result, slower when the pairs are few).  A non-NULL workspace smaller than that
+ * exchange their partial softmax states through the workspace's first part (an epoch
+ * word per pair, a flag per block and ~8 KB of state per block, at most ~2.1 MiB) and
+ * merge them in a fixed order; the result does not depend on timing.  NULL / 0: one
+ * block per pair (slower when the pairs are few; the fp32 merge order differs, so the
+ * bf16 outputs may differ in the last bit).  A non-NULL workspace smaller than that
  * part returns STEP5_ERR_WORKSPACE.  A bounded wait that gives up raises
  * STEP5_DEV_TIMEOUT (re-zero the workspace before the next call). */
 step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
