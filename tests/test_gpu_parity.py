@@ -414,3 +414,32 @@ def test_attention_rejects_a_workspace_too_small(s5):
     assert e.value.status == 3
     torch.cuda.synchronize()
     assert (out.cpu() == 0).all()   # nothing was enqueued
+
+
+def test_picks_clustered_in_one_share(s5):
+    """The K best regions are the last 600 of a long row (equal scores; every other score
+    is zero): one or two blocks of the split launch hold all the picks, and every score
+    outside them ties at zero; twice on one workspace."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [320000], "B": 1}, seed=53)
+    t = S.materialize(w, device="cuda")
+    R = int(w.row_pos[0]) // 8
+    summ = torch.zeros_like(t["summaries"])
+    summ[0, :, R - 600:R, :] = 0x38  # e4m3 +1.0
+    t["summaries"].copy_(summ)
+    t["idx_q"].abs_()  # no rotation below: every head's dot product with +1.0 is positive
+    t["w"].abs_()
+    K = geom.top_k
+    ws = s5.Workspace.create(geom, w.N, w.r_cap)
+    ids = torch.empty((1, 4, K), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((1, 4), dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        ids.fill_(-7)
+        s5.step5_index_score_topk(geom, t["idx_q"], t["w"], t["row_seq"], t["row_pos"], None, None,
+                                  t["summaries"], ids, cnt, ws.tensor, t_cap=w.t_cap)
+        torch.cuda.synchronize()
+        assert s5.step5_device_status() == 0
+        assert (cnt.cpu() == K).all()
+        want = torch.arange(R - 600, R - 600 + K, dtype=torch.int32)
+        for g in range(4):
+            assert torch.equal(ids[0, g].cpu(), want)
