@@ -62,6 +62,7 @@ def _load():
             "orc_score_group": (None, [P, P, i32, i32, i32, i32, P, P, P, i64, P]),
             "orc_select_topk": (i32, [P, i64, i32, P]),
             "orc_attend_group": (None, [P, i32, i32, P, P, P, i32, i32, i32, f64, P]),
+            "orc_sigmoid_gate": (None, [P, P, i64, i32]),
             "orc_summarize_batch": (i32, [i32, i32, i64, i64, i32, i32, i32, P, P, P, P,
                                           P, P, P, P, i32]),
             "orc_score_batch": (i32, [i32, i32, i32, i32, i32, i32, i64, P, P, P, P, P,
@@ -271,6 +272,16 @@ def attend_batch(q, k_cache, v_cache, row_seq, row_pos, sel_ids, sel_count, scal
                                   _p(_c(row_pos, np.int32)), _p(ids), _p(cnt), _p(out),
                                   nthreads)
     return out, th
+
+
+def sigmoid_gate(out, gate_codes) -> np.ndarray:
+    """out [N][Hq][D] fp64 scaled by sigmoid(gate [N][Hq] bf16 codes), head by head (a new
+    array; the per-head sigmoid output gate applied before the output's rounding)."""
+    o = np.array(out, dtype=np.float64, order="C", copy=True)
+    g = _c(gate_codes, np.uint16)
+    assert g.size * o.shape[-1] == o.size
+    _load().orc_sigmoid_gate(_p(o), _p(g), g.size, o.shape[-1])
+    return o
 
 
 def bf16_round_array(x: np.ndarray) -> np.ndarray:

@@ -264,6 +264,18 @@ void orc_attend_group(const uint16_t* q, int hq_g, int head_dim,
 }
 
 /* ------------------------------------------------------------------------------ */
+/* After step 4: the per-head sigmoid output gate.                                   */
+/* ------------------------------------------------------------------------------ */
+
+void orc_sigmoid_gate(double* out, const uint16_t* gate, int64_t rows, int head_dim) {
+    for (int64_t r = 0; r < rows; ++r) {
+        const double g = orc_bf16_value(gate[r]);
+        const double s = 1.0 / (1.0 + exp(-g));
+        for (int d = 0; d < head_dim; ++d) out[r * head_dim + d] *= s;
+    }
+}
+
+/* ------------------------------------------------------------------------------ */
 /* Batched drivers: independent items spread over host threads.                     */
 /* ------------------------------------------------------------------------------ */
 

@@ -81,6 +81,14 @@ void orc_attend_group(const uint16_t* q, int hq_g, int head_dim,
                       const int32_t* sel, int cnt, int pos, int region_tokens,
                       double scale, double* out);
 
+/* ---- after step 4: the per-head sigmoid output gate ----------------------------------
+ * ("Step-5-Preview on one 256 GB Mac", the native-family commit: Step-5's glue keeps
+ * "the per-head sigmoid gate" among StepFun's rounding points.)  Reading: one gate
+ * logit per (row, query head), a bf16 input; every output dim of the head is scaled by
+ * sigmoid(logit) before the output's single bf16 rounding.
+ * out: [rows][head_dim] fp64, scaled in place; gate: [rows] bf16 codes.              */
+void orc_sigmoid_gate(double* out, const uint16_t* gate, int64_t rows, int head_dim);
+
 /* ---- batched drivers: plain loops over independent items, spread over nthreads
  *      host threads (0 = all online cores).  They add no arithmetic of their own. ---- */
 
