@@ -215,6 +215,14 @@ def run_ours(args, rank, world, local_rank):
             s5.step5_sparse_attn(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
                                  sel_ids, sel_count, out, ws.tensor)
 
+        # the per-head sigmoid output gate after attention (timed beside the step only)
+        gate = (torch.randn((N, geom.num_q_heads), generator=torch.Generator().manual_seed(61)) * 3).to(
+            torch.bfloat16).to(dev)
+
+        def call_attn_gated():
+            s5.step5_sparse_attn_gated(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
+                                       sel_ids, sel_count, gate, out, ws.tensor)
+
         def step():
             # the whole step in one C-ABI call (summaries, score + select, attention)
             s5.step5_decode_step(geom, t, ws, sel_ids, sel_count, out, max_regions_per_seq=span)
@@ -269,13 +277,14 @@ def run_ours(args, rank, world, local_rank):
         # events bracket the kernels alone; without event nodes in graphs, eager calls
         # behind a 1 GiB write that covers their launch
         steps_b = steps
-        times_b = np.zeros((steps_b, 3))
+        calls_b = (call_sum, call_score, call_attn, call_attn_gated)
+        times_b = np.zeros((steps_b, len(calls_b)))
         try:
-            evg = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+            evg = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls_b) + 1)]
             g_b = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_b, capture_error_mode="thread_local"):
                 evg[0].record()
-                for j, fn in enumerate((call_sum, call_score, call_attn)):
+                for j, fn in enumerate(calls_b):
                     fn()
                     evg[j + 1].record()
             breakdown_how = "CUDA graph with event nodes between the calls"
@@ -284,26 +293,27 @@ def run_ours(args, rank, world, local_rank):
                 flush.zero_()
                 g_b.replay()
                 torch.cuda.synchronize()
-                times_b[i] = [evg[j].elapsed_time(evg[j + 1]) for j in range(3)]
+                times_b[i] = [evg[j].elapsed_time(evg[j + 1]) for j in range(len(calls_b))]
         except (TypeError, RuntimeError):
             breakdown_how = "eager calls behind a 1 GiB write"
             hold = torch.empty(4 * FLUSH_BYTES, dtype=torch.uint8, device=dev)
-            evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps_b)]
+            evb = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls_b) + 1)] for _ in range(steps_b)]
             barrier()
             for i in range(steps_b):
                 hold.zero_()
                 evb[i][0].record(stream)
-                for j, fn in enumerate((call_sum, call_score, call_attn)):
+                for j, fn in enumerate(calls_b):
                     fn()
                     evb[i][j + 1].record(stream)
             barrier()
-            times_b = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evb])
+            times_b = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(calls_b))] for e in evb])
             del hold
-        per_sum, per_score, per_attn = times_b[:, 0], times_b[:, 1], times_b[:, 2]
+        per_sum, per_score, per_attn, per_gated = times_b[:, 0], times_b[:, 1], times_b[:, 2], times_b[:, 3]
         bytes_step, bytes_score = step_bytes(w, geom)
         res = dict(w=w, ms=ms, ms_min=float(per_step.min()), per_score=float(per_score.mean()),
                    breakdown_how=breakdown_how,
-                   per_attn=float(per_attn.mean()), per_sum=float(per_sum.mean()), bytes_step=bytes_step,
+                   per_attn=float(per_attn.mean()), per_sum=float(per_sum.mean()),
+                   per_gated=float(per_gated.mean()), bytes_step=bytes_step,
                    bytes_score=bytes_score, launches=launches_per_step * steps, path=path, wall=wall,
                    clocks=sampler.summary() if sampler else None)
 
@@ -372,6 +382,7 @@ def run_ours(args, rank, world, local_rank):
         "breakdown_us": {"summarize": round(head["per_sum"] * 1e3, 2),
                          "score_select": round(head["per_score"] * 1e3, 2),
                          "attention": round(head["per_attn"] * 1e3, 2),
+                         "attention_gated": round(head["per_gated"] * 1e3, 2),
                          "how": head["breakdown_how"]},
         "roofline": {"kernel": "score_select_kernel (step5_index_score_topk, split path)",
                      "bound": "hbm", "achieved": round(score_gbs, 1), "peak": peak, "unit": "GB/s",
@@ -396,7 +407,8 @@ def run_ours(args, rank, world, local_rank):
                              "select_path": "fused" if sec["path"] == 1 else "split",
                              "breakdown_us": {"summarize": round(sec["per_sum"] * 1e3, 2),
                                               "score_select": round(sec["per_score"] * 1e3, 2),
-                                              "attention": round(sec["per_attn"] * 1e3, 2)}}
+                                              "attention": round(sec["per_attn"] * 1e3, 2),
+                                              "attention_gated": round(sec["per_gated"] * 1e3, 2)}}
         line["gpu_launches"] += sec["launches"]
     if rank == 0 and not args.no_cpu_baseline:
         cb = oracle_sample(args.workload, quarter=False)

@@ -10,6 +10,7 @@ Steps (TensorFold PR #903, "Step-5-Preview on one 256 GB Mac", CSA-indexer commi
   step5_region_summarize  -- e4m3 summary of each completed 8-token region
   step5_index_score_topk  -- sum_h relu(e4m3(q_h) . summary) * w_h, top-k by (-score, id)
   step5_sparse_attn       -- attention over the picked regions plus the row's own region
+  step5_sparse_attn_gated -- the same, followed by the per-head sigmoid output gate
 """
 from __future__ import annotations
 
@@ -25,7 +26,7 @@ from ._build import LIB, build  # noqa: F401
 
 __all__ = [
     "Step5Error", "Geometry", "STEP5_GEOMETRY", "library_path", "load",
-    "step5_region_summarize", "step5_index_score_topk", "step5_sparse_attn",
+    "step5_region_summarize", "step5_index_score_topk", "step5_sparse_attn", "step5_sparse_attn_gated",
     "step5_index_score_topk_noalloc",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
     "step5_set_select_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
@@ -90,6 +91,7 @@ def load():
         "step5_index_score_topk": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P,
                                          P, sz, P]),
         "step5_sparse_attn": (i32, [G, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]),
+        "step5_sparse_attn_gated": (i32, [G, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, sz, P]),
         "step5_decode_step": (i32, [G, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
                                     P, P, P, P, sz, P]),
         "step5_index_score_topk_noalloc": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P,
@@ -213,6 +215,20 @@ def step5_index_score_topk_noalloc(geom, idx_q, w, row_seq, row_pos, cos, sin, s
         ctypes.byref(Geometry.of(geom)), N, B, int(t_cap), r_cap, _ptr(idx_q), _ptr(w),
         _ptr(row_seq), _ptr(row_pos), _ptr(cos), _ptr(sin), _ptr(summaries), _ptr(sel_ids),
         _ptr(sel_count), _ptr(scores), _ptr(sel_scores), _stream(stream)))
+
+
+def step5_sparse_attn_gated(geom, q, k_cache, v_cache, row_seq, row_pos, sel_ids, sel_count, gate,
+                            out, workspace, stream=None):
+    """step5_sparse_attn followed by the per-head sigmoid output gate: gate [N][Hq] bf16
+    logits; every dim of head h of row n is scaled by sigmoid(gate[n][h]) before the
+    output's rounding."""
+    N = q.shape[0]
+    B, _, t_cap, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("step5_sparse_attn_gated", load().step5_sparse_attn_gated(
+        ctypes.byref(Geometry.of(geom)), N, B, t_cap, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(row_seq), _ptr(row_pos), _ptr(sel_ids), _ptr(sel_count), _ptr(gate), _ptr(out),
+        _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def step5_sparse_attn(geom, q, k_cache, v_cache, row_seq, row_pos, sel_ids, sel_count, out,

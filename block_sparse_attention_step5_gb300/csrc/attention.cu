@@ -1,4 +1,5 @@
-// attention.cu -- step (4): attention over the picked regions plus the row's own region.
+// attention.cu -- step (4): attention over the picked regions plus the row's own region
+// (and, optionally, the per-head sigmoid output gate that follows it).
 //
 // "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903), CSA-indexer commit:
 // "attention over those regions and the row's own"; below 512 regions every region is
@@ -52,6 +53,14 @@ size_t attn_smem_bytes() { return 1024 + kStageBytes + kBarBytes; }
 __device__ __forceinline__ uint32_t tile_off(int t, int c16) {
     const int half = c16 >> 3, c = c16 & 7;
     return (uint32_t)(half * 1024 + t * 128 + ((c ^ t) << 4));
+}
+
+// The per-head sigmoid output gate of query head h of row n (1 without a gate): every
+// output dim of the head is scaled by sigmoid(logit) before the one bf16 rounding.
+__device__ __forceinline__ float gate_factor(const AttnParams& p, int n, int h) {
+    if (p.gate == nullptr) return 1.0f;
+    const float g = bf16_to_f32(p.gate[(int64_t)n * p.Hq + h]);
+    return 1.0f / (1.0f + expf(-g));
 }
 
 __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -363,7 +372,8 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
             float O = 0.0f;
 #pragma unroll
             for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * kMergeRow + d] * s_wsc[w][r];
-            p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] = f32_to_bf16_bits(O / s_L[r]);
+            p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] =
+                f32_to_bf16_bits(O / s_L[r] * gate_factor(p, n, g * hq_g + r));
         }
         return;
     }
@@ -468,7 +478,8 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         const int e = e_lo + t, r = e >> 7;
         float O = 0.0f;
         for (int sp = 0; sp < S; ++sp) O += s_val[sp * nout + t] * s_sw[r - r_lo][sp];
-        p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + (e & 127)] = f32_to_bf16_bits(O / s_sL[r - r_lo]);
+        p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + (e & 127)] =
+            f32_to_bf16_bits(O / s_sL[r - r_lo] * gate_factor(p, n, g * hq_g + r));
     }
     STEP5_STAMP(4, 7);
 }

@@ -83,6 +83,7 @@ struct AttnParams {
     const int32_t* sel_ids;  // [N][G][top_k]
     const int32_t* sel_count;
     uint16_t* out;           // [N][Hq][128]
+    const uint16_t* gate;    // [N][Hq] bf16 logits of the per-head sigmoid output gate, or null
     float* part;             // splits > 1: [N*G][splits][hq_g][130] block states
     uint32_t* bar;           // splits > 1: [N*G] epoch of each (row, group)'s state exchange
     uint32_t* flags;         // splits > 1: [N*G][kAttnMaxSplits] epoch + 1 once a block's state is out

@@ -448,7 +448,8 @@ step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_
 step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, const void* q_bf16,
                        const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
                        const int32_t* row_pos, const int32_t* sel_ids, const int32_t* sel_count, void* out_bf16,
-                       void* workspace, size_t workspace_bytes, step5_stream_t stream, bool launch) {
+                       void* workspace, size_t workspace_bytes, step5_stream_t stream, bool launch,
+                       const void* gate_bf16 = nullptr) {
     step5_status s = check_geometry(geom);
     if (s != STEP5_OK) return s;
     if (N <= 0 || B <= 0 || t_cap <= 0 || (t_cap % geom->region_tokens)) return STEP5_ERR_INVALID_ARGUMENT;
@@ -479,6 +480,7 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     p.sel_ids = sel_ids;
     p.sel_count = sel_count;
     p.out = static_cast<uint16_t*>(out_bf16);
+    p.gate = static_cast<const uint16_t*>(gate_bf16);
     p.status = st;
     p.N = N;
     p.B = B;
@@ -529,6 +531,16 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
                                void* out_bf16, void* workspace, size_t workspace_bytes, step5_stream_t stream) {
     return attn_impl(geom, N, B, t_cap, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count,
                      out_bf16, workspace, workspace_bytes, stream, true);
+}
+
+step5_status step5_sparse_attn_gated(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap,
+                                     const void* q_bf16, const void* k_cache_bf16, const void* v_cache_bf16,
+                                     const int32_t* row_seq, const int32_t* row_pos, const int32_t* sel_ids,
+                                     const int32_t* sel_count, const void* gate_bf16, void* out_bf16,
+                                     void* workspace, size_t workspace_bytes, step5_stream_t stream) {
+    if (gate_bf16 == nullptr) return STEP5_ERR_INVALID_ARGUMENT;
+    return attn_impl(geom, N, B, t_cap, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count,
+                     out_bf16, workspace, workspace_bytes, stream, true, gate_bf16);
 }
 
 step5_status step5_decode_step(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,

@@ -177,6 +177,22 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
                                void* out_bf16, void* workspace, size_t workspace_bytes,
                                step5_stream_t stream);
 
+/* Step (4) followed by the per-head sigmoid output gate ("Step-5-Preview on one 256 GB
+ * Mac", native-family commit: Step-5's glue keeps "the per-head sigmoid gate" among
+ * StepFun's rounding points).  As step5_sparse_attn, except that every output dim of
+ * query head h of row n is scaled by sigmoid(gate[n][h]) before the output's single
+ * bf16 rounding:  out[n][h] = bf16(sigmoid(gate[n][h]) * softmax(...) V).
+ * gate_bf16: [N][num_q_heads] bf16 logits (device, required; NULL returns
+ * STEP5_ERR_INVALID_ARGUMENT).  Everything else as step5_sparse_attn. */
+step5_status step5_sparse_attn_gated(const step5_geometry* geom, int32_t N, int32_t B,
+                                     int32_t t_cap, const void* q_bf16,
+                                     const void* k_cache_bf16, const void* v_cache_bf16,
+                                     const int32_t* row_seq, const int32_t* row_pos,
+                                     const int32_t* sel_ids, const int32_t* sel_count,
+                                     const void* gate_bf16, void* out_bf16,
+                                     void* workspace, size_t workspace_bytes,
+                                     step5_stream_t stream);
+
 /* One whole step: step5_region_summarize, then step5_index_score_topk, then
  * step5_sparse_attn, on one stream, with the same arguments and the same results as the
  * three calls (no counterpart in the pages: a composition for serving loops).  Every

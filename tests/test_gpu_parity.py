@@ -443,3 +443,41 @@ def test_picks_clustered_in_one_share(s5):
         want = torch.arange(R - 600, R - 600 + K, dtype=torch.int32)
         for g in range(4):
             assert torch.equal(ids[0, g].cpu(), want)
+
+
+@pytest.mark.parametrize("cfg", [{"positions": [30000, 4100, 70, 15], "B": 2},
+                                 {"positions": [9000] * 40, "B": 5}])
+def test_gated_attention_matches_the_oracle(s5, cfg):
+    """step5_sparse_attn_gated: the per-head sigmoid output gate on the attention output,
+    against the oracle (attention, then the gate, one rounding), with the split over
+    blocks (workspace) and with one block per (row, group); a zero logit halves the
+    ungated output bit for bit."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload(cfg, seed=59)
+    t = S.materialize(w, device="cuda")
+    g = run_path(s5, geom, w, t, path=0)
+    assert g["status"] == 0
+    dev = t["q"].device
+    sel_ids = torch.from_numpy(g["sel_ids"]).to(dev)
+    sel_count = torch.from_numpy(g["sel_count"]).to(dev)
+    gen = torch.Generator().manual_seed(61)
+    gate = (torch.randn((w.N, geom.num_q_heads), generator=gen) * 3).to(torch.bfloat16).to(dev)
+    h = host_inputs(t)
+    ref, _ = oracle.attend_batch(h["q"], h["k_cache"], h["v_cache"], w.row_seq, w.row_pos,
+                                 g["sel_ids"], g["sel_count"], geom.softmax_scale)
+    ref_gated = oracle.sigmoid_gate(ref, S.codes16(gate))
+    ws = s5.Workspace.create(geom, w.N, w.r_cap, device=dev)
+    for workspace in (ws.tensor, None):
+        out = torch.full((w.N, geom.num_q_heads, geom.head_dim), float("nan"), dtype=torch.bfloat16, device=dev)
+        s5.step5_sparse_attn_gated(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
+                                   sel_ids, sel_count, gate, out, workspace)
+        plain = torch.empty_like(out)
+        s5.step5_sparse_attn(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
+                             sel_ids, sel_count, plain, workspace)
+        half = torch.empty_like(out)
+        s5.step5_sparse_attn_gated(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
+                                   sel_ids, sel_count, torch.zeros_like(gate), half, workspace)
+        torch.cuda.synchronize()
+        assert s5.step5_device_status() == 0
+        check_out(out.float().cpu().numpy(), ref_gated, where="gated")
+        assert torch.equal(half.float() * 2, plain.float())
