@@ -161,6 +161,24 @@ def step_bytes(w, geom):
     return total + score + summ, score_call
 
 
+# --------------------------------------------------------------------------- ranks
+
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of a list of floats over all ranks (the slowest rank sets
+    the job's time); the values themselves without a process group."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    tt = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return [float(v) for v in tt.tolist()]
+
+
+def whole_job_rate(rows_per_rank, world, ms):
+    """Rows per second of the whole job: every rank's rows over the slowest rank's time."""
+    return rows_per_rank * world / (ms / 1e3)
+
+
 # --------------------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -266,11 +284,7 @@ def run_ours(args, rank, world, local_rank):
             sampler.__exit__(None, None, None)
         per_step = np.array([e[0].elapsed_time(e[1]) for e in evs])
         assert s5.step5_device_status() == 0
-        ms = float(per_step.mean())
-        if dist is not None:
-            tt = torch.tensor([ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms = float(tt.item())
+        ms = max_over_ranks([float(per_step.mean())], dist, dev)[0]
 
         # per-kernel durations: the three calls captured in one CUDA graph with timing
         # event nodes between them (the events keep the kernels from overlapping), so the
@@ -350,10 +364,7 @@ def run_ours(args, rank, world, local_rank):
             ev2[i][1].record(stream)
         barrier()
         e2e_graph_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev2]))
-        if dist is not None:
-            tt = torch.tensor([e2e_ms, e2e_graph_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms, e2e_graph_ms = float(tt[0].item()), float(tt[1].item())
+        e2e_ms, e2e_graph_ms = max_over_ranks([e2e_ms, e2e_graph_ms], dist, dev)
         res.update(e2e_ms=e2e_ms, e2e_graph_ms=e2e_graph_ms, h2d=h2d, d2h=d2h)
         del t, flush
         torch.cuda.empty_cache()
@@ -363,7 +374,7 @@ def run_ours(args, rank, world, local_rank):
     head = measure(args.workload, args.steps, args.warmup, clocks=True)
     w = head["w"]
     rows = w.N * world
-    value = rows / (head["ms"] / 1e3)
+    value = whole_job_rate(w.N, world, head["ms"])
     score_gbs = head["bytes_score"] / (head["per_score"] / 1e3) / 1e9
     step_gbs = head["bytes_step"] / (head["ms"] / 1e3) / 1e9
     line = {
@@ -401,7 +412,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_secondary:
         sec = measure(2 if args.workload == 4 else 4, max(20, args.steps // 2), args.warmup)
         sgbs = sec["bytes_step"] / (sec["ms"] / 1e3) / 1e9
-        line["secondary"] = {"workload": sec["w"].name, "value": round(sec["w"].N * world / (sec["ms"] / 1e3), 2),
+        line["secondary"] = {"workload": sec["w"].name, "value": round(whole_job_rate(sec["w"].N, world, sec["ms"]), 2),
                              "unit": UNIT, "ms_per_step": round(sec["ms"], 5),
                              "achieved_gbs": round(sgbs, 1), "frac": round(sgbs / peak, 4),
                              "select_path": "fused" if sec["path"] == 1 else "split",
