@@ -63,6 +63,10 @@ def _load():
             "orc_select_topk": (i32, [P, i64, i32, P]),
             "orc_attend_group": (None, [P, i32, i32, P, P, P, i32, i32, i32, f64, P]),
             "orc_sigmoid_gate": (None, [P, P, i64, i32]),
+            "orc_rmsnorm_1pw": (None, [P, P, i32, f64, P]),
+            "orc_layernorm": (None, [P, P, P, i32, f64, P]),
+            "orc_indexer_front": (i32, [i32, i32, i32, i32, i32, i32, i32, i64, i64, f64,
+                                        P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
             "orc_summarize_batch": (i32, [i32, i32, i64, i64, i32, i32, i32, P, P, P, P,
                                           P, P, P, P, i32]),
             "orc_score_batch": (i32, [i32, i32, i32, i32, i32, i32, i64, P, P, P, P, P,
@@ -272,6 +276,63 @@ def attend_batch(q, k_cache, v_cache, row_seq, row_pos, sel_ids, sel_count, scal
                                   _p(_c(row_pos, np.int32)), _p(ids), _p(cnt), _p(out),
                                   nthreads)
     return out, th
+
+
+def rmsnorm_1pw(x_codes, w_codes, eps) -> np.ndarray:
+    """RMSNorm with weight (1 + w) over the last axis (bf16 codes in and out)."""
+    x = _c(x_codes, np.uint16)
+    w = _c(w_codes, np.uint16)
+    dim = x.shape[-1]
+    out = np.empty_like(x)
+    flat_x, flat_o = x.reshape(-1, dim), out.reshape(-1, dim)
+    for i in range(flat_x.shape[0]):
+        row = np.ascontiguousarray(flat_x[i])
+        o = np.empty(dim, dtype=np.uint16)
+        _load().orc_rmsnorm_1pw(_p(row), _p(w), dim, float(eps), _p(o))
+        flat_o[i] = o
+    return out
+
+
+def layernorm(x_codes, g_codes, b_codes, eps) -> np.ndarray:
+    """LayerNorm with weight g and bias b over the last axis (bf16 codes in and out)."""
+    x = _c(x_codes, np.uint16)
+    g = _c(g_codes, np.uint16)
+    b = _c(b_codes, np.uint16)
+    dim = x.shape[-1]
+    out = np.empty_like(x)
+    flat_x, flat_o = x.reshape(-1, dim), out.reshape(-1, dim)
+    for i in range(flat_x.shape[0]):
+        row = np.ascontiguousarray(flat_x[i])
+        o = np.empty(dim, dtype=np.uint16)
+        _load().orc_layernorm(_p(row), _p(g), _p(b), dim, float(eps), _p(o))
+        flat_o[i] = o
+    return out
+
+
+def indexer_front(q_pre, k_pre, z_pre, qw, kw, kb, row_seq, row_pos, cos, sin, k_cache, z_cache,
+                  summaries, eps, rope_dims, region_tokens=8):
+    """The decode front end on host copies: returns (q_out, k_cache, z_cache, summaries),
+    the caches and summaries updated in new arrays."""
+    qp = _c(q_pre, np.uint16)
+    kp = _c(k_pre, np.uint16)
+    zp = _c(z_pre, np.uint16)
+    N, H, D = qp.shape
+    G = kp.shape[1]
+    kc = np.array(k_cache, dtype=np.uint16, order="C", copy=True)
+    zc = np.array(z_cache, dtype=np.uint16, order="C", copy=True)
+    sm = np.array(summaries, dtype=np.uint8, order="C", copy=True)
+    B, _, t_cap, _ = kc.shape
+    r_cap = sm.shape[2]
+    q_out = np.empty_like(qp)
+    cs = None if cos is None else _c(cos, np.uint16)
+    sn = None if sin is None else _c(sin, np.uint16)
+    rc = _load().orc_indexer_front(N, G, H, D, region_tokens, rope_dims if cs is not None else 0, B, t_cap,
+                                   r_cap, float(eps), _p(qp), _p(kp), _p(zp), _p(_c(qw, np.uint16)),
+                                   _p(_c(kw, np.uint16)), _p(_c(kb, np.uint16)), _p(_c(row_seq, np.int32)),
+                                   _p(_c(row_pos, np.int32)), _p(cs) if cs is not None else None,
+                                   _p(sn) if sn is not None else None, _p(q_out), _p(kc), _p(zc), _p(sm))
+    assert rc == 0, "row out of range"
+    return q_out, kc, zc, sm
 
 
 def sigmoid_gate(out, gate_codes) -> np.ndarray:

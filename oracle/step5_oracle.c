@@ -124,6 +124,38 @@ void orc_rotate_neox(const uint16_t* x, int dim, int rope_dims,
 }
 
 /* ------------------------------------------------------------------------------ */
+/* Before step 1: the indexer's q and k norms.                                      */
+/* ------------------------------------------------------------------------------ */
+
+void orc_rmsnorm_1pw(const uint16_t* x, const uint16_t* w, int dim, double eps, uint16_t* out) {
+    double ss = 0.0;
+    for (int d = 0; d < dim; ++d) {
+        double v = orc_bf16_value(x[d]);
+        ss += v * v;
+    }
+    double rms = sqrt(ss / dim + eps);
+    for (int d = 0; d < dim; ++d)
+        out[d] = orc_bf16_code(orc_round_bf16(orc_bf16_value(x[d]) / rms * (1.0 + orc_bf16_value(w[d]))));
+}
+
+void orc_layernorm(const uint16_t* x, const uint16_t* g, const uint16_t* b, int dim, double eps,
+                   uint16_t* out) {
+    double mean = 0.0;
+    for (int d = 0; d < dim; ++d) mean += orc_bf16_value(x[d]);
+    mean /= dim;
+    double var = 0.0;
+    for (int d = 0; d < dim; ++d) {
+        double c = orc_bf16_value(x[d]) - mean;
+        var += c * c;
+    }
+    var /= dim;
+    double sd = sqrt(var + eps);
+    for (int d = 0; d < dim; ++d)
+        out[d] = orc_bf16_code(orc_round_bf16((orc_bf16_value(x[d]) - mean) / sd * orc_bf16_value(g[d]) +
+                                              orc_bf16_value(b[d])));
+}
+
+/* ------------------------------------------------------------------------------ */
 /* Step 1: summary of one completed region.                                         */
 /* ------------------------------------------------------------------------------ */
 
@@ -461,4 +493,43 @@ int orc_attend_batch(int N, int G, int num_q_heads, int head_dim, int region_tok
     att_ctx c = {G, num_q_heads, head_dim, region_tokens, K, t_cap, scale,
                  q, kc, vc, row_seq, row_pos, sel_ids, sel_count, out};
     return parallel_for((int64_t)N * G, nthreads, att_item, &c);
+}
+
+/* ------------------------------------------------------------------------------ */
+/* The decode front end (rows in order).                                            */
+/* ------------------------------------------------------------------------------ */
+
+int orc_indexer_front(int N, int G, int idx_heads, int dim, int region_tokens, int rope_dims,
+                      int B, int64_t t_cap, int64_t r_cap, double eps,
+                      const uint16_t* q_pre, const uint16_t* k_pre, const uint16_t* z_pre,
+                      const uint16_t* qw, const uint16_t* kw, const uint16_t* kb,
+                      const int32_t* row_seq, const int32_t* row_pos,
+                      const uint16_t* cos_tab, const uint16_t* sin_tab,
+                      uint16_t* q_out, uint16_t* k_cache, uint16_t* z_cache, uint8_t* summ) {
+    int bad = 0;
+    for (int n = 0; n < N; ++n) {
+        for (int h = 0; h < idx_heads; ++h)
+            orc_rmsnorm_1pw(q_pre + ((int64_t)n * idx_heads + h) * dim, qw, dim, eps,
+                            q_out + ((int64_t)n * idx_heads + h) * dim);
+        int b = row_seq[n], p = row_pos[n];
+        if (b < 0 || b >= B || p < 0 || p >= t_cap) {
+            bad = -1;
+            continue;
+        }
+        for (int g = 0; g < G; ++g) {
+            int64_t row = (((int64_t)b * G + g) * t_cap + p) * dim;
+            orc_layernorm(k_pre + ((int64_t)n * G + g) * dim, kw, kb, dim, eps, k_cache + row);
+            memcpy(z_cache + row, z_pre + ((int64_t)n * G + g) * dim, sizeof(uint16_t) * (size_t)dim);
+        }
+        if (p % region_tokens == region_tokens - 1 && p / region_tokens < r_cap) {
+            int r = p / region_tokens;
+            for (int g = 0; g < G; ++g) {
+                int64_t t0 = ((int64_t)b * G + g) * t_cap + (int64_t)r * region_tokens;
+                orc_summarize_region(k_cache + t0 * dim, z_cache + t0 * dim, region_tokens, dim,
+                                     r * region_tokens, rope_dims, cos_tab, sin_tab, NULL,
+                                     summ + (((int64_t)b * G + g) * r_cap + r) * dim);
+            }
+        }
+    }
+    return bad;
 }

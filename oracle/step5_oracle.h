@@ -47,6 +47,16 @@ void     orc_round_bf16_array(const double* in, uint16_t* out_codes, int64_t n);
 void orc_rotate_neox(const uint16_t* x, int dim, int rope_dims,
                      const uint16_t* cos_row, const uint16_t* sin_row, double* out);
 
+/* ---- before step 1: the indexer's q and k norms (decode front end) ------------------
+ * ("Step-5-Preview on one 256 GB Mac", CSA-indexer commit: "the indexer's q (16 heads,
+ * RMSNorm 1 + w), k (LayerNorm with bias) and z".)  x, w, g, b: dim bf16 codes; fp64
+ * arithmetic, one bf16 rounding of each output.
+ *   RMSNorm 1 + w:  y[d] = x[d] / sqrt(mean_d x^2 + eps) * (1 + w[d])
+ *   LayerNorm:      y[d] = (x[d] - mean) / sqrt(mean_d (x - mean)^2 + eps) * g[d] + b[d] */
+void orc_rmsnorm_1pw(const uint16_t* x, const uint16_t* w, int dim, double eps, uint16_t* out);
+void orc_layernorm(const uint16_t* x, const uint16_t* g, const uint16_t* b, int dim, double eps,
+                   uint16_t* out);
+
 /* ---- step 1: region summary -------------------------------------------------------
  * k, z: region_tokens rows of dim bf16 codes (row stride dim).  Token j sits at
  * position t0 + j; its rotation row is cos_tab[(t0 + j) * (rope_dims/2)].
@@ -127,6 +137,21 @@ int orc_attend_batch(int N, int G, int num_q_heads, int head_dim, int region_tok
                      const int32_t* row_seq, const int32_t* row_pos,
                      const int32_t* sel_ids, const int32_t* sel_count,
                      double* out, int nthreads);
+
+/* The decode front end, rows in order n = 0 .. N-1: the row's indexer q, head by head,
+ * through RMSNorm 1 + w into q_out [N][idx_heads][dim]; its k through LayerNorm and its
+ * z as they are, written at token row_pos[n] of the caches [B][G][t_cap][dim] of
+ * sequence row_seq[n]; when that token completes its region (row_pos % region_tokens
+ * == region_tokens - 1), the region's summary codes into summ [B][G][r_cap][dim] (as
+ * orc_summarize_region).  q_pre [N][idx_heads][dim], k_pre / z_pre [N][G][dim];
+ * qw [dim], kw [dim], kb [dim] bf16 codes.  Returns 0, or -1 for a row out of range. */
+int orc_indexer_front(int N, int G, int idx_heads, int dim, int region_tokens, int rope_dims,
+                      int B, int64_t t_cap, int64_t r_cap, double eps,
+                      const uint16_t* q_pre, const uint16_t* k_pre, const uint16_t* z_pre,
+                      const uint16_t* qw, const uint16_t* kw, const uint16_t* kb,
+                      const int32_t* row_seq, const int32_t* row_pos,
+                      const uint16_t* cos_tab, const uint16_t* sin_tab,
+                      uint16_t* q_out, uint16_t* k_cache, uint16_t* z_cache, uint8_t* summ);
 
 #ifdef __cplusplus
 }
