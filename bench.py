@@ -241,6 +241,20 @@ def run_ours(args, rank, world, local_rank):
             s5.step5_sparse_attn_gated(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
                                        sel_ids, sel_count, gate, out, ws.tensor)
 
+        # the indexer's decode front end (q/k norms, the row token's k/z write, a completed
+        # region's summary), timed beside the step only: it writes token p of the caches
+        # and, at p % 8 == 7, the summary of the row's own region, neither of which the
+        # step reads
+        fg = torch.Generator().manual_seed(71)
+        front_in = [(torch.randn(shape, generator=fg) * sc + sh).to(torch.bfloat16).to(dev) for shape, sc, sh in
+                    (((N, geom.idx_heads, 64), 2.0, 0.0), ((N, G, 64), 1.5, 0.3), ((N, G, 64), 1.0, 0.0),
+                     ((64,), 0.1, 0.0), ((64,), 0.1, 1.0), ((64,), 0.1, 0.0))]
+        q_front = torch.empty_like(front_in[0])
+
+        def call_front():
+            s5.step5_indexer_front(geom, *front_in, 1e-6, t["row_seq"], t["row_pos"], t["cos"], t["sin"], q_front,
+                                   t["idx_k"], t["idx_z"], t["summaries"])
+
         def step():
             # the whole step in one C-ABI call (summaries, score + select, attention)
             s5.step5_decode_step(geom, t, ws, sel_ids, sel_count, out, max_regions_per_seq=span)
@@ -291,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
         # events bracket the kernels alone; without event nodes in graphs, eager calls
         # behind a 1 GiB write that covers their launch
         steps_b = steps
-        calls_b = (call_sum, call_score, call_attn, call_attn_gated)
+        calls_b = (call_sum, call_score, call_attn, call_attn_gated, call_front)
         times_b = np.zeros((steps_b, len(calls_b)))
         try:
             evg = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls_b) + 1)]
@@ -323,11 +337,12 @@ def run_ours(args, rank, world, local_rank):
             times_b = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(calls_b))] for e in evb])
             del hold
         per_sum, per_score, per_attn, per_gated = times_b[:, 0], times_b[:, 1], times_b[:, 2], times_b[:, 3]
+        per_front = times_b[:, 4]
         bytes_step, bytes_score = step_bytes(w, geom)
         res = dict(w=w, ms=ms, ms_min=float(per_step.min()), per_score=float(per_score.mean()),
                    breakdown_how=breakdown_how,
                    per_attn=float(per_attn.mean()), per_sum=float(per_sum.mean()),
-                   per_gated=float(per_gated.mean()), bytes_step=bytes_step,
+                   per_gated=float(per_gated.mean()), per_front=float(per_front.mean()), bytes_step=bytes_step,
                    bytes_score=bytes_score, launches=launches_per_step * steps, path=path, wall=wall,
                    clocks=sampler.summary() if sampler else None)
 
@@ -394,6 +409,7 @@ def run_ours(args, rank, world, local_rank):
                          "score_select": round(head["per_score"] * 1e3, 2),
                          "attention": round(head["per_attn"] * 1e3, 2),
                          "attention_gated": round(head["per_gated"] * 1e3, 2),
+                         "indexer_front": round(head["per_front"] * 1e3, 2),
                          "how": head["breakdown_how"]},
         "roofline": {"kernel": "score_select_kernel (step5_index_score_topk, split path)",
                      "bound": "hbm", "achieved": round(score_gbs, 1), "peak": peak, "unit": "GB/s",
@@ -419,7 +435,8 @@ def run_ours(args, rank, world, local_rank):
                              "breakdown_us": {"summarize": round(sec["per_sum"] * 1e3, 2),
                                               "score_select": round(sec["per_score"] * 1e3, 2),
                                               "attention": round(sec["per_attn"] * 1e3, 2),
-                                              "attention_gated": round(sec["per_gated"] * 1e3, 2)}}
+                                              "attention_gated": round(sec["per_gated"] * 1e3, 2),
+                                              "indexer_front": round(sec["per_front"] * 1e3, 2)}}
         line["gpu_launches"] += sec["launches"]
     if rank == 0 and not args.no_cpu_baseline:
         cb = oracle_sample(args.workload, quarter=False)

@@ -11,6 +11,7 @@ Steps (TensorFold PR #903, "Step-5-Preview on one 256 GB Mac", CSA-indexer commi
   step5_index_score_topk  -- sum_h relu(e4m3(q_h) . summary) * w_h, top-k by (-score, id)
   step5_sparse_attn       -- attention over the picked regions plus the row's own region
   step5_sparse_attn_gated -- the same, followed by the per-head sigmoid output gate
+  step5_indexer_front     -- decode front end: q/k norms, k/z cache write, summary on completion
 """
 from __future__ import annotations
 
@@ -27,6 +28,7 @@ from ._build import LIB, build  # noqa: F401
 __all__ = [
     "Step5Error", "Geometry", "STEP5_GEOMETRY", "library_path", "load",
     "step5_region_summarize", "step5_index_score_topk", "step5_sparse_attn", "step5_sparse_attn_gated",
+    "step5_indexer_front",
     "step5_index_score_topk_noalloc",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
     "step5_set_select_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
@@ -92,6 +94,8 @@ def load():
                                          P, sz, P]),
         "step5_sparse_attn": (i32, [G, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]),
         "step5_sparse_attn_gated": (i32, [G, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, sz, P]),
+        "step5_indexer_front": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, ctypes.c_float, P, P, P, P,
+                                      P, P, P, P, P]),
         "step5_decode_step": (i32, [G, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
                                     P, P, P, P, sz, P]),
         "step5_index_score_topk_noalloc": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P,
@@ -215,6 +219,20 @@ def step5_index_score_topk_noalloc(geom, idx_q, w, row_seq, row_pos, cos, sin, s
         ctypes.byref(Geometry.of(geom)), N, B, int(t_cap), r_cap, _ptr(idx_q), _ptr(w),
         _ptr(row_seq), _ptr(row_pos), _ptr(cos), _ptr(sin), _ptr(summaries), _ptr(sel_ids),
         _ptr(sel_count), _ptr(scores), _ptr(sel_scores), _stream(stream)))
+
+
+def step5_indexer_front(geom, q_pre, k_pre, z_pre, q_norm_w, k_norm_w, k_norm_b, eps, row_seq, row_pos,
+                        cos, sin, idx_q_out, idx_k, idx_z, summaries, stream=None):
+    """The indexer's decode front end: q RMSNorm (1 + w) into idx_q_out, k LayerNorm and z
+    written at each row's position of the caches, and the summary of a region the row's
+    token completes (see the header)."""
+    N = q_pre.shape[0]
+    B, _, t_cap, _ = idx_k.shape
+    r_cap = summaries.shape[2]
+    _check("step5_indexer_front", load().step5_indexer_front(
+        ctypes.byref(Geometry.of(geom)), N, B, t_cap, r_cap, _ptr(q_pre), _ptr(k_pre), _ptr(z_pre),
+        _ptr(q_norm_w), _ptr(k_norm_w), _ptr(k_norm_b), float(eps), _ptr(row_seq), _ptr(row_pos),
+        _ptr(cos), _ptr(sin), _ptr(idx_q_out), _ptr(idx_k), _ptr(idx_z), _ptr(summaries), _stream(stream)))
 
 
 def step5_sparse_attn_gated(geom, q, k_cache, v_cache, row_seq, row_pos, sel_ids, sel_count, gate,

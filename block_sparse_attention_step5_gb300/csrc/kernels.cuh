@@ -22,6 +22,76 @@ struct SummarizeParams {
     int G, t_cap, r_cap, max_span, rope_dims;
 };
 cudaError_t launch_summarize(const SummarizeParams& p, int B, cudaStream_t stream);
+
+// Summary value of dim d of the region whose first cache row is row0 (element offset of
+// token 0, dim 0 in [B][G][t_cap][64]) and whose first token is position t0: the
+// per-dim softmax over z of the NEOX-rotated k, in fp32 with tokens in order (not yet
+// rounded).  CG: read through L2 (data written earlier in the same launch).
+template <bool CG>
+__device__ __forceinline__ float region_summary_dim(const uint16_t* idx_k, const uint16_t* idx_z,
+                                                    const uint16_t* cos, const uint16_t* sin, int rope_dims,
+                                                    int64_t row0, int t0, int d) {
+    auto ld = [](const uint16_t* a) -> uint16_t { return CG ? __ldcg(a) : __ldg(a); };
+    const int half = rope_dims >> 1;
+    const bool rotated = cos != nullptr && d < rope_dims;
+    const bool first = d < half;
+    const int pd = first ? d + half : d - half;  // NEOX partner dim
+    const int pi = first ? d : d - half;         // NEOX pair index
+    // every load of the region is issued before any arithmetic
+    uint16_t zv[8], kv[8], pv[8], cv[8], sv[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        zv[t] = ld(idx_z + row0 + t * 64 + d);
+        kv[t] = ld(idx_k + row0 + t * 64 + d);
+    }
+    if (rotated) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int64_t tab = (int64_t)(t0 + t) * half + pi;
+            pv[t] = ld(idx_k + row0 + t * 64 + pd);
+            cv[t] = ld(cos + tab);
+            sv[t] = ld(sin + tab);
+        }
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) m = fmaxf(m, bf16_to_f32(zv[t]));
+    // weights and weighted sum (fp32, tokens in order)
+    float den = 0.0f, num = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        float kr = bf16_to_f32(kv[t]);
+        if (rotated)
+            kr = bf16_to_f32(neox_rotate(kr, bf16_to_f32(pv[t]), bf16_to_f32(cv[t]), bf16_to_f32(sv[t]), first));
+        const float e = expf(bf16_to_f32(zv[t]) - m);
+        den += e;
+        num = fmaf(e, kr, num);
+    }
+    return num / den;
+}
+
+// Decode front end: the indexer's q RMSNorm (1 + w), k LayerNorm with bias, the k/z
+// cache write of the row's token and, when it completes its region, that summary.
+struct FrontParams {
+    const uint16_t* q_pre;   // [N][idx_heads][64]
+    const uint16_t* k_pre;   // [N][G][64]
+    const uint16_t* z_pre;   // [N][G][64]
+    const uint16_t* q_w;     // [64]
+    const uint16_t* k_w;     // [64]
+    const uint16_t* k_b;     // [64]
+    const int32_t* row_seq;
+    const int32_t* row_pos;
+    const uint16_t* cos;     // [t_cap][rope_dims/2] or null
+    const uint16_t* sin;
+    uint16_t* q_out;         // [N][idx_heads][64]
+    uint16_t* idx_k;         // [B][G][t_cap][64]
+    uint16_t* idx_z;
+    uint8_t* summ;           // [B][G][r_cap][64]
+    uint32_t* status;
+    int N, B, G, idx_heads, t_cap, r_cap, rope_dims;
+    float eps;
+};
+cudaError_t launch_front(const FrontParams& p, cudaStream_t stream);
 cudaError_t launch_convert(const uint16_t* in, uint8_t* out, int64_t n, cudaStream_t stream);
 
 // ----------------------------------------------------------------- steps (2) + (3)

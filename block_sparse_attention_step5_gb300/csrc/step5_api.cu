@@ -543,6 +543,54 @@ step5_status step5_sparse_attn_gated(const step5_geometry* geom, int32_t N, int3
                      out_bf16, workspace, workspace_bytes, stream, true, gate_bf16);
 }
 
+step5_status step5_indexer_front(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
+                                 const void* q_pre_bf16, const void* k_pre_bf16, const void* z_pre_bf16,
+                                 const void* q_norm_w_bf16, const void* k_norm_w_bf16, const void* k_norm_b_bf16,
+                                 float eps, const int32_t* row_seq, const int32_t* row_pos,
+                                 const void* rope_cos_bf16, const void* rope_sin_bf16, void* idx_q_out_bf16,
+                                 void* idx_k_bf16, void* idx_z_bf16, uint8_t* summaries_e4m3,
+                                 step5_stream_t stream) {
+    step5_status s = check_geometry(geom);
+    if (s != STEP5_OK) return s;
+    if (geom->num_kv_groups > 4) return STEP5_ERR_UNSUPPORTED;  // one thread per (group, dim)
+    if (N <= 0 || B <= 0 || t_cap <= 0 || r_cap <= 0 || (t_cap % geom->region_tokens)) return STEP5_ERR_INVALID_ARGUMENT;
+    if (!(eps >= 0.0f) || eps > 1.0f) return STEP5_ERR_INVALID_ARGUMENT;
+    if (!q_pre_bf16 || !k_pre_bf16 || !z_pre_bf16 || !q_norm_w_bf16 || !k_norm_w_bf16 || !k_norm_b_bf16 ||
+        !row_seq || !row_pos || !idx_q_out_bf16 || !idx_k_bf16 || !idx_z_bf16 || !summaries_e4m3)
+        return STEP5_ERR_INVALID_ARGUMENT;
+    if ((rope_cos_bf16 == nullptr) != (rope_sin_bf16 == nullptr)) return STEP5_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q_pre_bf16) || !aligned16(idx_q_out_bf16) || !aligned16(idx_k_bf16) || !aligned16(idx_z_bf16))
+        return STEP5_ERR_INVALID_ARGUMENT;
+    if ((int64_t)B * geom->num_kv_groups * t_cap > INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
+    uint32_t* st = status_ptr();
+    if (!st) return STEP5_ERR_CUDA;
+    FrontParams p;
+    p.q_pre = static_cast<const uint16_t*>(q_pre_bf16);
+    p.k_pre = static_cast<const uint16_t*>(k_pre_bf16);
+    p.z_pre = static_cast<const uint16_t*>(z_pre_bf16);
+    p.q_w = static_cast<const uint16_t*>(q_norm_w_bf16);
+    p.k_w = static_cast<const uint16_t*>(k_norm_w_bf16);
+    p.k_b = static_cast<const uint16_t*>(k_norm_b_bf16);
+    p.row_seq = row_seq;
+    p.row_pos = row_pos;
+    p.cos = static_cast<const uint16_t*>(rope_cos_bf16);
+    p.sin = static_cast<const uint16_t*>(rope_sin_bf16);
+    p.q_out = static_cast<uint16_t*>(idx_q_out_bf16);
+    p.idx_k = static_cast<uint16_t*>(idx_k_bf16);
+    p.idx_z = static_cast<uint16_t*>(idx_z_bf16);
+    p.summ = summaries_e4m3;
+    p.status = st;
+    p.N = N;
+    p.B = B;
+    p.G = geom->num_kv_groups;
+    p.idx_heads = geom->idx_heads;
+    p.t_cap = t_cap;
+    p.r_cap = r_cap;
+    p.rope_dims = rope_cos_bf16 ? geom->rope_dims : 0;
+    p.eps = eps;
+    return launch_front(p, (cudaStream_t)stream) == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
+}
+
 step5_status step5_decode_step(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
                                int32_t max_regions_per_seq, const void* idx_k_bf16, const void* idx_z_bf16,
                                const void* rope_cos_bf16, const void* rope_sin_bf16, const int32_t* region_begin,

@@ -38,44 +38,8 @@ __global__ void __maxnreg__(48) summarize_kernel(SummarizeParams p) {
     }
     if (r >= re || r < 0 || r >= p.r_cap || (int64_t)(r + 1) * 8 > p.t_cap) return;
 
-    const int half = p.rope_dims >> 1;
-    const bool rotated = p.cos != nullptr && d < p.rope_dims;
-    const bool first = d < half;
-    const int pd = first ? d + half : d - half;   // NEOX partner dim
-    const int pi = first ? d : d - half;          // NEOX pair index
-
     const int64_t row0 = (((int64_t)b * p.G + g) * p.t_cap + (int64_t)r * 8) * 64;
-    // every load of the region is issued before any arithmetic
-    uint16_t zv[8], kv[8], pv[8], cv[8], sv[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        zv[t] = __ldg(p.idx_z + row0 + t * 64 + d);
-        kv[t] = __ldg(p.idx_k + row0 + t * 64 + d);
-    }
-    if (rotated) {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const int64_t tab = (int64_t)(r * 8 + t) * half + pi;
-            pv[t] = __ldg(p.idx_k + row0 + t * 64 + pd);
-            cv[t] = __ldg(p.cos + tab);
-            sv[t] = __ldg(p.sin + tab);
-        }
-    }
-    float m = -INFINITY;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) m = fmaxf(m, bf16_to_f32(zv[t]));
-    // weights and weighted sum (fp32, tokens in order)
-    float den = 0.0f, num = 0.0f;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        float kr = bf16_to_f32(kv[t]);
-        if (rotated)
-            kr = bf16_to_f32(neox_rotate(kr, bf16_to_f32(pv[t]), bf16_to_f32(cv[t]), bf16_to_f32(sv[t]), first));
-        const float e = expf(bf16_to_f32(zv[t]) - m);
-        den += e;
-        num = fmaf(e, kr, num);
-    }
-    const float sum = num / den;
+    const float sum = region_summary_dim<false>(p.idx_k, p.idx_z, p.cos, p.sin, p.rope_dims, row0, r * 8, d);
     const int64_t srow = ((int64_t)b * p.G + g) * p.r_cap + r;
     p.summ[srow * 64 + d] = f32_to_e4m3(bf16_to_f32(f32_to_bf16_bits(sum)));  // through bf16
     if (p.summ_f32) p.summ_f32[srow * 64 + d] = sum;

@@ -71,6 +71,31 @@ typedef struct {
     float softmax_scale;    /* attention logit scale                                  */
 } step5_geometry;
 
+/* The indexer's decode front end, ahead of step (1) ("Step-5-Preview on one 256 GB Mac",
+ * CSA-indexer commit: "the indexer's q (16 heads, RMSNorm 1 + w), k (LayerNorm with
+ * bias) and z").  For every row n (a device [N] of sequences and positions):
+ *   idx_q_out[n][h] = bf16(q_pre[n][h] / sqrt(mean_d q_pre[n][h][d]^2 + eps) * (1 + q_norm_w))
+ *   idx_k[b][g][p]  = bf16((k_pre[n][g] - mean) / sqrt(var + eps) * k_norm_w + k_norm_b)
+ *   idx_z[b][g][p]  = z_pre[n][g]
+ * (fp32 arithmetic, one rounding; b = row_seq[n], p = row_pos[n]; the rotation of q and
+ * k is left to steps (2) and (1)), and when p % 8 == 7 the summaries of region p / 8,
+ * exactly as step5_region_summarize would write them.
+ * q_pre [N][idx_heads][idx_dim], k_pre / z_pre [N][G][idx_dim], norm weights and bias
+ * [idx_dim] (bf16, device); caches [B][G][t_cap][idx_dim], summaries
+ * [B][G][r_cap][idx_dim]; rope tables as step5_region_summarize (both NULL: the
+ * cache holds rotated k).  Up to 4 KV groups.  A row whose region completes reads
+ * that region's other 7 tokens from the caches: rows of one call must not write into
+ * one another's completing regions (decode: one row per sequence).  Out-of-range rows
+ * set STEP5_DEV_RANGE and write nothing but their normalised q. */
+step5_status step5_indexer_front(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap,
+                                 int32_t r_cap, const void* q_pre_bf16, const void* k_pre_bf16,
+                                 const void* z_pre_bf16, const void* q_norm_w_bf16,
+                                 const void* k_norm_w_bf16, const void* k_norm_b_bf16, float eps,
+                                 const int32_t* row_seq, const int32_t* row_pos,
+                                 const void* rope_cos_bf16, const void* rope_sin_bf16,
+                                 void* idx_q_out_bf16, void* idx_k_bf16, void* idx_z_bf16,
+                                 uint8_t* summaries_e4m3, step5_stream_t stream);
+
 /* Step (1): region summaries.
  * For every sequence b < B, KV group g and region r in [region_begin[b], region_end[b]):
  *   kr[t][d] = bf16(NEOX-rotated idx_k at position 8r+t) for d < rope_dims, else idx_k;

@@ -481,3 +481,63 @@ def test_gated_attention_matches_the_oracle(s5, cfg):
         assert s5.step5_device_status() == 0
         check_out(out.float().cpu().numpy(), ref_gated, where="gated")
         assert torch.equal(half.float() * 2, plain.float())
+
+
+def _bf16_ulps(a_codes, b_codes):
+    """|a - b| in bf16 units of the last place (codes of finite values)."""
+    a = a_codes.astype(np.int32)
+    b = b_codes.astype(np.int32)
+    a = np.where(a & 0x8000, 0x8000 - a, a)  # sign-magnitude to a monotone integer line
+    b = np.where(b & 0x8000, 0x8000 - b, b)
+    return np.abs(a - b)
+
+
+@pytest.mark.parametrize("rope", [True, False])
+def test_indexer_front_end(s5, rope):
+    """step5_indexer_front against the oracle: normalised q and k within one bf16 step
+    (fp32 against fp64 sums) and equal almost everywhere, z and every untouched cache
+    row bit for bit, and the summaries of the regions that rows complete equal to
+    step5_region_summarize over the same caches."""
+    geom = s5.STEP5_GEOMETRY
+    G, H, D, B, t_cap, r_cap = 4, geom.idx_heads, 64, 3, 256, 32
+    gen = torch.Generator().manual_seed(67)
+    dev = torch.device("cuda")
+    bf = lambda *shape, scale=1.0, shift=0.0: (torch.randn(shape, generator=gen) * scale + shift).to(torch.bfloat16)
+    q_pre, k_pre, z_pre = bf(3, H, D, scale=2.0), bf(3, G, D, scale=1.5, shift=0.3), bf(3, G, D)
+    qw, kw, kb = bf(D, scale=0.1), bf(D, scale=0.1, shift=1.0), bf(D, scale=0.1)
+    k_cache, z_cache = bf(B, G, t_cap, D), bf(B, G, t_cap, D)
+    summ = torch.zeros((B, G, r_cap, D), dtype=torch.uint8)
+    ang = np.outer(np.arange(t_cap), 10000.0 ** (-np.arange(16) * 2 / 32))
+    cos = torch.from_numpy(np.cos(ang)).to(torch.bfloat16) if rope else None
+    sin = torch.from_numpy(np.sin(ang)).to(torch.bfloat16) if rope else None
+    seqs = torch.tensor([2, 0, 1], dtype=torch.int32)
+    pos = torch.tensor([15, 100, 255], dtype=torch.int32)  # rows 0 and 2 complete regions 1 and 31
+    eps = 1e-6
+    ref_q, ref_k, ref_z, ref_s = oracle.indexer_front(S.codes16(q_pre), S.codes16(k_pre), S.codes16(z_pre),
+                                                      S.codes16(qw), S.codes16(kw), S.codes16(kb), seqs.numpy(),
+                                                      pos.numpy(), None if cos is None else S.codes16(cos),
+                                                      None if sin is None else S.codes16(sin), S.codes16(k_cache),
+                                                      S.codes16(z_cache), summ.numpy(), eps=eps, rope_dims=32)
+    d = {k: v.to(dev) for k, v in dict(q_pre=q_pre, k_pre=k_pre, z_pre=z_pre, qw=qw, kw=kw, kb=kb, kc=k_cache,
+                                       zc=z_cache, summ=summ, seqs=seqs, pos=pos).items()}
+    dcos = cos.to(dev) if rope else None
+    dsin = sin.to(dev) if rope else None
+    q_out = torch.empty_like(d["q_pre"])
+    s5.step5_indexer_front(geom, d["q_pre"], d["k_pre"], d["z_pre"], d["qw"], d["kw"], d["kb"], eps, d["seqs"],
+                           d["pos"], dcos, dsin, q_out, d["kc"], d["zc"], d["summ"])
+    torch.cuda.synchronize()
+    assert s5.step5_device_status() == 0
+    gq, gk, gz, gs = S.codes16(q_out), S.codes16(d["kc"]), S.codes16(d["zc"]), d["summ"].cpu().numpy()
+    for got, ref in ((gq, ref_q), (gk, ref_k)):
+        ulps = _bf16_ulps(got, ref)
+        assert ulps.max() <= 1 and (ulps > 0).mean() < 0.01
+    assert np.array_equal(gz, ref_z)
+    # the completed regions' summaries: the summary kernel over the same (GPU) caches
+    chk = torch.zeros_like(d["summ"])
+    rb = torch.tensor([0, 0, 0], dtype=torch.int32, device=dev)
+    re = torch.tensor([0, 0, 0], dtype=torch.int32, device=dev)
+    rb[2], re[2], rb[1], re[1] = 1, 2, 31, 32
+    s5.step5_region_summarize(geom, d["kc"], d["zc"], dcos, dsin, rb, re, chk, max_regions_per_seq=1)
+    torch.cuda.synchronize()
+    assert np.array_equal(gs, chk.cpu().numpy())
+    assert gs[2, :, 1].any() and gs[1, :, 31].any() and not gs[0].any()
