@@ -63,6 +63,9 @@ def _load():
             "orc_select_topk": (i32, [P, i64, i32, P]),
             "orc_attend_group": (None, [P, i32, i32, P, P, P, i32, i32, i32, f64, P]),
             "orc_sigmoid_gate": (None, [P, P, i64, i32]),
+            "orc_merge_topk": (i32, [i32, i32, i32, P, P, P, P]),
+            "orc_attend_partial": (None, [P, i32, i32, P, P, P, i32, i32, i32, i64, i64, f64, P, P, P]),
+            "orc_attn_combine": (None, [i32, i32, P, P, P, P]),
             "orc_rmsnorm_1pw": (None, [P, P, i32, f64, P]),
             "orc_layernorm": (None, [P, P, P, i32, f64, P]),
             "orc_indexer_front": (i32, [i32, i32, i32, i32, i32, i32, i32, i64, i64, f64,
@@ -333,6 +336,42 @@ def indexer_front(q_pre, k_pre, z_pre, qw, kw, kb, row_seq, row_pos, cos, sin, k
                                    _p(sn) if sn is not None else None, _p(q_out), _p(kc), _p(zc), _p(sm))
     assert rc == 0, "row out of range"
     return q_out, kc, zc, sm
+
+
+def merge_topk(ids, scores, counts, K):
+    """The K smallest keys (-score, id) of the union of S shards' picks: ids / scores
+    [S][K], counts [S].  Returns the merged ids in key order."""
+    i = _c(ids, np.int32)
+    sc = _c(scores, np.float64)
+    c = _c(counts, np.int32)
+    out = np.full(K, -1, dtype=np.int32)
+    n = _load().orc_merge_topk(i.shape[0], i.shape[1], K, _p(i), _p(sc), _p(c), _p(out))
+    return out[:n]
+
+
+def attend_partial(q_codes, k_cache, v_cache, sel, pos, tok_lo, tok_hi, scale, region_tokens=8):
+    """(m [hq], l [hq], o [hq][D]) of one (row, group) over the keys in [tok_lo, tok_hi)."""
+    q = _c(q_codes, np.uint16)
+    kc = _c(k_cache, np.uint16)
+    vc = _c(v_cache, np.uint16)
+    sel = _c(sel, np.int32)
+    hq, D = q.shape
+    m = np.empty(hq)
+    l = np.empty(hq)
+    o = np.empty((hq, D))
+    _load().orc_attend_partial(_p(q), hq, D, _p(kc), _p(vc), _p(sel), sel.size, int(pos), region_tokens,
+                               int(tok_lo), int(tok_hi), float(scale), _p(m), _p(l), _p(o))
+    return m, l, o
+
+
+def attn_combine(m, l, o) -> np.ndarray:
+    """Combine S partial states of one head: m, l [S], o [S][D] -> out [D]."""
+    mm = _c(m, np.float64)
+    ll = _c(l, np.float64)
+    oo = _c(o, np.float64)
+    out = np.empty(oo.shape[1])
+    _load().orc_attn_combine(mm.size, oo.shape[1], _p(mm), _p(ll), _p(oo), _p(out))
+    return out
 
 
 def sigmoid_gate(out, gate_codes) -> np.ndarray:

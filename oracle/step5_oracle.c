@@ -296,6 +296,89 @@ void orc_attend_group(const uint16_t* q, int hq_g, int head_dim,
 }
 
 /* ------------------------------------------------------------------------------ */
+/* Sequence-sharded decode: merge of the shards' picks, partial attention, combine.  */
+/* ------------------------------------------------------------------------------ */
+
+int orc_merge_topk(int S, int L, int K, const int32_t* ids, const double* scores, const int32_t* counts,
+                   int32_t* ids_out) {
+    int64_t total = 0;
+    for (int s = 0; s < S; ++s) total += counts[s];
+    orc_key* keys = (orc_key*)malloc(sizeof(orc_key) * (size_t)(total > 0 ? total : 1));
+    int64_t n = 0;
+    for (int s = 0; s < S; ++s)
+        for (int i = 0; i < counts[s]; ++i) {
+            double sc = scores[(int64_t)s * L + i];
+            keys[n].neg_score = (sc == 0.0) ? 0.0 : -sc;
+            keys[n].id = ids[(int64_t)s * L + i];
+            ++n;
+        }
+    qsort(keys, (size_t)n, sizeof(orc_key), key_cmp);
+    int take = n < K ? (int)n : K;
+    for (int i = 0; i < take; ++i) ids_out[i] = (int32_t)keys[i].id;
+    for (int i = take; i < K; ++i) ids_out[i] = -1;
+    free(keys);
+    return take;
+}
+
+void orc_attend_partial(const uint16_t* q, int hq_g, int head_dim, const uint16_t* kc, const uint16_t* vc,
+                        const int32_t* sel, int cnt, int pos, int region_tokens, int64_t tok_lo,
+                        int64_t tok_hi, double scale, double* m, double* l, double* o) {
+    int own = pos / region_tokens;
+    int own_len = pos - own * region_tokens + 1;
+    int64_t* tok = (int64_t*)malloc(sizeof(int64_t) * ((size_t)cnt * region_tokens + own_len + 1));
+    int64_t n = 0;
+    for (int i = 0; i < cnt; ++i)
+        for (int j = 0; j < region_tokens; ++j) {
+            int64_t t = (int64_t)sel[i] * region_tokens + j;
+            if (t >= tok_lo && t < tok_hi) tok[n++] = t;
+        }
+    for (int j = 0; j < own_len; ++j) {
+        int64_t t = (int64_t)own * region_tokens + j;
+        if (t >= tok_lo && t < tok_hi) tok[n++] = t;
+    }
+    double* logit = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    for (int h = 0; h < hq_g; ++h) {
+        const uint16_t* qh = q + (int64_t)h * head_dim;
+        double mh = -INFINITY;
+        for (int64_t t = 0; t < n; ++t) {
+            const uint16_t* kt = kc + tok[t] * head_dim;
+            double dot = 0.0;
+            for (int d = 0; d < head_dim; ++d) dot += orc_bf16_value(qh[d]) * orc_bf16_value(kt[d]);
+            logit[t] = scale * dot;
+            if (logit[t] > mh) mh = logit[t];
+        }
+        double lh = 0.0;
+        for (int64_t t = 0; t < n; ++t) {
+            logit[t] = exp(logit[t] - mh);
+            lh += logit[t];
+        }
+        m[h] = mh;
+        l[h] = lh;
+        for (int d = 0; d < head_dim; ++d) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < n; ++t) acc += logit[t] * orc_bf16_value(vc[tok[t] * head_dim + d]);
+            o[(int64_t)h * head_dim + d] = acc;
+        }
+    }
+    free(logit);
+    free(tok);
+}
+
+void orc_attn_combine(int S, int head_dim, const double* m, const double* l, const double* o, double* out) {
+    double M = -INFINITY;
+    for (int s = 0; s < S; ++s)
+        if (m[s] > M) M = m[s];
+    double L = 0.0;
+    for (int s = 0; s < S; ++s) L += (l[s] > 0.0 ? exp(m[s] - M) * l[s] : 0.0);
+    for (int d = 0; d < head_dim; ++d) {
+        double acc = 0.0;
+        for (int s = 0; s < S; ++s)
+            if (l[s] > 0.0) acc += exp(m[s] - M) * o[(int64_t)s * head_dim + d];
+        out[d] = acc / L;
+    }
+}
+
+/* ------------------------------------------------------------------------------ */
 /* After step 4: the per-head sigmoid output gate.                                   */
 /* ------------------------------------------------------------------------------ */
 

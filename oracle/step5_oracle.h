@@ -91,6 +91,29 @@ void orc_attend_group(const uint16_t* q, int hq_g, int head_dim,
                       const int32_t* sel, int cnt, int pos, int region_tokens,
                       double scale, double* out);
 
+/* ---- sequence-sharded decode (one row's regions split over shards) ------------------
+ * Merge: the K smallest keys (-score, id) of the union of S shards' picks (shard s's
+ * list: ids[s][0 .. cnt_s) and their scores, rows of L entries), written in key order
+ * (ids_out has K entries, -1 padded); returns the count.
+ * The pick of the whole row equals this merge of the shards' own top K whenever the
+ * shards partition its regions.                                                        */
+int orc_merge_topk(int S, int L, int K, const int32_t* ids, const double* scores, const int32_t* counts,
+                   int32_t* ids_out);
+
+/* Partial attention of one (row, KV group) over the keys of a shard of its tokens
+ * [tok_lo, tok_hi): the picked regions inside it and, when it holds the row's own region,
+ * that region's tokens 8o .. pos.  Per head h, with logits x_t = scale * q_h . k_t:
+ *   m[h] = max_t x_t,  l[h] = sum_t exp(x_t - m[h]),  o[h][d] = sum_t exp(x_t - m[h]) v_t[d]
+ * (m = -inf, l = 0, o = 0 when the shard holds no key).  kc, vc: the whole (sequence,
+ * group) cache (t_cap rows, global token index); fp64.                               */
+void orc_attend_partial(const uint16_t* q, int hq_g, int head_dim, const uint16_t* kc, const uint16_t* vc,
+                        const int32_t* sel, int cnt, int pos, int region_tokens, int64_t tok_lo,
+                        int64_t tok_hi, double scale, double* m, double* l, double* o);
+
+/* Combine of S partial states of one head: out[d] = sum_s e^(m_s - M) o_s[d] /
+ * sum_s e^(m_s - M) l_s, M = max_s m_s.  m, l: [S]; o: [S][head_dim].                */
+void orc_attn_combine(int S, int head_dim, const double* m, const double* l, const double* o, double* out);
+
 /* ---- after step 4: the per-head sigmoid output gate ----------------------------------
  * ("Step-5-Preview on one 256 GB Mac", the native-family commit: Step-5's glue keeps
  * "the per-head sigmoid gate" among StepFun's rounding points.)  Reading: one gate
