@@ -47,6 +47,8 @@ def parse():
                     help="workload: 4 (headline, 1 row at 1M), 2 (4 rows at 128K), 0, 1, 3")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shards", type=int, default=4,
+                    help="sequence shards of the headline row timed beside the step (0: none)")
     return ap.parse_args()
 
 
@@ -202,7 +204,7 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def measure(cfg, steps, warmup, clocks=False):
+    def measure(cfg, steps, warmup, clocks=False, n_shards=0):
         w = S.workload(cfg, seed=17)
         t = S.materialize(w, device=dev)
         N, G = w.N, geom.num_kv_groups
@@ -300,42 +302,47 @@ def run_ours(args, rank, world, local_rank):
         assert s5.step5_device_status() == 0
         ms = max_over_ranks([float(per_step.mean())], dist, dev)[0]
 
-        # per-kernel durations: the three calls captured in one CUDA graph with timing
-        # event nodes between them (the events keep the kernels from overlapping), so the
-        # events bracket the kernels alone; without event nodes in graphs, eager calls
-        # behind a 1 GiB write that covers their launch
+        # per-kernel durations: the calls captured in one CUDA graph with timing event
+        # nodes between them (the events keep the kernels from overlapping), so the events
+        # bracket the kernels alone; without event nodes in graphs, eager calls behind a
+        # 1 GiB write that covers their launch
+        def time_calls(calls, reps):
+            times = np.zeros((reps, len(calls)))
+            try:
+                evg = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls) + 1)]
+                g_b = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g_b, capture_error_mode="thread_local"):
+                    evg[0].record()
+                    for j, fn in enumerate(calls):
+                        fn()
+                        evg[j + 1].record()
+                how = "CUDA graph with event nodes between the calls"
+                barrier()
+                for i in range(reps):
+                    flush.zero_()
+                    g_b.replay()
+                    torch.cuda.synchronize()
+                    times[i] = [evg[j].elapsed_time(evg[j + 1]) for j in range(len(calls))]
+            except (TypeError, RuntimeError):
+                how = "eager calls behind a 1 GiB write"
+                hold = torch.empty(4 * FLUSH_BYTES, dtype=torch.uint8, device=dev)
+                evb = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(reps)]
+                barrier()
+                for i in range(reps):
+                    hold.zero_()
+                    evb[i][0].record(stream)
+                    for j, fn in enumerate(calls):
+                        fn()
+                        evb[i][j + 1].record(stream)
+                barrier()
+                times = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(calls))] for e in evb])
+                del hold
+            assert s5.step5_device_status() == 0
+            return times, how
+
         steps_b = steps
         calls_b = (call_sum, call_score, call_attn, call_attn_gated, call_front)
-        times_b = np.zeros((steps_b, len(calls_b)))
-        try:
-            evg = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls_b) + 1)]
-            g_b = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_b, capture_error_mode="thread_local"):
-                evg[0].record()
-                for j, fn in enumerate(calls_b):
-                    fn()
-                    evg[j + 1].record()
-            breakdown_how = "CUDA graph with event nodes between the calls"
-            barrier()
-            for i in range(steps_b):
-                flush.zero_()
-                g_b.replay()
-                torch.cuda.synchronize()
-                times_b[i] = [evg[j].elapsed_time(evg[j + 1]) for j in range(len(calls_b))]
-        except (TypeError, RuntimeError):
-            breakdown_how = "eager calls behind a 1 GiB write"
-            hold = torch.empty(4 * FLUSH_BYTES, dtype=torch.uint8, device=dev)
-            evb = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls_b) + 1)] for _ in range(steps_b)]
-            barrier()
-            for i in range(steps_b):
-                hold.zero_()
-                evb[i][0].record(stream)
-                for j, fn in enumerate(calls_b):
-                    fn()
-                    evb[i][j + 1].record(stream)
-            barrier()
-            times_b = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(calls_b))] for e in evb])
-            del hold
+        times_b, breakdown_how = time_calls(calls_b, steps_b)
         per_sum, per_score, per_attn, per_gated = times_b[:, 0], times_b[:, 1], times_b[:, 2], times_b[:, 3]
         per_front = times_b[:, 4]
         bytes_step, bytes_score = step_bytes(w, geom)
@@ -345,6 +352,65 @@ def run_ours(args, rank, world, local_rank):
                    per_gated=float(per_gated.mean()), per_front=float(per_front.mean()), bytes_step=bytes_step,
                    bytes_score=bytes_score, launches=launches_per_step * steps, path=path, wall=wall,
                    clocks=sampler.summary() if sampler else None)
+
+        # sequence shards of the rows (each shard's summaries and K/V a copy of its part,
+        # as one GPU of a sharded deployment would hold them): each shard's score + pick,
+        # the merge, each shard's attention and the combine, timed call by call on this
+        # one GPU (the exchange of picks and states between GPUs is not part of it)
+        if n_shards > 1:
+            cuts = [w.t_cap // 8 * i // n_shards * 8 for i in range(n_shards)] + [w.t_cap]
+            Hq, K = geom.num_q_heads, geom.top_k
+            sh_ids = torch.empty((n_shards, N, G, K), dtype=torch.int32, device=dev)
+            sh_cnt = torch.empty((n_shards, N, G), dtype=torch.int32, device=dev)
+            sh_sc = torch.empty((n_shards, N, G, K), dtype=torch.float32, device=dev)
+            sh_states = torch.empty((n_shards, N, Hq, 130), dtype=torch.float32, device=dev)
+            m_ids = torch.empty_like(sel_ids)
+            m_cnt = torch.empty_like(sel_count)
+            parts = []
+            for i in range(n_shards):
+                lo_t, hi_t = cuts[i], cuts[i + 1]
+                lo, hi = lo_t // 8, min(hi_t // 8, w.r_cap)
+                parts.append(dict(lo=lo, lo_t=lo_t, summ=t["summaries"][:, :, lo:hi].contiguous(),
+                                  kc=t["k_cache"][:, :, lo_t:hi_t].contiguous(),
+                                  vc=t["v_cache"][:, :, lo_t:hi_t].contiguous(),
+                                  ws=s5.Workspace.create(geom, N, hi - lo, device=dev)))
+
+            def shard_score(i):
+                d = parts[i]
+                return lambda: s5.step5_index_score_topk_shard(
+                    geom, t["idx_q"], t["w"], t["row_seq"], t["row_pos"], t["cos"], t["sin"], d["summ"], d["lo"],
+                    sh_ids[i], sh_cnt[i], sh_sc[i], d["ws"].tensor, t_cap=w.t_cap)
+
+            def shard_attn(i):
+                d = parts[i]
+                return lambda: s5.step5_sparse_attn_shard(
+                    geom, t["q"], d["kc"], d["vc"], d["lo_t"], t["row_seq"], t["row_pos"], m_ids, m_cnt,
+                    sh_states[i], d["ws"].tensor)
+
+            calls_s = ([shard_score(i) for i in range(n_shards)] +
+                       [lambda: s5.step5_merge_topk(geom, sh_ids, sh_sc, sh_cnt, m_ids, m_cnt)] +
+                       [shard_attn(i) for i in range(n_shards)] +
+                       [lambda: s5.step5_attn_combine(geom, sh_states, out)])
+            for _ in range(warmup):
+                for fn in calls_s:
+                    fn()
+            torch.cuda.synchronize()
+            assert s5.step5_device_status() == 0
+            times_s, _ = time_calls(calls_s, steps_b)
+            ts = times_s.mean(axis=0) * 1e3
+            sc_us, at_us = ts[:n_shards], ts[n_shards + 1:2 * n_shards + 1]
+            res["shards"] = {
+                "shards": n_shards, "tokens_per_shard": cuts[1] - cuts[0],
+                "score_select_us": [round(float(x), 2) for x in sc_us],
+                "merge_us": round(float(ts[n_shards]), 2),
+                "attention_us": [round(float(x), 2) for x in at_us],
+                "combine_us": round(float(ts[-1]), 2),
+                "per_gpu_critical_path_us": round(float(sc_us.max() + ts[n_shards] + at_us.max() + ts[-1]), 2),
+                "picks_equal_whole_row": bool(torch.equal(m_ids, sel_ids) and torch.equal(m_cnt, sel_count)),
+                "how": "calls timed one by one on one GPU; critical path = slowest shard's score + merge + "
+                       "slowest shard's attention + combine, without the exchange between GPUs"}
+            del parts
+            torch.cuda.empty_cache()
 
         # end to end through the C ABI with host buffers: the rows' inputs copied in from
         # pinned memory and the output copied back, every step
@@ -386,7 +452,7 @@ def run_ours(args, rank, world, local_rank):
         return res
 
     peak, peak_kind = peaks()
-    head = measure(args.workload, args.steps, args.warmup, clocks=True)
+    head = measure(args.workload, args.steps, args.warmup, clocks=True, n_shards=args.shards)
     w = head["w"]
     rows = w.N * world
     value = whole_job_rate(w.N, world, head["ms"])
@@ -425,6 +491,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": head["launches"],
         "clocks": head["clocks"],
     }
+    if "shards" in head:
+        line["sharded_decode"] = head["shards"]
     if not args.no_secondary:
         sec = measure(2 if args.workload == 4 else 4, max(20, args.steps // 2), args.warmup)
         sgbs = sec["bytes_step"] / (sec["ms"] / 1e3) / 1e9

@@ -30,6 +30,7 @@ __all__ = [
     "step5_region_summarize", "step5_index_score_topk", "step5_sparse_attn", "step5_sparse_attn_gated",
     "step5_indexer_front",
     "step5_index_score_topk_noalloc",
+    "step5_index_score_topk_shard", "step5_merge_topk", "step5_sparse_attn_shard", "step5_attn_combine",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
     "step5_set_select_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
     "Workspace", "decode_step",
@@ -100,6 +101,11 @@ def load():
                                     P, P, P, P, sz, P]),
         "step5_index_score_topk_noalloc": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P,
                                                  P, P, P]),
+        "step5_index_score_topk_shard": (i32, [G, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P,
+                                               P, P, sz, P]),
+        "step5_merge_topk": (i32, [G, i32, i32, P, P, P, P, P, P, P]),
+        "step5_sparse_attn_shard": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]),
+        "step5_attn_combine": (i32, [G, i32, i32, P, P, P, P]),
         "step5_workspace_bytes": (sz, [G, i32, i32]),
         "step5_workspace_init": (i32, [P, sz, P]),
         "step5_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32), P]),
@@ -259,6 +265,51 @@ def step5_sparse_attn(geom, q, k_cache, v_cache, row_seq, row_pos, sel_ids, sel_
         ctypes.byref(Geometry.of(geom)), N, B, t_cap, _ptr(q), _ptr(k_cache), _ptr(v_cache),
         _ptr(row_seq), _ptr(row_pos), _ptr(sel_ids), _ptr(sel_count), _ptr(out), _ptr(workspace),
         ws_bytes, _stream(stream)))
+
+
+def step5_index_score_topk_shard(geom, idx_q, w, row_seq, row_pos, cos, sin, summaries, region_lo,
+                                 sel_ids, sel_count, sel_scores, workspace, t_cap, stream=None):
+    """Scoring and top-k of one sequence shard: summaries [B][G][r_cap_local][64] hold
+    regions region_lo .. region_lo + r_cap_local - 1; writes the shard's pick with the
+    rows' region ids, sel_scores required."""
+    N = idx_q.shape[0]
+    B, _, r_cap, _ = summaries.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("step5_index_score_topk_shard", load().step5_index_score_topk_shard(
+        ctypes.byref(Geometry.of(geom)), N, B, int(t_cap), r_cap, int(region_lo), _ptr(idx_q), _ptr(w),
+        _ptr(row_seq), _ptr(row_pos), _ptr(cos), _ptr(sin), _ptr(summaries), _ptr(sel_ids),
+        _ptr(sel_count), _ptr(sel_scores), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def step5_merge_topk(geom, shard_ids, shard_scores, shard_counts, sel_ids, sel_count, sel_scores=None,
+                     stream=None):
+    """The rows' pick from S shards' picks: shard_ids / shard_scores [S][N][G][top_k],
+    shard_counts [S][N][G] -> sel_ids [N][G][top_k], sel_count [N][G] (+ sel_scores)."""
+    S, N = shard_ids.shape[0], shard_ids.shape[1]
+    _check("step5_merge_topk", load().step5_merge_topk(
+        ctypes.byref(Geometry.of(geom)), S, N, _ptr(shard_ids), _ptr(shard_scores), _ptr(shard_counts),
+        _ptr(sel_ids), _ptr(sel_count), _ptr(sel_scores), _stream(stream)))
+
+
+def step5_sparse_attn_shard(geom, q, k_cache, v_cache, token_lo, row_seq, row_pos, sel_ids, sel_count,
+                            states, workspace, stream=None):
+    """Attention of one sequence shard: k/v cache [B][G][t_cap_local][128] hold tokens
+    token_lo .. token_lo + t_cap_local - 1; writes states [N][Hq][130] fp32 (m, l, o)."""
+    N = q.shape[0]
+    B, _, t_cap, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("step5_sparse_attn_shard", load().step5_sparse_attn_shard(
+        ctypes.byref(Geometry.of(geom)), N, B, t_cap, int(token_lo), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(row_seq), _ptr(row_pos), _ptr(sel_ids), _ptr(sel_count), _ptr(states), _ptr(workspace),
+        ws_bytes, _stream(stream)))
+
+
+def step5_attn_combine(geom, states, out, gate=None, stream=None):
+    """The output from S shards' states [S][N][Hq][130] -> out [N][Hq][128] bf16 (with the
+    per-head sigmoid gate [N][Hq] when given)."""
+    S, N = states.shape[0], states.shape[1]
+    _check("step5_attn_combine", load().step5_attn_combine(
+        ctypes.byref(Geometry.of(geom)), S, N, _ptr(states), _ptr(gate), _ptr(out), _stream(stream)))
 
 
 def step5_decode_step(geom, t: dict, ws, sel_ids, sel_count, out, max_regions_per_seq, stream=None):

@@ -98,12 +98,18 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     const uint32_t epoch = S > 1 ? __ldcg(p.bar + ng) : 0u;
     __syncthreads();
     STEP5_STAMP(4, 8);
-    if (b < 0 || b >= p.B || pos < 0 || pos >= p.t_cap) {
+    // (a shard's cache holds tokens tok_lo .. tok_lo + t_cap - 1 of the row's sequence)
+    if (b < 0 || b >= p.B || pos < 0 || (p.states == nullptr && pos >= p.t_cap)) {
         // the same for every block of the (row, group): all leave before its barrier
         if (split == 0) {
             if (tid == 0) raise_status(p.status, kDevRange);
-            for (int i = tid; i < hq_g * 128; i += kThreads)
-                p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g) * 128 + i] = 0;
+            const int64_t h0 = (int64_t)n * p.Hq + (int64_t)g * hq_g;
+            if (p.states == nullptr) {
+                for (int i = tid; i < hq_g * 128; i += kThreads) p.out[h0 * 128 + i] = 0;
+            } else {  // an empty state
+                for (int i = tid; i < hq_g * kSlotFloats; i += kThreads)
+                    p.states[h0 * kSlotFloats + i] = i % kSlotFloats == 0 ? -INFINITY : 0.0f;
+            }
         }
         return;
     }
@@ -130,23 +136,33 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     __syncwarp();
     STEP5_STAMP(4, 9);
 
-    // entry e -> (region id, valid tokens); invalid ids are masked out entirely
+    // entry e -> (region id, valid tokens); invalid ids are masked out entirely, and so
+    // are regions outside a shard's tokens (rid is then the region's first cache row
+    // of this call, relative to tok_lo, in tokens / 8)
+    const int rlo = p.tok_lo >> 3, rhi = (p.tok_lo + p.t_cap) >> 3;
     auto entry = [&](int e, int& rid) -> int {
         if (e >= e1) {
             rid = -1;
             return 0;
         }
+        int ntok = 8;
         if (e == cnt) {
             rid = own;
-            return own_tokens;
+            ntok = own_tokens;
+        } else {
+            rid = s_ids[e - e0];
+            if (rid < 0 || rid >= own) {
+                raise_status(p.status, kDevRange);
+                rid = -1;
+                return 0;
+            }
         }
-        rid = s_ids[e - e0];
-        if (rid < 0 || rid >= own) {
-            raise_status(p.status, kDevRange);
+        if (rid < rlo || rid >= rhi) {
             rid = -1;
             return 0;
         }
-        return 8;
+        rid -= rlo;
+        return ntok;
     };
 
     auto issue = [&](int li) {
@@ -372,8 +388,17 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
             float O = 0.0f;
 #pragma unroll
             for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * kMergeRow + d] * s_wsc[w][r];
-            p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + d] =
-                f32_to_bf16_bits(O / s_L[r] * gate_factor(p, n, g * hq_g + r));
+            const int64_t hrow = (int64_t)n * p.Hq + (int64_t)g * hq_g + r;
+            if (p.states != nullptr) {  // a shard: the state, not the output
+                float* st = p.states + hrow * kSlotFloats;
+                st[2 + d] = O;
+                if (d == 0) {
+                    st[0] = s_M[r];
+                    st[1] = s_L[r];
+                }
+            } else {
+                p.out[hrow * 128 + d] = f32_to_bf16_bits(O / s_L[r] * gate_factor(p, n, g * hq_g + r));
+            }
         }
         return;
     }
@@ -466,7 +491,14 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (lane == 0) s_sL[r - r_lo] = L;
+        if (lane == 0) {
+            s_sL[r - r_lo] = L;
+            if (p.states != nullptr) {  // a shard: (every block touching the row writes the same)
+                float* st = p.states + ((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * kSlotFloats;
+                st[0] = M;
+                st[1] = L;
+            }
+        }
     }
 #pragma unroll
     for (int u = 0; u < kItems; ++u) {
@@ -478,8 +510,11 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         const int e = e_lo + t, r = e >> 7;
         float O = 0.0f;
         for (int sp = 0; sp < S; ++sp) O += s_val[sp * nout + t] * s_sw[r - r_lo][sp];
-        p.out[((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * 128 + (e & 127)] =
-            f32_to_bf16_bits(O / s_sL[r - r_lo] * gate_factor(p, n, g * hq_g + r));
+        const int64_t hrow = (int64_t)n * p.Hq + (int64_t)g * hq_g + r;
+        if (p.states != nullptr)
+            p.states[hrow * kSlotFloats + 2 + (e & 127)] = O;
+        else
+            p.out[hrow * 128 + (e & 127)] = f32_to_bf16_bits(O / s_sL[r - r_lo] * gate_factor(p, n, g * hq_g + r));
     }
     STEP5_STAMP(4, 7);
 }

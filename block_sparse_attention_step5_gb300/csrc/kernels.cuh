@@ -122,6 +122,8 @@ struct ScoreParams {
     uint32_t* bar2;          // [N][G] generation | arrivals      (split path)
     uint32_t* status;
     int N, B, G, idx_heads, hpg, t_cap, r_cap, rope_dims, top_k;
+    int region_lo;           // the summaries' first region (a shard of the rows' regions), else 0
+    int shard;               // 1: a shard's call (regions past the summaries belong to other shards)
     int num_sms;             // split path: persistent blocks (one per SM)
     int overlap_prologue;    // split path: read the non-summary inputs before the launch wait
     // split path with overlap_prologue: the launch before writes only the summaries of
@@ -154,6 +156,8 @@ struct AttnParams {
     const int32_t* sel_count;
     uint16_t* out;           // [N][Hq][128]
     const uint16_t* gate;    // [N][Hq] bf16 logits of the per-head sigmoid output gate, or null
+    float* states;           // a shard of the rows' tokens: [N][Hq][130] (m, l, o) instead of out
+    int tok_lo;              // the cache's first token (a shard), else 0
     float* part;             // splits > 1: [N*G][splits][hq_g][130] block states
     uint32_t* bar;           // splits > 1: [N*G] epoch of each (row, group)'s state exchange
     uint32_t* flags;         // splits > 1: [N*G][kAttnMaxSplits] epoch + 1 once a block's state is out
@@ -166,5 +170,31 @@ cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const
                              cudaStream_t stream, bool pdl);
 size_t attention_smem_bytes();  // dynamic part
 constexpr size_t kAttnStaticSmem = (kMaxTopK + 2) * 4 + 16384;  // picked ids + merge scratch
+
+// ----------------------------------------------------------------- sequence shards
+constexpr int kMaxShards = 32;        // shards of one row (a warp's lanes in the combine)
+constexpr int kMaxShardKeys = 16384;  // S * top_k keys a merge block stages (128 KB)
+
+// The row's top K from the shards' own top K lists (each in key order).
+struct MergeParams {
+    const int32_t* ids;      // [S][NG][top_k] region ids of the row (global)
+    const float* scores;     // [S][NG][top_k]
+    const int32_t* counts;   // [S][NG]
+    int32_t* sel_ids;        // [NG][top_k]
+    int32_t* sel_count;      // [NG]
+    float* sel_scores;       // [NG][top_k] or null
+    uint32_t* status;
+    int S, NG, top_k;
+};
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+
+// out = (sum_s 2^(m_s - M) o_s) / (sum_s 2^(m_s - M) l_s), M = max_s m_s, per head row.
+struct CombineParams {
+    const float* states;     // [S][N][Hq][130] (m, l, o[128]) of each shard
+    const uint16_t* gate;    // [N][Hq] bf16 gate logits or null
+    uint16_t* out;           // [N][Hq][128]
+    int S, N, Hq;
+};
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 }  // namespace step5

@@ -388,7 +388,7 @@ __device__ void write_selection(const ScoreParams& p, int n, int g, int take, co
     for (int i = threadIdx.x; i < p.top_k; i += NT) {
         if (i < take) {
             const uint64_t key = s_sel[i];
-            ids[i] = (int32_t)(uint32_t)(key & 0xffffffffu);
+            ids[i] = (int32_t)(uint32_t)(key & 0xffffffffu) + p.region_lo;
             if (ss) ss[i] = score_of_desc_key((uint32_t)(key >> 32));
         } else {
             ids[i] = -1;
@@ -399,11 +399,15 @@ __device__ void write_selection(const ScoreParams& p, int n, int g, int take, co
 }
 
 // Validated (sequence, R) of row n, or R = -1 when the row is out of range.
+// Candidate regions of row n in this call's summaries: region_lo + [0, R).  A whole-row
+// call needs a slot for every candidate; a shard takes those of its slots.
 __device__ __forceinline__ int row_regions(const ScoreParams& p, int n, int& b, int& pos) {
     b = p.row_seq[n];
     pos = p.row_pos[n];
-    if (b < 0 || b >= p.B || pos < 0 || pos >= p.t_cap || pos / 8 > p.r_cap) return -1;
-    return pos / 8;
+    if (b < 0 || b >= p.B || pos < 0 || pos >= p.t_cap) return -1;
+    const int R = pos / 8 - p.region_lo;
+    if (!p.shard) return R > p.r_cap ? -1 : R;
+    return R < 0 ? 0 : (R > p.r_cap ? p.r_cap : R);
 }
 
 // ----------------------------------------------------------------- fused path
@@ -953,7 +957,7 @@ __device__ void rank_segment(const ScoreParams& p, int ng, int sub, int nb, uint
 #pragma unroll
                 for (int w = 0; w < kSplitWarps; ++w) rank += s_w[w * 32 + lane];
                 if (rank < (uint32_t)K) {
-                    ids[rank] = (int32_t)(uint32_t)(key & 0xffffffffu);
+                    ids[rank] = (int32_t)(uint32_t)(key & 0xffffffffu) + p.region_lo;
                     if (ss) ss[rank] = score_of_desc_key((uint32_t)(key >> 32));
                 }
             }

@@ -379,7 +379,8 @@ step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_
                         const void* rope_cos_bf16, const void* rope_sin_bf16, const uint8_t* summaries_e4m3,
                         int32_t* sel_ids, int32_t* sel_count, float* scores_or_null, float* sel_scores_or_null,
                         void* workspace, size_t workspace_bytes, step5_stream_t stream, int overlap,
-                        const int32_t* defer_begin, const int32_t* defer_end, bool launch) {
+                        const int32_t* defer_begin, const int32_t* defer_end, bool launch,
+                        int32_t region_lo = 0, bool shard = false) {
     step5_status s = check_geometry(geom);
     if (s != STEP5_OK) return s;
     if (N <= 0 || B <= 0 || t_cap <= 0 || r_cap <= 0) return STEP5_ERR_INVALID_ARGUMENT;
@@ -432,6 +433,8 @@ step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_
     p.t_cap = t_cap;
     p.r_cap = r_cap;
     p.rope_dims = rope_cos_bf16 ? geom->rope_dims : 0;
+    p.region_lo = region_lo;
+    p.shard = shard ? 1 : 0;
     p.top_k = geom->top_k;
     cudaError_t e;
     if (fused) {
@@ -449,14 +452,18 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
                        const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
                        const int32_t* row_pos, const int32_t* sel_ids, const int32_t* sel_count, void* out_bf16,
                        void* workspace, size_t workspace_bytes, step5_stream_t stream, bool launch,
-                       const void* gate_bf16 = nullptr) {
+                       const void* gate_bf16 = nullptr, float* states = nullptr, int32_t tok_lo = 0) {
     step5_status s = check_geometry(geom);
     if (s != STEP5_OK) return s;
     if (N <= 0 || B <= 0 || t_cap <= 0 || (t_cap % geom->region_tokens)) return STEP5_ERR_INVALID_ARGUMENT;
     if (N > 65535) return STEP5_ERR_UNSUPPORTED;
-    if (!q_bf16 || !k_cache_bf16 || !v_cache_bf16 || !row_seq || !row_pos || !sel_ids || !sel_count || !out_bf16)
+    if (!q_bf16 || !k_cache_bf16 || !v_cache_bf16 || !row_seq || !row_pos || !sel_ids || !sel_count ||
+        (out_bf16 == nullptr) == (states == nullptr))
         return STEP5_ERR_INVALID_ARGUMENT;
-    if (!aligned16(q_bf16) || !aligned16(k_cache_bf16) || !aligned16(v_cache_bf16) || !aligned16(out_bf16))
+    if (!aligned16(q_bf16) || !aligned16(k_cache_bf16) || !aligned16(v_cache_bf16) ||
+        (out_bf16 && !aligned16(out_bf16)) || (states && !aligned16(states)))
+        return STEP5_ERR_INVALID_ARGUMENT;
+    if (tok_lo < 0 || tok_lo % geom->region_tokens || (int64_t)tok_lo + t_cap > INT32_MAX)
         return STEP5_ERR_INVALID_ARGUMENT;
     const int G = geom->num_kv_groups;
     const uint64_t rows = (uint64_t)B * G * t_cap;
@@ -481,6 +488,8 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     p.sel_count = sel_count;
     p.out = static_cast<uint16_t*>(out_bf16);
     p.gate = static_cast<const uint16_t*>(gate_bf16);
+    p.states = states;
+    p.tok_lo = tok_lo;
     p.status = st;
     p.N = N;
     p.B = B;
@@ -525,6 +534,20 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
                       workspace_bytes, stream, g_overlap_prologue, nullptr, nullptr, true);
 }
 
+step5_status step5_index_score_topk_shard(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap,
+                                          int32_t r_cap_local, int32_t region_lo, const void* idx_q_bf16,
+                                          const float* w, const int32_t* row_seq, const int32_t* row_pos,
+                                          const void* rope_cos_bf16, const void* rope_sin_bf16,
+                                          const uint8_t* summaries_e4m3, int32_t* sel_ids, int32_t* sel_count,
+                                          float* sel_scores, void* workspace, size_t workspace_bytes,
+                                          step5_stream_t stream) {
+    if (region_lo < 0 || sel_scores == nullptr) return STEP5_ERR_INVALID_ARGUMENT;
+    if ((int64_t)region_lo + r_cap_local > INT32_MAX / 8) return STEP5_ERR_INVALID_ARGUMENT;
+    return score_impl(geom, N, B, t_cap, r_cap_local, idx_q_bf16, w, row_seq, row_pos, rope_cos_bf16,
+                      rope_sin_bf16, summaries_e4m3, sel_ids, sel_count, nullptr, sel_scores, workspace,
+                      workspace_bytes, stream, g_overlap_prologue, nullptr, nullptr, true, region_lo, true);
+}
+
 step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, const void* q_bf16,
                                const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
                                const int32_t* row_pos, const int32_t* sel_ids, const int32_t* sel_count,
@@ -541,6 +564,59 @@ step5_status step5_sparse_attn_gated(const step5_geometry* geom, int32_t N, int3
     if (gate_bf16 == nullptr) return STEP5_ERR_INVALID_ARGUMENT;
     return attn_impl(geom, N, B, t_cap, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count,
                      out_bf16, workspace, workspace_bytes, stream, true, gate_bf16);
+}
+
+step5_status step5_sparse_attn_shard(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap_local,
+                                     int32_t token_lo, const void* q_bf16, const void* k_cache_bf16,
+                                     const void* v_cache_bf16, const int32_t* row_seq, const int32_t* row_pos,
+                                     const int32_t* sel_ids, const int32_t* sel_count, float* states_f32,
+                                     void* workspace, size_t workspace_bytes, step5_stream_t stream) {
+    if (states_f32 == nullptr) return STEP5_ERR_INVALID_ARGUMENT;
+    return attn_impl(geom, N, B, t_cap_local, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids,
+                     sel_count, nullptr, workspace, workspace_bytes, stream, true, nullptr, states_f32, token_lo);
+}
+
+step5_status step5_merge_topk(const step5_geometry* geom, int32_t S, int32_t N, const int32_t* shard_ids,
+                              const float* shard_scores, const int32_t* shard_counts, int32_t* sel_ids,
+                              int32_t* sel_count, float* sel_scores_or_null, step5_stream_t stream) {
+    step5_status s = check_geometry(geom);
+    if (s != STEP5_OK) return s;
+    if (S <= 0 || N <= 0) return STEP5_ERR_INVALID_ARGUMENT;
+    if (!shard_ids || !shard_scores || !shard_counts || !sel_ids || !sel_count) return STEP5_ERR_INVALID_ARGUMENT;
+    const int64_t NG = (int64_t)N * geom->num_kv_groups;
+    if (NG > INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
+    if (S > kMaxShards || (int64_t)S * geom->top_k > kMaxShardKeys) return STEP5_ERR_UNSUPPORTED;
+    uint32_t* st = status_ptr();
+    if (!st) return STEP5_ERR_CUDA;
+    MergeParams p;
+    p.ids = shard_ids;
+    p.scores = shard_scores;
+    p.counts = shard_counts;
+    p.sel_ids = sel_ids;
+    p.sel_count = sel_count;
+    p.sel_scores = sel_scores_or_null;
+    p.status = st;
+    p.S = S;
+    p.NG = (int)NG;
+    p.top_k = geom->top_k;
+    return launch_merge(p, (cudaStream_t)stream) == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
+}
+
+step5_status step5_attn_combine(const step5_geometry* geom, int32_t S, int32_t N, const float* states_f32,
+                                const void* gate_bf16_or_null, void* out_bf16, step5_stream_t stream) {
+    step5_status s = check_geometry(geom);
+    if (s != STEP5_OK) return s;
+    if (S <= 0 || N <= 0 || !states_f32 || !out_bf16 || !aligned16(out_bf16)) return STEP5_ERR_INVALID_ARGUMENT;
+    if (S > kMaxShards) return STEP5_ERR_UNSUPPORTED;
+    if ((int64_t)N * geom->num_q_heads * kAttnSlotFloats * S > ((int64_t)1 << 40)) return STEP5_ERR_INVALID_ARGUMENT;
+    CombineParams p;
+    p.states = states_f32;
+    p.gate = static_cast<const uint16_t*>(gate_bf16_or_null);
+    p.out = static_cast<uint16_t*>(out_bf16);
+    p.S = S;
+    p.N = N;
+    p.Hq = geom->num_q_heads;
+    return launch_combine(p, (cudaStream_t)stream) == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
 }
 
 step5_status step5_indexer_front(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,

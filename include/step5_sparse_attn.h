@@ -218,6 +218,68 @@ step5_status step5_sparse_attn_gated(const step5_geometry* geom, int32_t N, int3
                                      void* workspace, size_t workspace_bytes,
                                      step5_stream_t stream);
 
+/* Sequence-sharded decode ("Step-5-Preview on one 256 GB Mac", CSA-indexer commit:
+ * the indexer is what takes Step-5 to contexts of 1M tokens; with a row's regions and
+ * KV cache split over S shards (one per GPU, or processed one after another) the
+ * method's result is unchanged, since:
+ *  - a region among the row's top_k by (-score, id) is among its own shard's top_k, so
+ *    the row's pick is the top_k of the union of the shards' picks (step5_merge_topk);
+ *  - softmax attention over a union of disjoint key sets is the combine of each set's
+ *    (max m, sum l, weighted sum o) state (step5_attn_combine).)
+ * Every call below takes the geometry and conventions of the whole-row calls.
+ *
+ * Step (2)+(3) on one shard: the shard holds the summaries of regions region_lo ..
+ * region_lo + r_cap_local - 1 of every sequence, summaries_e4m3 [B][G][r_cap_local][64];
+ * row n's candidates in it are those below its own region, o = p / 8.  Writes that
+ * shard's pick as step5_index_score_topk does, with ids the row's region ids (region_lo
+ * added) and sel_scores (required) their scores.  t_cap is the rows' token capacity
+ * (the rope tables' rows; positions must be below it).  region_lo >= 0.  Other
+ * arguments as step5_index_score_topk (scores are not exported). */
+step5_status step5_index_score_topk_shard(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap,
+                                          int32_t r_cap_local, int32_t region_lo, const void* idx_q_bf16,
+                                          const float* w, const int32_t* row_seq, const int32_t* row_pos,
+                                          const void* rope_cos_bf16, const void* rope_sin_bf16,
+                                          const uint8_t* summaries_e4m3, int32_t* sel_ids, int32_t* sel_count,
+                                          float* sel_scores, void* workspace, size_t workspace_bytes,
+                                          step5_stream_t stream);
+
+/* The row's pick from S shards' picks: for each (n, g), the min(top_k, sum_s count)
+ * smallest (-score, id) keys of the union of shard_ids[s][n][g][0 .. shard_counts[s][n][g])
+ * (each shard's list in ascending key order, as step5_index_score_topk_shard writes
+ * it; ids distinct across shards), in ascending key order; the rest of sel_ids is -1
+ * (sel_scores -inf).  shard_ids, shard_scores: [S][N][G][top_k]; shard_counts [S][N][G];
+ * sel_ids [N][G][top_k]; sel_count [N][G]; sel_scores_or_null [N][G][top_k] or NULL.
+ * 1 <= S <= 32 and S * top_k <= 16384, else STEP5_ERR_UNSUPPORTED.  A count outside
+ * [0, top_k] raises STEP5_DEV_RANGE and is clamped. */
+step5_status step5_merge_topk(const step5_geometry* geom, int32_t S, int32_t N, const int32_t* shard_ids,
+                              const float* shard_scores, const int32_t* shard_counts, int32_t* sel_ids,
+                              int32_t* sel_count, float* sel_scores_or_null, step5_stream_t stream);
+
+/* Step (4) on one shard: the shard's caches k_cache_bf16, v_cache_bf16
+ * [B][G][t_cap_local][head_dim] hold tokens token_lo .. token_lo + t_cap_local - 1 of
+ * every sequence (token_lo and t_cap_local multiples of region_tokens).  Of row n's keys
+ * (the regions sel_ids picked for the whole row, then its own region) those inside the
+ * shard are attended; instead of an output, the call writes per query head the state
+ * (m, l, o[128]) with m the largest scaled score softmax_scale * log2(e) * q . k
+ * (-inf when the shard holds none of the row's keys), l = sum 2^(s - m), o = sum
+ * 2^(s - m) v (fp32; the P V product takes P in bf16 as step5_sparse_attn does):
+ * states_f32 [N][num_q_heads][130], 16-byte aligned.  Positions may lie past the
+ * shard.  workspace as for step5_sparse_attn. */
+step5_status step5_sparse_attn_shard(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap_local,
+                                     int32_t token_lo, const void* q_bf16, const void* k_cache_bf16,
+                                     const void* v_cache_bf16, const int32_t* row_seq, const int32_t* row_pos,
+                                     const int32_t* sel_ids, const int32_t* sel_count, float* states_f32,
+                                     void* workspace, size_t workspace_bytes, step5_stream_t stream);
+
+/* The output from S shards' states: states_f32 [S][N][num_q_heads][130] (shard s's
+ * states at s * N * num_q_heads * 130); per head row, M = max_s m_s and
+ *   out = bf16( sigmoid(gate) * (sum_s 2^(m_s - M) o_s) / (sum_s 2^(m_s - M) l_s) )
+ * summed in shard order, with the gate factor 1 when gate_bf16_or_null is NULL
+ * (gate [N][num_q_heads] bf16 logits); 0 where no shard holds a key.
+ * out_bf16 [N][num_q_heads][head_dim], 16-byte aligned.  1 <= S <= 32. */
+step5_status step5_attn_combine(const step5_geometry* geom, int32_t S, int32_t N, const float* states_f32,
+                                const void* gate_bf16_or_null, void* out_bf16, step5_stream_t stream);
+
 /* One whole step: step5_region_summarize, then step5_index_score_topk, then
  * step5_sparse_attn, on one stream, with the same arguments and the same results as the
  * three calls (no counterpart in the pages: a composition for serving loops).  Every

@@ -128,6 +128,36 @@ def test_null_and_size_rejections(s5):
                                  fake, fake, fake, None, 0, None) == 2
 
 
+def test_shard_call_rejections(s5):
+    """The sequence-shard calls reject bad arguments on the host, before any launch."""
+    lib = s5.load()
+    g = G()
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    # shard scoring: negative region_lo, missing picked-score output
+    assert lib.step5_index_score_topk_shard(ctypes.byref(g), 1, 1, 64, 8, -8, fake, fake, fake, fake, None,
+                                            None, fake, fake, fake, fake, None, 0, None) == 1
+    assert lib.step5_index_score_topk_shard(ctypes.byref(g), 1, 1, 64, 8, 0, fake, fake, fake, fake, None,
+                                            None, fake, fake, fake, None, None, 0, None) == 1
+    # merge: no shards, too many shards or keys, null inputs
+    assert lib.step5_merge_topk(ctypes.byref(g), 0, 1, fake, fake, fake, fake, fake, None, None) == 1
+    assert lib.step5_merge_topk(ctypes.byref(g), 33, 1, fake, fake, fake, fake, fake, None, None) == 2
+    assert lib.step5_merge_topk(ctypes.byref(G(top_k=2048)), 9, 1, fake, fake, fake, fake, fake, None,
+                                None) == 2
+    assert lib.step5_merge_topk(ctypes.byref(g), 2, 1, None, fake, fake, fake, fake, None, None) == 1
+    # shard attention: no states, token_lo off the region grid, misaligned states
+    assert lib.step5_sparse_attn_shard(ctypes.byref(g), 1, 1, 64, 0, fake, fake, fake, fake, fake, fake,
+                                       fake, None, None, 0, None) == 1
+    assert lib.step5_sparse_attn_shard(ctypes.byref(g), 1, 1, 64, 4, fake, fake, fake, fake, fake, fake,
+                                       fake, fake, None, 0, None) == 1
+    assert lib.step5_sparse_attn_shard(ctypes.byref(g), 1, 1, 64, 8, fake, fake, fake, fake, fake, fake,
+                                       fake, odd, None, 0, None) == 1
+    # combine: no shards, too many, misaligned output
+    assert lib.step5_attn_combine(ctypes.byref(g), 0, 1, fake, None, fake, None) == 1
+    assert lib.step5_attn_combine(ctypes.byref(g), 33, 1, fake, None, fake, None) == 2
+    assert lib.step5_attn_combine(ctypes.byref(g), 2, 1, fake, None, odd, None) == 1
+
+
 def test_status_strings(s5):
     for code in range(6):
         assert isinstance(s5.step5_status_string(code), str)
