@@ -239,9 +239,11 @@ def run_ours(args, rank, world, local_rank):
         gate = (torch.randn((N, geom.num_q_heads), generator=torch.Generator().manual_seed(61)) * 3).to(
             torch.bfloat16).to(dev)
 
+        out_gated = torch.empty_like(out)
+
         def call_attn_gated():
             s5.step5_sparse_attn_gated(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"],
-                                       sel_ids, sel_count, gate, out, ws.tensor)
+                                       sel_ids, sel_count, gate, out_gated, ws.tensor)
 
         # the indexer's decode front end (q/k norms, the row token's k/z write, a completed
         # region's summary), timed beside the step only: it writes token p of the caches
@@ -366,6 +368,7 @@ def run_ours(args, rank, world, local_rank):
             sh_states = torch.empty((n_shards, N, Hq, 130), dtype=torch.float32, device=dev)
             m_ids = torch.empty_like(sel_ids)
             m_cnt = torch.empty_like(sel_count)
+            out_sh = torch.empty_like(out)
             parts = []
             for i in range(n_shards):
                 lo_t, hi_t = cuts[i], cuts[i + 1]
@@ -390,7 +393,7 @@ def run_ours(args, rank, world, local_rank):
             calls_s = ([shard_score(i) for i in range(n_shards)] +
                        [lambda: s5.step5_merge_topk(geom, sh_ids, sh_sc, sh_cnt, m_ids, m_cnt)] +
                        [shard_attn(i) for i in range(n_shards)] +
-                       [lambda: s5.step5_attn_combine(geom, sh_states, out)])
+                       [lambda: s5.step5_attn_combine(geom, sh_states, out_sh)])
             for _ in range(warmup):
                 for fn in calls_s:
                     fn()
@@ -407,44 +410,51 @@ def run_ours(args, rank, world, local_rank):
                 "combine_us": round(float(ts[-1]), 2),
                 "per_gpu_critical_path_us": round(float(sc_us.max() + ts[n_shards] + at_us.max() + ts[-1]), 2),
                 "picks_equal_whole_row": bool(torch.equal(m_ids, sel_ids) and torch.equal(m_cnt, sel_count)),
+                "out_max_abs_diff_vs_whole_row": float((out_sh.float() - out.float()).abs().max()),
                 "how": "calls timed one by one on one GPU; critical path = slowest shard's score + merge + "
                        "slowest shard's attention + combine, without the exchange between GPUs"}
             del parts
             torch.cuda.empty_cache()
 
-        # end to end through the C ABI with host buffers: the rows' inputs copied in from
-        # pinned memory and the output copied back, every step
-        names = ("q", "idx_q", "w", "row_seq", "row_pos")
-        host = {k: torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True) for k in names}
-        for k in names:
-            host[k].copy_(t[k].cpu())
-        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        h2d = sum(host[k].numel() * host[k].element_size() for k in names)
-        d2h = out_host.numel() * out_host.element_size()
+        # end to end through the C ABI with host buffers: step5_decode_step_host copies the
+        # step's per-row inputs (packed in one page-locked buffer: q, indexer q, weights,
+        # rows' sequences and positions, the summarised region ranges) to the device, runs
+        # the step and copies the output back to page-locked memory, every step
+        rows = s5.HostRows(geom, N, w.B, device=dev)
+        for src, name in (("q", "q"), ("idx_q", "idx_q"), ("w", "w"), ("row_seq", "row_seq"),
+                          ("row_pos", "row_pos"), ("sum_begin", "region_begin"), ("sum_end", "region_end")):
+            rows.view(name).copy_(t[src].cpu())
+        h2d, d2h = rows.h2d_bytes, rows.d2h_bytes
+
+        def step_host():
+            s5.step5_decode_step_host(geom, t, ws, rows, sel_ids, sel_count, max_regions_per_seq=span)
+
+        for _ in range(warmup):
+            step_host()
+        torch.cuda.synchronize()
+        assert torch.equal(rows.out_host.view(torch.int16), out.cpu().view(torch.int16))
         ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
         barrier()
         for i in range(steps):
             flush.zero_()
             ev2[i][0].record(stream)
-            for k in names:
-                t[k].copy_(host[k], non_blocking=True)
-            step()
-            out_host.copy_(out, non_blocking=True)
+            step_host()
             ev2[i][1].record(stream)
         barrier()
         e2e_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev2]))
-        # the same with the step replayed from its CUDA graph
+        # the same call captured once in a CUDA graph (copies and kernels) and replayed
+        g_host = capture(step_host)
+        for _ in range(warmup):
+            g_host.replay()
         barrier()
         for i in range(steps):
             flush.zero_()
             ev2[i][0].record(stream)
-            for k in names:
-                t[k].copy_(host[k], non_blocking=True)
-            g_step.replay()
-            out_host.copy_(out, non_blocking=True)
+            g_host.replay()
             ev2[i][1].record(stream)
         barrier()
         e2e_graph_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev2]))
+        assert s5.step5_device_status() == 0
         e2e_ms, e2e_graph_ms = max_over_ranks([e2e_ms, e2e_graph_ms], dist, dev)
         res.update(e2e_ms=e2e_ms, e2e_graph_ms=e2e_graph_ms, h2d=h2d, d2h=d2h)
         del t, flush
@@ -485,7 +495,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(rows / (head["e2e_ms"] / 1e3), 2), "unit": UNIT,
                 "ms_per_step": round(head["e2e_ms"], 5), "h2d_bytes_per_step": head["h2d"],
                 "d2h_bytes_per_step": head["d2h"],
-                "how": "pinned host inputs copied in, step5_decode_step (one C-ABI call) issued eagerly, output copied out",
+                "how": "step5_decode_step_host (one C-ABI call, issued eagerly): the step's per-row inputs "
+                       "copied from one page-locked buffer, the step, the output copied to page-locked memory",
                 "graph_value": round(rows / (head["e2e_graph_ms"] / 1e3), 2),
                 "graph_ms_per_step": round(head["e2e_graph_ms"], 5)},
         "gpu_launches": head["launches"],

@@ -31,6 +31,7 @@ __all__ = [
     "step5_indexer_front",
     "step5_index_score_topk_noalloc",
     "step5_index_score_topk_shard", "step5_merge_topk", "step5_sparse_attn_shard", "step5_attn_combine",
+    "RowsLayout", "step5_rows_layout_for", "HostRows", "step5_decode_step_host",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
     "step5_set_select_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
     "Workspace", "decode_step",
@@ -106,6 +107,9 @@ def load():
         "step5_merge_topk": (i32, [G, i32, i32, P, P, P, P, P, P, P]),
         "step5_sparse_attn_shard": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]),
         "step5_attn_combine": (i32, [G, i32, i32, P, P, P, P]),
+        "step5_rows_layout_for": (i32, [G, i32, i32, ctypes.POINTER(RowsLayout)]),
+        "step5_decode_step_host": (i32, [G, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                         P, sz, P]),
         "step5_workspace_bytes": (sz, [G, i32, i32]),
         "step5_workspace_init": (i32, [P, sz, P]),
         "step5_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32), P]),
@@ -327,6 +331,78 @@ def step5_decode_step(geom, t: dict, ws, sel_ids, sel_count, out, max_regions_pe
         _ptr(t["sum_end"]), _ptr(t["summaries"]), _ptr(t["idx_q"]), _ptr(t["w"]), _ptr(t["row_seq"]),
         _ptr(t["row_pos"]), _ptr(t["q"]), _ptr(t["k_cache"]), _ptr(t["v_cache"]), _ptr(sel_ids),
         _ptr(sel_count), _ptr(out), _ptr(ws_t), ws_bytes, _stream(stream)))
+
+
+class RowsLayout(ctypes.Structure):
+    """Byte offsets of a step's per-row inputs packed in one buffer (step5_rows_layout_for)."""
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("q", "idx_q", "w", "row_seq", "row_pos", "region_begin", "region_end", "total")]
+
+
+def step5_rows_layout_for(geom, N: int, B: int) -> RowsLayout:
+    lay = RowsLayout()
+    _check("step5_rows_layout_for", load().step5_rows_layout_for(ctypes.byref(Geometry.of(geom)), N, B,
+                                                                 ctypes.byref(lay)))
+    return lay
+
+
+class HostRows:
+    """A decode step's per-row inputs packed in one page-locked host buffer (filled by the
+    caller through ``view``) and its device copy, plus the page-locked output; the buffers
+    that step5_decode_step_host takes."""
+
+    def __init__(self, geom, N: int, B: int, device="cuda"):
+        g = Geometry.of(geom)
+        self.N, self.B = N, B
+        self.layout = step5_rows_layout_for(geom, N, B)
+        self.host = torch.zeros(self.layout.total, dtype=torch.uint8, pin_memory=True)
+        self.dev = torch.zeros(self.layout.total, dtype=torch.uint8, device=device)
+        self.out_host = torch.zeros((N, g.num_q_heads, g.head_dim), dtype=torch.bfloat16, pin_memory=True)
+        self.out_dev = torch.zeros((N, g.num_q_heads, g.head_dim), dtype=torch.bfloat16, device=device)
+        self._shapes = {"q": ((N, g.num_q_heads, g.head_dim), torch.bfloat16),
+                        "idx_q": ((N, g.idx_heads, g.idx_dim), torch.bfloat16),
+                        "w": ((N, g.idx_heads), torch.float32), "row_seq": ((N,), torch.int32),
+                        "row_pos": ((N,), torch.int32), "region_begin": ((B,), torch.int32),
+                        "region_end": ((B,), torch.int32)}
+
+    def view(self, name: str, on_device: bool = False) -> torch.Tensor:
+        """The array ``name`` of the packed buffer (host, or its device copy)."""
+        shape, dtype = self._shapes[name]
+        off = getattr(self.layout, name)
+        nbytes = math.prod(shape) * torch.tensor([], dtype=dtype).element_size()
+        buf = self.dev if on_device else self.host
+        return buf[off:off + nbytes].view(dtype).view(shape)
+
+    @property
+    def h2d_bytes(self) -> int:
+        return int(self.layout.total)
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.out_host.numel() * self.out_host.element_size()
+
+
+def _hptr(t: torch.Tensor):
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError("host buffers passed to libstep5sa must be contiguous CPU tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def step5_decode_step_host(geom, t: dict, ws, rows: HostRows, sel_ids, sel_count, max_regions_per_seq,
+                           stream=None):
+    """The whole step from host inputs to host output in one C-ABI call: rows.host is
+    copied to rows.dev, the step runs over it and the device caches, summaries and
+    tables of ``t``, and the output lands in rows.out_host (valid after the stream
+    reaches the end of the call's work)."""
+    B, G, t_cap, _ = t["idx_k"].shape
+    r_cap = t["summaries"].shape[2]
+    ws_t = None if ws is None else (ws.tensor if isinstance(ws, Workspace) else ws)
+    ws_bytes = 0 if ws_t is None else ws_t.numel() * ws_t.element_size()
+    _check("step5_decode_step_host", load().step5_decode_step_host(
+        ctypes.byref(Geometry.of(geom)), rows.N, B, t_cap, r_cap, int(max_regions_per_seq),
+        _ptr(t["idx_k"]), _ptr(t["idx_z"]), _ptr(t["cos"]), _ptr(t["sin"]), _ptr(t["summaries"]),
+        _ptr(t["k_cache"]), _ptr(t["v_cache"]), _hptr(rows.host), _ptr(rows.dev), _hptr(rows.out_host),
+        _ptr(rows.out_dev), _ptr(sel_ids), _ptr(sel_count), _ptr(ws_t), ws_bytes, _stream(stream)))
 
 
 @dataclass

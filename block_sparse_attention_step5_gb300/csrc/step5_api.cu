@@ -703,4 +703,68 @@ step5_status step5_decode_step(const step5_geometry* geom, int32_t N, int32_t B,
                      out_bf16, workspace, workspace_bytes, stream, true);
 }
 
+step5_status step5_rows_layout_for(const step5_geometry* geom, int32_t N, int32_t B, step5_rows_layout* layout) {
+    step5_status s = check_geometry(geom);
+    if (s != STEP5_OK) return s;
+    if (N <= 0 || B <= 0 || layout == nullptr) return STEP5_ERR_INVALID_ARGUMENT;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    size_t at = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = at;
+        at += up(bytes);
+        return o;
+    };
+    layout->q = take((size_t)N * geom->num_q_heads * geom->head_dim * 2);
+    layout->idx_q = take((size_t)N * geom->idx_heads * geom->idx_dim * 2);
+    layout->w = take((size_t)N * geom->idx_heads * 4);
+    layout->row_seq = take((size_t)N * 4);
+    layout->row_pos = take((size_t)N * 4);
+    layout->region_begin = take((size_t)B * 4);
+    layout->region_end = take((size_t)B * 4);
+    layout->total = at;
+    return STEP5_OK;
+}
+
+step5_status step5_decode_step_host(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
+                                    int32_t max_regions_per_seq, const void* idx_k_bf16, const void* idx_z_bf16,
+                                    const void* rope_cos_bf16, const void* rope_sin_bf16, uint8_t* summaries_e4m3,
+                                    const void* k_cache_bf16, const void* v_cache_bf16, const void* rows_host,
+                                    void* rows_dev, void* out_host, void* out_dev, int32_t* sel_ids,
+                                    int32_t* sel_count, void* workspace, size_t workspace_bytes,
+                                    step5_stream_t stream) {
+    step5_rows_layout L;
+    step5_status s = step5_rows_layout_for(geom, N, B, &L);
+    if (s != STEP5_OK) return s;
+    if (!rows_host || !rows_dev || !out_host || !out_dev || !aligned16(rows_dev)) return STEP5_ERR_INVALID_ARGUMENT;
+    uint8_t* d = static_cast<uint8_t*>(rows_dev);
+    const void* q = d + L.q;
+    const void* idx_q = d + L.idx_q;
+    const float* w = reinterpret_cast<const float*>(d + L.w);
+    const int32_t* row_seq = reinterpret_cast<const int32_t*>(d + L.row_seq);
+    const int32_t* row_pos = reinterpret_cast<const int32_t*>(d + L.row_pos);
+    const int32_t* rb = reinterpret_cast<const int32_t*>(d + L.region_begin);
+    const int32_t* re = reinterpret_cast<const int32_t*>(d + L.region_end);
+    // every argument is checked before anything is enqueued
+    s = summarize_impl(geom, B, t_cap, r_cap, max_regions_per_seq, idx_k_bf16, idx_z_bf16, rope_cos_bf16,
+                       rope_sin_bf16, rb, re, summaries_e4m3, nullptr, stream, false);
+    if (s != STEP5_OK) return s;
+    s = score_impl(geom, N, B, t_cap, r_cap, idx_q, w, row_seq, row_pos, rope_cos_bf16, rope_sin_bf16,
+                   summaries_e4m3, sel_ids, sel_count, nullptr, nullptr, workspace, workspace_bytes, stream, 0,
+                   nullptr, nullptr, false);
+    if (s != STEP5_OK) return s;
+    s = attn_impl(geom, N, B, t_cap, q, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count, out_dev,
+                  workspace, workspace_bytes, stream, false);
+    if (s != STEP5_OK) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(rows_dev, rows_host, L.total, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return STEP5_ERR_CUDA;
+    s = step5_decode_step(geom, N, B, t_cap, r_cap, max_regions_per_seq, idx_k_bf16, idx_z_bf16, rope_cos_bf16,
+                          rope_sin_bf16, rb, re, summaries_e4m3, idx_q, w, row_seq, row_pos, q, k_cache_bf16,
+                          v_cache_bf16, sel_ids, sel_count, out_dev, workspace, workspace_bytes, stream);
+    if (s != STEP5_OK) return s;
+    const size_t out_bytes = (size_t)N * geom->num_q_heads * geom->head_dim * 2;
+    return cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess ? STEP5_OK
+                                                                                                   : STEP5_ERR_CUDA;
+}
+
 }  // extern "C"

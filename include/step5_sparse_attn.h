@@ -302,6 +302,39 @@ step5_status step5_decode_step(const step5_geometry* geom, int32_t N, int32_t B,
                                int32_t* sel_count, void* out_bf16, void* workspace, size_t workspace_bytes,
                                step5_stream_t stream);
 
+/* Byte offsets of a decode step's per-row inputs packed in one buffer (no counterpart in
+ * the pages: the host-side form of step5_decode_step's inputs, so that a step needs one
+ * host-to-device copy).  Each array starts on a 256-byte boundary, in this order:
+ *   q [N][num_q_heads][head_dim] bf16, idx_q [N][idx_heads][idx_dim] bf16,
+ *   w [N][idx_heads] fp32, row_seq [N] int32, row_pos [N] int32,
+ *   region_begin [B] int32, region_end [B] int32;
+ * total = the buffer's size in bytes. */
+typedef struct {
+    size_t q, idx_q, w, row_seq, row_pos, region_begin, region_end, total;
+} step5_rows_layout;
+
+/* Fills *layout for N rows and B sequences.  STEP5_ERR_INVALID_ARGUMENT for N or B <= 0
+ * or a NULL layout; geometry errors as elsewhere. */
+step5_status step5_rows_layout_for(const step5_geometry* geom, int32_t N, int32_t B, step5_rows_layout* layout);
+
+/* step5_decode_step with its per-row inputs and its output in HOST memory: enqueues the
+ * copy of rows_host (laid out by step5_rows_layout_for, layout.total bytes) into rows_dev,
+ * the step over rows_dev's arrays, and the copy of out_dev ([N][num_q_heads][head_dim]
+ * bf16) into out_host.  rows_host and out_host are host pointers, page-locked for the
+ * copies to be asynchronous (pageable memory works, with the runtime's synchronous copy
+ * rules); rows_dev (16-byte aligned, layout.total bytes) and out_dev are device buffers
+ * owned by the caller.  The caches, rope tables, summaries, sel_ids, sel_count and the
+ * workspace are device-resident as for step5_decode_step.  Every argument is checked
+ * before anything is enqueued; results and errors are step5_decode_step's.  out_host is
+ * valid once `stream` has reached the end of the call's work. */
+step5_status step5_decode_step_host(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
+                                    int32_t max_regions_per_seq, const void* idx_k_bf16, const void* idx_z_bf16,
+                                    const void* rope_cos_bf16, const void* rope_sin_bf16, uint8_t* summaries_e4m3,
+                                    const void* k_cache_bf16, const void* v_cache_bf16, const void* rows_host,
+                                    void* rows_dev, void* out_host, void* out_dev, int32_t* sel_ids,
+                                    int32_t* sel_count, void* workspace, size_t workspace_bytes,
+                                    step5_stream_t stream);
+
 /* Bytes of device workspace that step5_index_score_topk and step5_sparse_attn need for
  * N rows and r_cap summary slots (one buffer serves both: step (4)'s part comes first
  * and depends on the geometry and N only).  Returns 0 for an unsupported geometry. */

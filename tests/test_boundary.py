@@ -158,6 +158,31 @@ def test_shard_call_rejections(s5):
     assert lib.step5_attn_combine(ctypes.byref(g), 2, 1, fake, None, odd, None) == 1
 
 
+def test_rows_layout_and_host_step_rejections(s5):
+    """The packed per-row input layout (256-byte aligned arrays in the documented order,
+    no overlap) and the host-buffer step's argument checks."""
+    lib = s5.load()
+    g = s5.STEP5_GEOMETRY
+    for N, B in ((1, 1), (16, 16), (2048, 1), (3, 7)):
+        lay = s5.step5_rows_layout_for(g, N, B)
+        sizes = [N * g.num_q_heads * g.head_dim * 2, N * g.idx_heads * g.idx_dim * 2, N * g.idx_heads * 4,
+                 N * 4, N * 4, B * 4, B * 4]
+        offs = [lay.q, lay.idx_q, lay.w, lay.row_seq, lay.row_pos, lay.region_begin, lay.region_end, lay.total]
+        assert offs[0] == 0
+        for i, size in enumerate(sizes):
+            assert offs[i] % 256 == 0 and offs[i] + size <= offs[i + 1] < offs[i] + size + 256
+    with pytest.raises(s5.Step5Error):
+        s5.step5_rows_layout_for(g, 0, 1)
+    G_ = ctypes.byref(G())
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    args = lambda rows_host, rows_dev, out_host: (G_, 1, 1, 64, 8, 1, fake, fake, None, None, fake, fake, fake,
+                                                  rows_host, rows_dev, out_host, fake, fake, fake, None, 0, None)
+    assert lib.step5_decode_step_host(*args(None, fake, fake)) == 1
+    assert lib.step5_decode_step_host(*args(fake, odd, fake)) == 1
+    assert lib.step5_decode_step_host(*args(fake, fake, None)) == 1
+
+
 def test_status_strings(s5):
     for code in range(6):
         assert isinstance(s5.step5_status_string(code), str)
