@@ -31,7 +31,7 @@ __all__ = [
     "step5_indexer_front",
     "step5_index_score_topk_noalloc",
     "step5_index_score_topk_shard", "step5_merge_topk", "step5_sparse_attn_shard", "step5_attn_combine",
-    "RowsLayout", "step5_rows_layout_for", "HostRows", "step5_decode_step_host",
+    "RowsLayout", "step5_rows_layout_for", "HostRows", "step5_decode_step_host", "step5_set_host_copies",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
     "step5_set_select_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
     "Workspace", "decode_step",
@@ -115,6 +115,7 @@ def load():
         "step5_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32), P]),
         "step5_set_select_path": (i32, [i32]),
         "step5_set_prologue_overlap": (i32, [i32]),
+        "step5_set_host_copies": (i32, [i32]),
         "step5_select_path_for": (i32, [G, i32, i32]),
         "step5_status_string": (ctypes.c_char_p, [i32]),
         "step5_convert_bf16_to_e4m3": (i32, [P, P, i64, P]),
@@ -160,6 +161,12 @@ def step5_set_prologue_overlap(enable: int) -> int:
     """1 = the scoring kernel reads its non-summary inputs before waiting for the launch
     before it (which must not write them); 0 = every read waits.  Returns the previous."""
     return load().step5_set_prologue_overlap(enable)
+
+
+def step5_set_host_copies(always: int) -> int:
+    """1: step5_decode_step_host always copies its host buffers; 0 (default): in place
+    when they are device-addressable page-locked memory.  Returns the previous value."""
+    return load().step5_set_host_copies(int(always))
 
 
 def step5_select_path_for(geom, N: int, r_cap: int) -> int:
@@ -390,10 +397,10 @@ def _hptr(t: torch.Tensor):
 
 def step5_decode_step_host(geom, t: dict, ws, rows: HostRows, sel_ids, sel_count, max_regions_per_seq,
                            stream=None):
-    """The whole step from host inputs to host output in one C-ABI call: rows.host is
-    copied to rows.dev, the step runs over it and the device caches, summaries and
-    tables of ``t``, and the output lands in rows.out_host (valid after the stream
-    reaches the end of the call's work)."""
+    """The whole step from host inputs to host output in one C-ABI call: the step runs
+    over rows.host's arrays (in place when the device can address them, else copied to
+    rows.dev) and the device caches, summaries and tables of ``t``; the output lands in
+    rows.out_host (valid after the stream reaches the end of the call's work)."""
     B, G, t_cap, _ = t["idx_k"].shape
     r_cap = t["summaries"].shape[2]
     ws_t = None if ws is None else (ws.tensor if isinstance(ws, Workspace) else ws)

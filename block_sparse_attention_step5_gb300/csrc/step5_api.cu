@@ -19,6 +19,7 @@ __device__ uint32_t g_status_word;
 
 int32_t g_select_path = 0;  // 0 auto, 1 fused, 2 split
 int32_t g_overlap_prologue = 0;
+int32_t g_host_copies = 0;  // step5_decode_step_host: 1 = always through copies
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -280,6 +281,12 @@ const char* step5_status_string(step5_status s) {
         case STEP5_ERR_TIMEOUT: return "device wait timed out";
     }
     return "unknown status";
+}
+
+int32_t step5_set_host_copies(int32_t always) {
+    const int32_t prev = g_host_copies;
+    if (always == 0 || always == 1) g_host_copies = always;
+    return prev;
 }
 
 int32_t step5_set_prologue_overlap(int32_t enable) {
@@ -736,7 +743,21 @@ step5_status step5_decode_step_host(const step5_geometry* geom, int32_t N, int32
     step5_status s = step5_rows_layout_for(geom, N, B, &L);
     if (s != STEP5_OK) return s;
     if (!rows_host || !rows_dev || !out_host || !out_dev || !aligned16(rows_dev)) return STEP5_ERR_INVALID_ARGUMENT;
-    uint8_t* d = static_cast<uint8_t*>(rows_dev);
+    // Page-locked host buffers that the device can address (unified addressing; on
+    // Grace, over NVLink-C2C) are read and written by the step's kernels in place: no
+    // copy operations.  Otherwise (or with step5_set_host_copies(1)) the inputs are
+    // copied into rows_dev and the output out of out_dev.
+    void* rows_map = nullptr;
+    void* out_map = nullptr;
+    bool mapped = false;
+    if (!g_host_copies) {
+        mapped = cudaHostGetDevicePointer(&rows_map, const_cast<void*>(rows_host), 0) == cudaSuccess &&
+                 cudaHostGetDevicePointer(&out_map, out_host, 0) == cudaSuccess && aligned16(rows_map) &&
+                 aligned16(out_map);
+        if (!mapped) (void)cudaGetLastError();  // a refused lookup leaves no error behind
+    }
+    uint8_t* d = static_cast<uint8_t*>(mapped ? rows_map : rows_dev);
+    void* out = mapped ? out_map : out_dev;
     const void* q = d + L.q;
     const void* idx_q = d + L.idx_q;
     const float* w = reinterpret_cast<const float*>(d + L.w);
@@ -752,16 +773,16 @@ step5_status step5_decode_step_host(const step5_geometry* geom, int32_t N, int32
                    summaries_e4m3, sel_ids, sel_count, nullptr, nullptr, workspace, workspace_bytes, stream, 0,
                    nullptr, nullptr, false);
     if (s != STEP5_OK) return s;
-    s = attn_impl(geom, N, B, t_cap, q, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count, out_dev,
+    s = attn_impl(geom, N, B, t_cap, q, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count, out,
                   workspace, workspace_bytes, stream, false);
     if (s != STEP5_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
-    if (cudaMemcpyAsync(rows_dev, rows_host, L.total, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    if (!mapped && cudaMemcpyAsync(rows_dev, rows_host, L.total, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return STEP5_ERR_CUDA;
     s = step5_decode_step(geom, N, B, t_cap, r_cap, max_regions_per_seq, idx_k_bf16, idx_z_bf16, rope_cos_bf16,
                           rope_sin_bf16, rb, re, summaries_e4m3, idx_q, w, row_seq, row_pos, q, k_cache_bf16,
-                          v_cache_bf16, sel_ids, sel_count, out_dev, workspace, workspace_bytes, stream);
-    if (s != STEP5_OK) return s;
+                          v_cache_bf16, sel_ids, sel_count, out, workspace, workspace_bytes, stream);
+    if (s != STEP5_OK || mapped) return s;
     const size_t out_bytes = (size_t)N * geom->num_q_heads * geom->head_dim * 2;
     return cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess ? STEP5_OK
                                                                                                    : STEP5_ERR_CUDA;

@@ -317,16 +317,23 @@ typedef struct {
  * or a NULL layout; geometry errors as elsewhere. */
 step5_status step5_rows_layout_for(const step5_geometry* geom, int32_t N, int32_t B, step5_rows_layout* layout);
 
-/* step5_decode_step with its per-row inputs and its output in HOST memory: enqueues the
- * copy of rows_host (laid out by step5_rows_layout_for, layout.total bytes) into rows_dev,
- * the step over rows_dev's arrays, and the copy of out_dev ([N][num_q_heads][head_dim]
- * bf16) into out_host.  rows_host and out_host are host pointers, page-locked for the
- * copies to be asynchronous (pageable memory works, with the runtime's synchronous copy
- * rules); rows_dev (16-byte aligned, layout.total bytes) and out_dev are device buffers
- * owned by the caller.  The caches, rope tables, summaries, sel_ids, sel_count and the
- * workspace are device-resident as for step5_decode_step.  Every argument is checked
- * before anything is enqueued; results and errors are step5_decode_step's.  out_host is
- * valid once `stream` has reached the end of the call's work. */
+/* step5_decode_step with its per-row inputs and its output in HOST memory: rows_host
+ * (laid out by step5_rows_layout_for, layout.total bytes) holds the step's per-row
+ * inputs and out_host ([N][num_q_heads][head_dim] bf16) receives its output.
+ *  - When both are page-locked allocations that the device can address (cudaHostAlloc /
+ *    cudaMallocHost memory under unified addressing; on Grace, over NVLink-C2C), the
+ *    step's kernels read the inputs from rows_host and write the output into out_host in
+ *    place: no copy operation is enqueued and rows_dev / out_dev are not touched.
+ *  - Otherwise (or after step5_set_host_copies(1)) the call enqueues the copy of
+ *    rows_host into rows_dev, the step over rows_dev's arrays and the copy of out_dev into
+ *    out_host (pageable host memory works, under the runtime's synchronous-copy rules).
+ * rows_dev (16-byte aligned, layout.total bytes) and out_dev are device buffers owned by
+ * the caller, required in both cases.  The caches, rope tables, summaries, sel_ids,
+ * sel_count and the workspace are device-resident as for step5_decode_step.  Every
+ * argument is checked before anything is enqueued; results and errors are
+ * step5_decode_step's, bit for bit the same in both modes.  rows_host must stay
+ * unchanged, and out_host is valid, once `stream` has reached the end of the call's
+ * work. */
 step5_status step5_decode_step_host(const step5_geometry* geom, int32_t N, int32_t B, int32_t t_cap, int32_t r_cap,
                                     int32_t max_regions_per_seq, const void* idx_k_bf16, const void* idx_z_bf16,
                                     const void* rope_cos_bf16, const void* rope_sin_bf16, uint8_t* summaries_e4m3,
@@ -370,6 +377,11 @@ int32_t step5_set_select_path(int32_t mode);
  * waits.  Process-wide, read when a call is enqueued; values other than 0 and 1 are
  * ignored.  Returns the previous value. */
 int32_t step5_set_prologue_overlap(int32_t enable);
+
+/* step5_decode_step_host's host-buffer access: 0 (default) = in place when the host
+ * buffers are device-addressable page-locked memory, else through copies; 1 = always
+ * through copies.  Process-wide; other values are ignored.  Returns the previous value. */
+int32_t step5_set_host_copies(int32_t always);
 
 /* The selection path step5_index_score_topk takes for this geometry, N and r_cap under
  * the current step5_set_select_path setting: 1 (fused: one block per (row, group)) or 2

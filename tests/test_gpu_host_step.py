@@ -1,6 +1,7 @@
 """GPU: the whole step from host inputs to host output (step5_decode_step_host) gives
 the same selection and output, bit for bit, as step5_decode_step on the same inputs in
-device memory, eagerly and replayed from a CUDA graph."""
+device memory, eagerly and replayed from a CUDA graph, with the page-locked host buffers
+read and written in place by the kernels and through copies."""
 import pytest
 import torch
 
@@ -18,8 +19,9 @@ def s5():
     return s5
 
 
+@pytest.mark.parametrize("copies", [0, 1])
 @pytest.mark.parametrize("cfg", [0, {"positions": [30000, 4100, 70, 15], "B": 2}, 1])
-def test_host_step_equals_device_step(s5, cfg):
+def test_host_step_equals_device_step(s5, cfg, copies):
     geom = s5.STEP5_GEOMETRY
     w = S.workload(cfg, seed=89)
     t = S.materialize(w, device="cuda")
@@ -49,7 +51,11 @@ def test_host_step_equals_device_step(s5, cfg):
     cnt_h = torch.full_like(cnt_d, -7)
 
     def call():
-        s5.step5_decode_step_host(geom, t, ws2, rows, ids_h, cnt_h, max_regions_per_seq=w.max_span)
+        prev = s5.step5_set_host_copies(copies)
+        try:
+            s5.step5_decode_step_host(geom, t, ws2, rows, ids_h, cnt_h, max_regions_per_seq=w.max_span)
+        finally:
+            s5.step5_set_host_copies(prev)
 
     call()
     torch.cuda.synchronize()
@@ -57,6 +63,10 @@ def test_host_step_equals_device_step(s5, cfg):
     assert torch.equal(ids_h, ids_d) and torch.equal(cnt_h, cnt_d)
     assert torch.equal(t["summaries"], summ_d)
     assert torch.equal(rows.out_host.view(torch.int16), out_d.cpu().view(torch.int16))
+    # in place: the device staging buffers were not used (page-locked memory is
+    # device-addressable here); through copies: they hold the inputs and the output
+    assert bool(rows.dev.any()) == bool(copies)
+    assert bool(rows.out_dev.view(torch.int16).any()) == bool(copies)
     # replayed from a graph, from fresh host values
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, capture_error_mode="thread_local"):
