@@ -154,20 +154,27 @@ struct AttnParams {
     const int32_t* row_pos;
     const int32_t* sel_ids;  // [N][G][top_k]
     const int32_t* sel_count;
-    uint16_t* out;           // [N][Hq][128]
+    union {
+        uint16_t* out;       // the whole row: [N][Hq][128] bf16
+        float* states;       // a shard of the rows' tokens: [N][Hq][130] (m, l, o)
+    };
     const uint16_t* gate;    // [N][Hq] bf16 logits of the per-head sigmoid output gate, or null
-    float* states;           // a shard of the rows' tokens: [N][Hq][130] (m, l, o) instead of out
-    int tok_lo;              // the cache's first token (a shard), else 0
     float* part;             // splits > 1: [N*G][splits][hq_g][130] block states
     uint32_t* bar;           // splits > 1: [N*G] epoch of each (row, group)'s state exchange
     uint32_t* flags;         // splits > 1: [N*G][kAttnMaxSplits] epoch + 1 once a block's state is out
     uint32_t* status;
-    int N, B, G, Hq, hq_g, t_cap, top_k;
+    int tok_lo;              // a shard: the cache's first token (else 0); the grid covers the N rows
+    int B, G, Hq, hq_g, t_cap, top_k;
     int splits, entries_per_split;  // blocks per (row, group) and the entries each takes
     float scale_log2;        // softmax_scale * log2(e)
 };
-cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+// (kept at 128 bytes: a larger block measurably slows the prefill launches)
+static_assert(sizeof(AttnParams) == 128, "attention parameter block");
+cudaError_t launch_attention(const AttnParams& p, int N, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream, bool pdl);
+// the shard instantiation (p.states in place of p.out)
+cudaError_t launch_attention_shard(const AttnParams& p, int N, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                   cudaStream_t stream, bool pdl);
 size_t attention_smem_bytes();  // dynamic part
 constexpr size_t kAttnStaticSmem = (kMaxTopK + 2) * 4 + 16384;  // picked ids + merge scratch
 

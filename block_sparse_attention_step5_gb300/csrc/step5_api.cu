@@ -475,7 +475,6 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     const int G = geom->num_kv_groups;
     const uint64_t rows = (uint64_t)B * G * t_cap;
     if (rows > (uint64_t)INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
-    const int hq_g = geom->num_q_heads / G;
     const AttnArea A = attn_area(geom, N);
     const bool use_area = workspace != nullptr && workspace_bytes > 0 && A.end > 0;
     if (use_area && workspace_bytes < A.end) return STEP5_ERR_WORKSPACE;
@@ -493,16 +492,17 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     p.row_pos = row_pos;
     p.sel_ids = sel_ids;
     p.sel_count = sel_count;
-    p.out = static_cast<uint16_t*>(out_bf16);
+    if (states != nullptr)
+        p.states = states;
+    else
+        p.out = static_cast<uint16_t*>(out_bf16);
     p.gate = static_cast<const uint16_t*>(gate_bf16);
-    p.states = states;
     p.tok_lo = tok_lo;
     p.status = st;
-    p.N = N;
     p.B = B;
     p.G = G;
     p.Hq = geom->num_q_heads;
-    p.hq_g = hq_g;
+    p.hq_g = geom->num_q_heads / G;
     p.t_cap = t_cap;
     p.top_k = geom->top_k;
     p.splits = splits;
@@ -512,7 +512,8 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     p.flags = splits > 1 ? reinterpret_cast<uint32_t*>(ws + A.flags) : nullptr;
     p.part = splits > 1 ? reinterpret_cast<float*>(ws + A.part) : nullptr;
     p.scale_log2 = geom->softmax_scale * 1.4426950408889634f;
-    cudaError_t e = launch_attention(p, kmap, vmap, (cudaStream_t)stream, use_pdl());
+    cudaError_t e = states != nullptr ? launch_attention_shard(p, N, kmap, vmap, (cudaStream_t)stream, use_pdl())
+                                      : launch_attention(p, N, kmap, vmap, (cudaStream_t)stream, use_pdl());
     return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
 }
 
