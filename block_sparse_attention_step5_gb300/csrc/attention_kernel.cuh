@@ -534,13 +534,12 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
 template <bool kShard>
 cudaError_t launch_sparse_attn(const AttnParams& p, int N, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t stream, bool pdl) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<kShard>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)attn_smem_bytes());
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_set{0};
+    cudaError_t e = once_per_device(attr_set, [] {
+        return cudaFuncSetAttribute(sparse_attn_kernel<kShard>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)attn_smem_bytes());
+    });
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.splits, p.G, N);
     cfg.blockDim = dim3(kThreads);

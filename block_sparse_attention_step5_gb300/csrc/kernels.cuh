@@ -4,9 +4,26 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace step5 {
+
+// Runs set() once per CUDA device: kernel attributes belong to a device's context, so a
+// process driving several GPUs sets them on each.  `done` holds a bit per device ordinal
+// below 64 (others run set() on every call).
+template <class F>
+cudaError_t once_per_device(std::atomic<uint64_t>& done, F&& set) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = set();
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // ----------------------------------------------------------------- step (1)
 struct SummarizeParams {

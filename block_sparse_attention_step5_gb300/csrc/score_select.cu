@@ -1416,17 +1416,18 @@ template <int HPG>
 cudaError_t split_for(const ScoreParams& p_in, const CUtensorMap& smap, cudaStream_t stream, bool pdl) {
     // one persistent launch with every block resident: one block per SM, at most one per
     // tile
-    static int per_sm = 0;
-    if (per_sm == 0) {
-        cudaError_t e0 = cudaFuncSetAttribute(score_select_kernel<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)kScoreSmem);
-        if (e0 != cudaSuccess) return e0;
+    static std::atomic<uint64_t> ready{0};
+    cudaError_t e0 = once_per_device(ready, [] {
+        cudaError_t e = cudaFuncSetAttribute(score_select_kernel<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kScoreSmem);
+        if (e != cudaSuccess) return e;
         int b = 0;
-        e0 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, score_select_kernel<HPG>, kSplitThreads, kScoreSmem);
-        if (e0 != cudaSuccess) return e0;
-        if (b < 1) return cudaErrorInvalidConfiguration;
-        per_sm = 1;
-    }
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, score_select_kernel<HPG>, kSplitThreads, kScoreSmem);
+        if (e != cudaSuccess) return e;
+        return b < 1 ? cudaErrorInvalidConfiguration : cudaSuccess;
+    });
+    if (e0 != cudaSuccess) return e0;
+    const int per_sm = 1;
     // rows in batches small enough that a block's share covers at most kMaxShareSegs
     // (row, group)s
     const int64_t full_grid = (int64_t)per_sm * p_in.num_sms;

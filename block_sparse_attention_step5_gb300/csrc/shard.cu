@@ -121,13 +121,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)((size_t)kMaxShardKeys * 8));
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    cudaError_t e = once_per_device(attr, [] {
+        return cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)((size_t)kMaxShardKeys * 8));
+    });
+    if (e != cudaSuccess) return e;
     merge_kernel<<<p.NG, kMergeThreads, (size_t)p.S * p.top_k * 8, stream>>>(p);
     return cudaGetLastError();
 }

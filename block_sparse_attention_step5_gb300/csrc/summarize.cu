@@ -57,13 +57,12 @@ __global__ void convert_kernel(const uint16_t* in, uint8_t* out, int64_t n) {
 cudaError_t launch_summarize(const SummarizeParams& p, int B, cudaStream_t stream) {
     // the SM's shared-memory split of the scoring kernel that follows, so that blocks of
     // both fit on one SM without the SM first draining to change it
-    static bool carveout_set = false;
-    if (!carveout_set) {
-        cudaError_t e = cudaFuncSetAttribute(summarize_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                             (int)cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        carveout_set = true;
-    }
+    static std::atomic<uint64_t> carveout_set{0};
+    cudaError_t e = once_per_device(carveout_set, [] {
+        return cudaFuncSetAttribute(summarize_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    (int)cudaSharedmemCarveoutMaxShared);
+    });
+    if (e != cudaSuccess) return e;
     dim3 grid((p.max_span + kRegionsPerCta - 1) / kRegionsPerCta, p.G, B);
     summarize_kernel<<<grid, kSumThreads, 0, stream>>>(p);
     return cudaGetLastError();
