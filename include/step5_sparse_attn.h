@@ -155,7 +155,8 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
  * scratch after the ~2 MiB any workspace keeps for step5_sparse_attn; one array per
  * device that loads the library, held until the process exits).  It allocates nothing.
  *  - Limit: step5_workspace_bytes(geom, N, r_cap) must fit the array (for Step-5's
- *    geometry about N * r_cap <= 220,000, e.g. one row at 1M tokens or four at 128K);
+ *    geometry: one row up to ~322,000 summary slots, four up to ~74,000 each, sixteen up
+ *    to ~12,400 each; e.g. one row at 1M tokens or four at 128K);
  *    larger problems return STEP5_ERR_WORKSPACE before anything is enqueued.
  *  - The first call on a device looks up the array's device address (with that device
  *    current); make that first call before any stream capture.
