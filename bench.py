@@ -120,10 +120,15 @@ class ClockSampler:
 
 
 def kernel_source_sha():
+    """sha256 (first 16 hex digits) of the dominant kernel's sources with comments and
+    blank lines removed, so that only a change of code retires a recorded profile."""
     src = os.path.join(ROOT, "block_sparse_attention_step5_gb300", "csrc")
     h = hashlib.sha256()
     for name in ("score_select.cu", "common.cuh", "kernels.cuh"):
-        h.update(open(os.path.join(src, name), "rb").read())
+        text = open(os.path.join(src, name)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.split("\n") if line.strip()).encode())
     return h.hexdigest()[:16]
 
 

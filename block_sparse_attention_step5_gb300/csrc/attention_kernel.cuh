@@ -1,11 +1,11 @@
 // attention_kernel.cuh -- step (4): attention over the picked regions plus the row's own region
 // (and, optionally, the per-head sigmoid output gate that follows it).
 //
-// "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903), CSA-indexer commit:
-// "attention over those regions and the row's own"; below 512 regions every region is
-// read, which is the dense attention it replaces.  The same page's decode kernel splits
-// a row's keys over many workers and merges their online-softmax states in a fixed
-// order ("one simdgroup walking every key alone left decode waiting on loads").
+// "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903), CSA-indexer commit: each row
+// attends to its picked regions plus its own region; with at most 512 regions that is
+// every region, i.e. the dense attention the indexer replaces.  The same page's decode
+// kernel spreads a row's keys over many workers (a single worker per row was
+// load-latency bound) and merges their online-softmax states in a fixed order.
 //
 // Design (sm_103a):
 //  * S blocks per (row, KV group) (S = 1..64, as many as the SMs allow: one SM gathers

@@ -1,9 +1,9 @@
 // score_select.cu -- steps (2) and (3): FP8 index scores and top-k by (-score, id).
 //
-// "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903), CSA-indexer commit: scores
-// sum_h relu(e4m3(q_h) . summary) * w_h per KV group; the top 512 by (-score, id),
-// ascending.  Provider groups own contiguous blocks of indexer heads (vLLM Step5 DSA
-// geometry: "the sparse indexer reduces scores within provider groups").
+// "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903), CSA-indexer commit: a
+// region's score in a KV group is sum_h relu(e4m3(q_h) . summary) * w_h over the group's
+// indexer heads; the 512 smallest (-score, id) keys are kept, in key order.  Provider groups own contiguous blocks of indexer heads (vLLM Step5 DSA
+// geometry: the indexer's scores are summed within each provider group).
 //
 // Scoring runs on the CUDA cores.  With 4 indexer heads per group a thread scores whole
 // regions (two at a time against a shared-memory query broadcast); otherwise each region

@@ -3,13 +3,14 @@
  * the Step-5 full-attention layer's sparse-indexer attention (DSA/CSA).
  *
  * The method is stated in "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903), in
- * the commit that runs StepFun's CSA indexer "for contexts to 1M tokens":
+ * the commit that adds StepFun's CSA indexer so that contexts reach 1M tokens:
  *   (1) every completed 8-token region is summarised, per KV group, as a per-dim
  *       softmax over z of the indexer k, rounded through bf16 to e4m3;
- *   (2) each region is scored as sum_h relu(e4m3(q_h) . summary) * w_h per KV group;
- *   (3) the top 512 regions by (-score, id), ascending, are kept;
- *   (4) attention runs over those regions and the row's own region; below 512 regions
- *       every region is read, which is the dense attention it replaces.
+ *   (2) a region's score in KV group g is sum_h relu(e4m3(q_h) . summary) * w_h over
+ *       g's indexer heads h;
+ *   (3) the 512 regions with the smallest (-score, id) keys are kept, in key order;
+ *   (4) the row attends to those regions and to its own region; a row with at most
+ *       512 candidate regions keeps them all, so its attention is the dense one.
  * The indexer q and k take NEOX rotation on their first 32 dims from bf16 cos/sin (same
  * page, commit on Step-5's glue).  Geometry rules follow the vLLM Step5 model's DSA
  * validation (`_validate_step5_dsa_parallel_geometry`): indexer provider groups equal
@@ -72,8 +73,8 @@ typedef struct {
 } step5_geometry;
 
 /* The indexer's decode front end, ahead of step (1) ("Step-5-Preview on one 256 GB Mac",
- * CSA-indexer commit: "the indexer's q (16 heads, RMSNorm 1 + w), k (LayerNorm with
- * bias) and z").  For every row n (a device [N] of sequences and positions):
+ * CSA-indexer commit: the indexer's 16-head q takes an RMSNorm with weight 1 + w,
+ * its k a LayerNorm with bias, and z stays unnormalised).  For every row n (a device [N] of sequences and positions):
  *   idx_q_out[n][h] = bf16(q_pre[n][h] / sqrt(mean_d q_pre[n][h][d]^2 + eps) * (1 + q_norm_w))
  *   idx_k[b][g][p]  = bf16((k_pre[n][g] - mean) / sqrt(var + eps) * k_norm_w + k_norm_b)
  *   idx_z[b][g][p]  = z_pre[n][g]
@@ -204,7 +205,7 @@ step5_status step5_sparse_attn(const step5_geometry* geom, int32_t N, int32_t B,
                                step5_stream_t stream);
 
 /* Step (4) followed by the per-head sigmoid output gate ("Step-5-Preview on one 256 GB
- * Mac", native-family commit: Step-5's glue keeps "the per-head sigmoid gate" among
+ * Mac", native-family commit: Step-5's glue lists a per-head sigmoid gate among
  * StepFun's rounding points).  As step5_sparse_attn, except that every output dim of
  * query head h of row n is scaled by sigmoid(gate[n][h]) before the output's single
  * bf16 rounding:  out[n][h] = bf16(sigmoid(gate[n][h]) * softmax(...) V).

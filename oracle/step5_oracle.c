@@ -4,7 +4,7 @@
  * TEST INFRASTRUCTURE ONLY (tests, the smoke check and the benchmark's CPU-baseline
  * leg).  No code is shared with the CUDA library.  Every function follows the
  * definition stated in "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903,
- * the commit adding the CSA indexer "for contexts to 1M tokens"), written out in the
+ * the commit adding the CSA indexer for contexts up to 1M tokens), written out in the
  * page's order with no blocking, fusion or reordering.  Compile with
  * -ffp-contract=off so that the arithmetic is the same on every host.
  */

@@ -6,11 +6,11 @@
  * It shares no code, header, table or helper with the CUDA library.
  *
  * Source of the method: "Step-5-Preview on one 256 GB Mac" (TensorFold PR #903),
- * the commit that adds the CSA indexer "for contexts to 1M tokens": every completed
+ * the commit that adds the CSA indexer for contexts up to 1M tokens: every completed
  * 8-token region is summarised as a per-dim softmax over z of the indexer k, rounded
- * through bf16 to e4m3; scores are sum_h relu(e4m3(q_h) . summary) * w_h per KV group;
- * the top 512 regions by (-score, id), ascending, are kept; attention runs over those
- * regions and the row's own region.  The indexer's q and k take NEOX rotation on their
+ * through bf16 to e4m3; a region's score in a KV group is sum_h relu(e4m3(q_h) . summary)
+ * * w_h over the group's indexer heads; the 512 smallest (-score, id) keys are kept in
+ * key order; the row attends to those regions and to its own region.  The indexer's q and k take NEOX rotation on their
  * first 32 dims from bf16 cos/sin (same page, the commit on Step-5's glue).
  *
  * Arithmetic: fp64 everywhere except at the rounding points the page fixes
@@ -38,8 +38,8 @@ double   orc_e4m3_value(uint8_t code);
 void     orc_bf16_codes_to_e4m3_codes(const uint16_t* in, uint8_t* out, int64_t n);
 void     orc_round_bf16_array(const double* in, uint16_t* out_codes, int64_t n);
 
-/* ---- NEOX partial rotation (the page's glue commit: "q/k norm and NEOX rotation from
- *      bf16 cos/sin"; the indexer commit: "NEOX on their first 32 dims") -----------
+/* ---- NEOX partial rotation (the page's glue commit: q and k rotated NEOX-style from
+ *      bf16 cos/sin tables; the indexer commit: the first 32 dims rotate) -----------
  * x: dim bf16 codes.  Pairs (i, i + rope_dims/2) for i < rope_dims/2 rotate by the
  * angle whose bf16 cosine/sine are cos_row[i]/sin_row[i].  Each rotated element is
  * x1*c - x2*s (first half) or x2*c + x1*s (second half), rounded once to bf16.
@@ -48,8 +48,8 @@ void orc_rotate_neox(const uint16_t* x, int dim, int rope_dims,
                      const uint16_t* cos_row, const uint16_t* sin_row, double* out);
 
 /* ---- before step 1: the indexer's q and k norms (decode front end) ------------------
- * ("Step-5-Preview on one 256 GB Mac", CSA-indexer commit: "the indexer's q (16 heads,
- * RMSNorm 1 + w), k (LayerNorm with bias) and z".)  x, w, g, b: dim bf16 codes; fp64
+ * ("Step-5-Preview on one 256 GB Mac", CSA-indexer commit: the indexer's 16-head q
+ * takes an RMSNorm with weight 1 + w, its k a LayerNorm with bias; z is not normalised.)  x, w, g, b: dim bf16 codes; fp64
  * arithmetic, one bf16 rounding of each output.
  *   RMSNorm 1 + w:  y[d] = x[d] / sqrt(mean_d x^2 + eps) * (1 + w[d])
  *   LayerNorm:      y[d] = (x[d] - mean) / sqrt(mean_d (x - mean)^2 + eps) * g[d] + b[d] */
@@ -116,7 +116,7 @@ void orc_attn_combine(int S, int head_dim, const double* m, const double* l, con
 
 /* ---- after step 4: the per-head sigmoid output gate ----------------------------------
  * ("Step-5-Preview on one 256 GB Mac", the native-family commit: Step-5's glue keeps
- * "the per-head sigmoid gate" among StepFun's rounding points.)  Reading: one gate
+ * a per-head sigmoid gate among StepFun's rounding points.)  Reading: one gate
  * logit per (row, query head), a bf16 input; every output dim of the head is scaled by
  * sigmoid(logit) before the output's single bf16 rounding.
  * out: [rows][head_dim] fp64, scaled in place; gate: [rows] bf16 codes.              */

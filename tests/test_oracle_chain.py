@@ -1,7 +1,7 @@
 """The oracle's four steps chained over a small synthetic workload.
 
-Invariant from the CSA-indexer commit: "below 512 regions every region is read,
-which is the dense attention it replaces" -- while a row has at most 512 completed
+Invariant from the CSA-indexer commit: a row with at most 512 candidate regions keeps
+them all, so its attention is the dense one -- while a row has at most 512 completed
 regions the selection is every region (in key order) and the output equals dense
 causal attention (torch SDPA, fp64).  Above 512 regions the chain keeps exactly 512
 ids, each the id of a completed region, none repeated, in non-increasing score order.

@@ -1,5 +1,5 @@
-"""Pins of the oracle's indexer front end (CSA-indexer commit: "the indexer's q (16 heads,
-RMSNorm 1 + w), k (LayerNorm with bias) and z"), by closed forms of the two norms
+"""Pins of the oracle's indexer front end (CSA-indexer commit: the indexer's 16-head q
+takes an RMSNorm with weight 1 + w, its k a LayerNorm with bias), by closed forms of the two norms
 (constant, +-1 and 3-4 inputs, power-of-two scale and shift invariance) and by the
 front end's composition: its caches and summaries are those of the separate steps, and
 a region is summarised exactly when its last token arrives.

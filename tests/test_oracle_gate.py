@@ -1,5 +1,5 @@
 """Pins of the oracle's per-head sigmoid output gate (the step after attention in the
-Step-5 glue: "the per-head sigmoid gate").  Reading: one bf16 logit per (row, query
+Step-5 glue, which lists a per-head sigmoid gate).  Reading: one bf16 logit per (row, query
 head); every output dim of the head is scaled by sigmoid(logit) before the output's one
 bf16 rounding.  Pinned by closed forms: sigmoid(0) = 1/2 exactly, sigmoid(g) +
 sigmoid(-g) = 1, sigmoid(1) = e / (1 + e), saturation at large |g|, and head

@@ -1,7 +1,7 @@
 """Pins of the oracle's NEOX rotation and region summary.
 
-Rotation ("q/k norm and NEOX rotation from bf16 cos/sin", "NEOX on their first 32
-dims"): pairs (i, i + 16), x1' = x1 c - x2 s, x2' = x2 c + x1 s, rounded once to bf16.
+Rotation (the page's glue commit: q and k take NEOX rotation from bf16 cos/sin tables;
+the indexer commit: on their first 32 dims): pairs (i, i + 16), x1' = x1 c - x2 s, x2' = x2 c + x1 s, rounded once to bf16.
 Summary (CSA-indexer commit): s[d] = sum_t softmax_t(z[., d]) rot(k)[t][d], then
 e4m3(bf16(s)).  Pinned by hand-derived golden cases, closed forms and the fp64
 torch.softmax / einsum library path.

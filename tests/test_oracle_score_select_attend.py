@@ -1,9 +1,9 @@
 """Pins of the oracle's score, selection and attention.
 
-Score (CSA-indexer commit): sum_h relu(e4m3(q_h) . summary) * w_h per KV group, the
-group's heads being a contiguous block (provider groups).  Pinned by exact rational
+Score (CSA-indexer commit): sum_h relu(e4m3(q_h) . summary) * w_h over a KV group's
+indexer heads, a contiguous block of them (provider groups).  Pinned by exact rational
 arithmetic, hand-derived golden cases and special cases.
-Selection: the top K by (-score, id), ascending; pinned by Python's sort and golden
+Selection: the K smallest (-score, id) keys, in key order; pinned by Python's sort and golden
 cases.  Attention over the picks plus the row's own region; with every region picked
 it is dense causal attention (torch's scaled_dot_product_attention in fp64 is the
 independent library pin).
