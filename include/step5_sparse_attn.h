@@ -322,10 +322,12 @@ step5_status step5_rows_layout_for(const step5_geometry* geom, int32_t N, int32_
 /* step5_decode_step with its per-row inputs and its output in HOST memory: rows_host
  * (laid out by step5_rows_layout_for, layout.total bytes) holds the step's per-row
  * inputs and out_host ([N][num_q_heads][head_dim] bf16) receives its output.
- *  - When both are page-locked allocations that the device can address (cudaHostAlloc /
- *    cudaMallocHost memory under unified addressing; on Grace, over NVLink-C2C), the
- *    step's kernels read the inputs from rows_host and write the output into out_host in
- *    place: no copy operation is enqueued and rows_dev / out_dev are not touched.
+ *  - When the device can address both (cudaHostGetDevicePointer accepts them:
+ *    cudaHostAlloc / cudaMallocHost memory under unified addressing, and on Grace, where
+ *    NVLink-C2C is coherent and the GPU uses the CPU's page tables, pageable memory too),
+ *    the step's kernels read the inputs from rows_host and write the output into
+ *    out_host in place: no copy operation is enqueued and rows_dev / out_dev are not
+ *    touched.
  *  - Otherwise (or after step5_set_host_copies(1)) the call enqueues the copy of
  *    rows_host into rows_dev, the step over rows_dev's arrays and the copy of out_dev into
  *    out_host (pageable host memory works, under the runtime's synchronous-copy rules).

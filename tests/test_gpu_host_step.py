@@ -88,3 +88,37 @@ def test_host_step_equals_device_step(s5, cfg, copies):
     assert s5.step5_device_status() == 0
     assert (cnt_h.cpu() == 1).all()
     assert not torch.equal(rows.out_host.view(torch.int16), out_d.cpu().view(torch.int16))
+
+
+def test_host_step_with_pageable_buffers(s5):
+    """Pageable host buffers give the same results: where the device can address them
+    (on Grace, through the CPU's page tables) the kernels use them in place, elsewhere
+    the call copies them through the device staging buffers."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [4100, 70], "B": 2}, seed=97)
+    t = S.materialize(w, device="cuda")
+    dev = t["q"].device
+    N, G, K = w.N, geom.num_kv_groups, geom.top_k
+    summ0 = t["summaries"].clone()
+    ws = s5.Workspace.create(geom, N, w.r_cap, device=dev)
+    ids_d = torch.empty((N, G, K), dtype=torch.int32, device=dev)
+    cnt_d = torch.empty((N, G), dtype=torch.int32, device=dev)
+    out_d = torch.empty((N, geom.num_q_heads, geom.head_dim), dtype=torch.bfloat16, device=dev)
+    s5.step5_decode_step(geom, t, ws, ids_d, cnt_d, out_d, max_regions_per_seq=w.max_span)
+    torch.cuda.synchronize()
+    t["summaries"].copy_(summ0)
+    rows = s5.HostRows(geom, N, w.B, device=dev)
+    rows.host = torch.zeros(rows.host.shape, dtype=rows.host.dtype)  # pageable
+    rows.out_host = torch.zeros(rows.out_host.shape, dtype=rows.out_host.dtype)
+    assert not rows.host.is_pinned() and not rows.out_host.is_pinned()
+    for src, name in (("q", "q"), ("idx_q", "idx_q"), ("w", "w"), ("row_seq", "row_seq"), ("row_pos", "row_pos"),
+                      ("sum_begin", "region_begin"), ("sum_end", "region_end")):
+        rows.view(name).copy_(t[src].cpu())
+    ws2 = s5.Workspace.create(geom, N, w.r_cap, device=dev)
+    ids_h = torch.full_like(ids_d, -7)
+    cnt_h = torch.full_like(cnt_d, -7)
+    s5.step5_decode_step_host(geom, t, ws2, rows, ids_h, cnt_h, max_regions_per_seq=w.max_span)
+    torch.cuda.synchronize()
+    assert s5.step5_device_status() == 0
+    assert torch.equal(ids_h, ids_d) and torch.equal(cnt_h, cnt_d)
+    assert torch.equal(rows.out_host.view(torch.int16), out_d.cpu().view(torch.int16))

@@ -189,3 +189,42 @@ def test_merge_clamps_a_bad_count(s5):
     assert s5.step5_device_status() == s5.DEV_RANGE
     assert (m_cnt.cpu() == K).all()
     assert torch.equal(m_ids.cpu(), ids[1].cpu())
+
+
+@pytest.mark.parametrize("S_, K", [(1, 512), (8, 2048), (32, 512)])
+def test_merge_at_its_limits(s5, S_, K):
+    """The merge against the oracle's merge at one shard and at S * top_k = 16,384 keys
+    (the most a merge block stages), with random scores, ties and short lists."""
+    geom = s5.Geometry.step5(top_k=K)
+    G = geom.num_kv_groups
+    dev = torch.device("cuda")
+    rng = np.random.default_rng(101 + S_)
+    N = 2
+    ids = np.full((S_, N, G, K), -1, dtype=np.int32)
+    scs = np.full((S_, N, G, K), -np.inf, dtype=np.float32)
+    cnt = np.zeros((S_, N, G), dtype=np.int32)
+    for s in range(S_):
+        for n in range(N):
+            for g in range(G):
+                c = int(rng.integers(0, K + 1)) if (s + n + g) % 3 else K
+                pool = rng.choice(1 << 20, size=c, replace=False).astype(np.int32) * S_ + s  # distinct across shards
+                sc = np.round(rng.standard_normal(c) * 4).astype(np.float32)  # many exact ties
+                order = np.lexsort((pool, -sc.astype(np.float64)))
+                ids[s, n, g, :c] = pool[order]
+                scs[s, n, g, :c] = sc[order]
+                cnt[s, n, g] = c
+    d_ids, d_scs, d_cnt = (torch.from_numpy(x).to(dev) for x in (ids, scs, cnt))
+    m_ids = torch.full((N, G, K), -7, dtype=torch.int32, device=dev)
+    m_cnt = torch.full((N, G), -7, dtype=torch.int32, device=dev)
+    m_sc = torch.empty((N, G, K), dtype=torch.float32, device=dev)
+    s5.step5_merge_topk(geom, d_ids, d_scs, d_cnt, m_ids, m_cnt, m_sc)
+    torch.cuda.synchronize()
+    assert s5.step5_device_status() == 0
+    got_ids, got_cnt, got_sc = m_ids.cpu().numpy(), m_cnt.cpu().numpy(), m_sc.cpu().numpy()
+    for n in range(N):
+        for g in range(G):
+            ref = oracle.merge_topk(ids[:, n, g], scs[:, n, g], cnt[:, n, g], K)
+            c = int(got_cnt[n, g])
+            assert c == len(ref)
+            assert np.array_equal(got_ids[n, g, :c], ref)
+            assert np.all(got_ids[n, g, c:] == -1) and np.all(np.isneginf(got_sc[n, g, c:]))
