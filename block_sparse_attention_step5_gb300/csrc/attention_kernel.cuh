@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageBytes);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x, g = blockIdx.y, n = blockIdx.z;
+    const int split = blockIdx.x, n = blockIdx.y, g = blockIdx.z;  // group-major (see the launch)
     const int64_t ng = (int64_t)n * p.G + g;
     const int hq_g = p.hq_g;
     const int S = p.splits;
@@ -541,7 +541,9 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int N, const CUtensorMap& km
     });
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.splits, p.G, N);
+    // rows before groups: blocks that run together share one KV group's cache (for a
+    // prefill chunk, 1/G of the K/V it reads), which then stays in L2
+    cfg.gridDim = dim3(p.splits, N, p.G);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = attn_smem_bytes();
     cfg.stream = stream;
