@@ -235,7 +235,10 @@ bool use_pdl() { return true; }
 
 
 // Fused (one block per (row, group), keys in shared memory) when there are many rows or
-// few regions; the histogram split path when a few rows have many regions.
+// few regions; the histogram split path when a few rows have many regions.  Measured on
+// GB300 (eager calls after an L2 flush): one row at 4,001 regions fused 33 us / split
+// 35 us, at 6,001 fused 44 / split 40; four rows at 4,001 fused 35 / split 44, at 8,001
+// fused 52 / split 48; sixteen rows at 2,500-3,842 fused 29-31 / split 40-45.
 bool choose_fused(const step5_geometry* geom, int N, int r_cap) {
     const int G = geom->num_kv_groups;
     const int hpg = geom->idx_heads / G;
@@ -248,7 +251,7 @@ bool choose_fused(const step5_geometry* geom, int N, int r_cap) {
     else if (g_select_path == 2)
         fused = false;
     else
-        fused = (int64_t)N * G >= 128 || r_cap <= 2048;
+        fused = (int64_t)N * G >= 128 || r_cap <= 6144;
     if (r_cap > kFusedMaxRegions || fused_need > 200 * 1024) fused = false;
     return fused;
 }
