@@ -236,9 +236,10 @@ bool use_pdl() { return true; }
 
 // Fused (one block per (row, group), keys in shared memory) when there are many rows or
 // few regions; the histogram split path when a few rows have many regions.  Measured on
-// GB300 (eager calls after an L2 flush): one row at 4,001 regions fused 33 us / split
-// 35 us, at 6,001 fused 44 / split 40; four rows at 4,001 fused 35 / split 44, at 8,001
-// fused 52 / split 48; sixteen rows at 2,500-3,842 fused 29-31 / split 40-45.
+// GB300 (eager calls after an L2 flush, summaries built from k and z): the split path's
+// time grows with the (row, group) count NG (23-25 us at NG = 4, 33 at 16, 37 at 32, 42
+// at 64), the fused path's with the regions per row (25 us at 2,050, 31 at 4,000, 41 at
+// 6,000); the crossover moves from ~3,000 regions at NG = 4 to past 3,842 at NG = 64.
 bool choose_fused(const step5_geometry* geom, int N, int r_cap) {
     const int G = geom->num_kv_groups;
     const int hpg = geom->idx_heads / G;
@@ -251,7 +252,7 @@ bool choose_fused(const step5_geometry* geom, int N, int r_cap) {
     else if (g_select_path == 2)
         fused = false;
     else
-        fused = (int64_t)N * G >= 128 || r_cap <= 6144;
+        fused = (int64_t)N * G >= 128 || r_cap <= 2800 + 45 * N * G;
     if (r_cap > kFusedMaxRegions || fused_need > 200 * 1024) fused = false;
     return fused;
 }
