@@ -183,6 +183,21 @@ def test_rows_layout_and_host_step_rejections(s5):
     assert lib.step5_decode_step_host(*args(fake, fake, None)) == 1
 
 
+def test_select_path_rule(s5):
+    """The automatic scoring path at the measured points: fused for one row up to ~3,000
+    regions and for sixteen rows at 16K-32K tokens, split for single rows beyond that and
+    for the 128K / 1M decodes, fused for prefill chunks (many (row, group)s)."""
+    g = s5.STEP5_GEOMETRY
+    prev = s5.step5_set_select_path(0)
+    try:
+        for N, r_cap, want in ((1, 577, 1), (1, 2051, 1), (1, 3001, 2), (1, 6001, 2), (4, 6001, 2),
+                               (16, 3842, 1), (16, 4097, 1), (16, 8000, 2), (4, 16385, 2), (1, 131073, 2),
+                               (2048, 8449, 1)):
+            assert s5.step5_select_path_for(g, N, r_cap) == want, (N, r_cap)
+    finally:
+        s5.step5_set_select_path(prev)
+
+
 def test_status_strings(s5):
     for code in range(6):
         assert isinstance(s5.step5_status_string(code), str)
