@@ -33,7 +33,7 @@ __all__ = [
     "step5_index_score_topk_shard", "step5_merge_topk", "step5_sparse_attn_shard", "step5_attn_combine",
     "RowsLayout", "step5_rows_layout_for", "HostRows", "step5_decode_step_host", "step5_set_host_copies",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
-    "step5_set_select_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
+    "step5_set_select_path", "step5_set_wait_polls", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
     "Workspace", "decode_step",
 ]
 
@@ -114,6 +114,7 @@ def load():
         "step5_workspace_init": (i32, [P, sz, P]),
         "step5_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32), P]),
         "step5_set_select_path": (i32, [i32]),
+        "step5_set_wait_polls": (ctypes.c_uint32, [ctypes.c_uint32]),
         "step5_set_prologue_overlap": (i32, [i32]),
         "step5_set_host_copies": (i32, [i32]),
         "step5_select_path_for": (i32, [G, i32, i32]),
@@ -155,6 +156,12 @@ def step5_status_string(status: int) -> str:
 def step5_set_select_path(mode: int) -> int:
     """0 = automatic, 1 = one block per (row, group), 2 = histogram split path."""
     return load().step5_set_select_path(mode)
+
+
+def step5_set_wait_polls(polls: int) -> int:
+    """Poll limit of the split selection path's waits on other blocks (0 = default);
+    returns the previous limit."""
+    return int(load().step5_set_wait_polls(polls))
 
 
 def step5_set_prologue_overlap(enable: int) -> int:
@@ -228,8 +235,10 @@ def step5_index_score_topk(geom, idx_q, w, row_seq, row_pos, cos, sin, summaries
 
 def step5_index_score_topk_noalloc(geom, idx_q, w, row_seq, row_pos, cos, sin, summaries, sel_ids,
                                    sel_count, t_cap, scores=None, sel_scores=None, stream=None):
-    """step5_index_score_topk with the library's fixed 4 MiB scratch instead of a caller
-    workspace, for callers that cannot allocate device memory (see the header)."""
+    """step5_index_score_topk with the library's fixed static scratch (about 6.1 MiB: 4 MiB
+    for this call's own scratch after the ~2.1 MiB any workspace keeps for step (4))
+    instead of a caller workspace, for callers that cannot allocate device memory (see
+    the header for the size limit and the sharing rules)."""
     N = idx_q.shape[0]
     B, _, r_cap, _ = summaries.shape
     _check("step5_index_score_topk_noalloc", load().step5_index_score_topk_noalloc(

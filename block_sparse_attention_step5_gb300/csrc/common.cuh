@@ -246,10 +246,10 @@ __device__ __forceinline__ uint32_t arrive_gen(uint32_t* word, uint32_t nb) {
 }
 
 // Waits until the generation of a barrier word differs from gen (kArrivedLast: no
-// wait); false when the wait gives up.
-__device__ __forceinline__ bool wait_gen(const uint32_t* word, uint32_t gen) {
+// wait); false when the wait gives up after `polls` polls.
+__device__ __forceinline__ bool wait_gen(const uint32_t* word, uint32_t gen, uint32_t polls = kBarrierPolls) {
     if (gen == kArrivedLast) return true;
-    for (uint32_t it = 0; it < kBarrierPolls; ++it)
+    for (uint32_t it = 0; it < polls; ++it)
         if ((ld_relaxed_u32(word) >> 16) != gen) {
             fence_acquire_gpu();
             return true;

@@ -143,6 +143,7 @@ struct ScoreParams {
     int shard;               // 1: a shard's call (regions past the summaries belong to other shards)
     int num_sms;             // split path: persistent blocks (one per SM)
     int overlap_prologue;    // split path: read the non-summary inputs before the launch wait
+    uint32_t wait_polls;     // split path: polls of a wait on other blocks before it gives up
     // split path with overlap_prologue: the launch before writes only the summaries of
     // regions [defer_begin[b], defer_end[b]) of each sequence b; tiles clear of those
     // ranges are fetched before the launch wait (null: wait before the first tile)

@@ -10,8 +10,6 @@
 // owns for as long as it is loaded.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "kernels.cuh"
 #include "step5_sparse_attn.h"
 
@@ -24,25 +22,13 @@ constexpr size_t kNoallocScratchBytes = ((size_t)4 << 20) + kAttnAreaMaxBytes;
 // The scratch array: one copy on every device that loads the library, held until exit.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-// Device address of the array, looked up once per device (with that device current).
+// Device address of the array on the current device.  Looked up on every call (a
+// cached address would go stale if the device's context were torn down and created
+// again in this process); the lookup is cheap next to the memset that follows.
 void* scratch_address(cudaError_t* err) {
-    static void* addr[64] = {};
-    static std::mutex mu;
-    int dev = 0;
-    *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess) return nullptr;
-    if (dev < 0 || dev >= 64) {
-        *err = cudaErrorInvalidDevice;
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void* p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (*err != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    return *err == cudaSuccess ? p : nullptr;
 }
 
 }  // namespace

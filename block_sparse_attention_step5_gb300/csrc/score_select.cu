@@ -8,9 +8,11 @@
 // Scoring runs on the CUDA cores.  With 4 indexer heads per group a thread scores whole
 // regions (two at a time against a shared-memory query broadcast); otherwise each region
 // is read as four 16-byte vectors, one per thread, and a butterfly completes the 64-dim
-// dot products.  Every e4m3 pair is widened to fp32 (exact) and multiplied with packed
-// fp32x2 FMAs.  Selection works on 64-bit keys (desc(score) << 32 | id), which are
-// unique, so any exact selection yields the same ordered ids.
+// dot products.  Every e4m3 pair is widened to an f16 pair (exact: f16 holds every e4m3
+// value) and multiplied by the mixed-precision fma (f16 products, fp32 addend and
+// result, one rounding), which gives the bits of an fp32 fma on the decoded values.
+// Selection works on 64-bit keys (desc(score) << 32 | id), which are unique, so any
+// exact selection yields the same ordered ids.
 //
 // Two selection paths with identical results:
 //  * fused: one block per (row, group) scores every region into shared memory, then
@@ -888,9 +890,9 @@ __device__ void publish_threshold(const ScoreParams& p, int ng, uint32_t gen, ui
 }
 
 // Waits (thread 0) for the threshold of (row, group) ng published after generation
-// gen; -1 when the wait gives up.
+// gen; -1 when the wait gives up (after p.wait_polls polls).
 __device__ int wait_threshold(const ScoreParams& p, int ng, uint32_t gen) {
-    for (uint32_t it = 0; it < kBarrierPolls; ++it) {
+    for (uint32_t it = 0; it < p.wait_polls; ++it) {
         const uint32_t v = ld_relaxed_u32(p.thr + ng);
         if ((v >> 12) != gen) {
             fence_acquire_gpu();
@@ -1352,7 +1354,7 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
     }
     for (int ng = ngA; ng <= ngB; ++ng) {
         __syncthreads();
-        if (__syncthreads_or(tid == 0 && !wait_gen(p.bar2 + ng, s_gen2[ng - ngA]))) {
+        if (__syncthreads_or(tid == 0 && !wait_gen(p.bar2 + ng, s_gen2[ng - ngA], p.wait_polls))) {
             if (tid == 0) raise_status(p.status, kDevTimeout);
             return;
         }

@@ -20,6 +20,7 @@ __device__ uint32_t g_status_word;
 int32_t g_select_path = 0;  // 0 auto, 1 fused, 2 split
 int32_t g_overlap_prologue = 0;
 int32_t g_host_copies = 0;  // step5_decode_step_host: 1 = always through copies
+uint32_t g_wait_polls = 0;  // split path's waits on other blocks: 0 = kBarrierPolls
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -299,6 +300,12 @@ int32_t step5_set_prologue_overlap(int32_t enable) {
     return prev;
 }
 
+uint32_t step5_set_wait_polls(uint32_t polls) {
+    const uint32_t prev = g_wait_polls ? g_wait_polls : kBarrierPolls;
+    g_wait_polls = polls;
+    return prev;
+}
+
 int32_t step5_set_select_path(int32_t mode) {
     const int32_t prev = g_select_path;
     if (mode >= 0 && mode <= 2) g_select_path = mode;
@@ -433,6 +440,7 @@ step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_
     p.bar2 = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.bar2);
     p.num_sms = num_sms();
     p.overlap_prologue = overlap;
+    p.wait_polls = g_wait_polls ? g_wait_polls : kBarrierPolls;
     p.defer_begin = overlap ? defer_begin : nullptr;
     p.defer_end = overlap ? defer_end : nullptr;
     p.status = st;

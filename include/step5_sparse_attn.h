@@ -159,8 +159,9 @@ step5_status step5_index_score_topk(const step5_geometry* geom, int32_t N, int32
  *    geometry: one row up to ~322,000 summary slots, four up to ~74,000 each, sixteen up
  *    to ~12,400 each; e.g. one row at 1M tokens or four at 128K);
  *    larger problems return STEP5_ERR_WORKSPACE before anything is enqueued.
- *  - The first call on a device looks up the array's device address (with that device
- *    current); make that first call before any stream capture.
+ *  - Every call looks up the array's address on the current device (a cheap lookup,
+ *    so no stale address survives a device reset); the first call on a device may
+ *    also load the library's device code there, so make it before any stream capture.
  *  - Each call clears the part of the array it uses (an enqueued memset), since the
  *    array keeps the previous call's contents.  All calls share the one array: calls
  *    whose executions overlap on the GPU (other streams, other threads) race. */
@@ -364,6 +365,15 @@ step5_status step5_workspace_init(void* workspace, size_t workspace_bytes, step5
 #define STEP5_DEV_RANGE   1u  /* a position, id, range or sequence index out of bounds */
 #define STEP5_DEV_TIMEOUT 2u  /* a bounded wait on an in-flight copy gave up           */
 step5_status step5_device_status(uint32_t* flags_out, step5_stream_t stream);
+
+/* Poll limit of the split selection path's waits on other blocks (the threshold word
+ * and the per-(row, group) barrier of step5_index_score_topk; no counterpart in the
+ * pages: a testing and tuning switch).  A wait that polls `polls` times without seeing
+ * the other blocks gives up: the kernel raises STEP5_DEV_TIMEOUT, returns without
+ * writing the (row, group)'s selection, and the workspace must be zeroed
+ * (step5_workspace_init) before its next use.  0 restores the default (2^22 polls,
+ * seconds).  Process-wide, read when a call is enqueued.  Returns the previous limit. */
+uint32_t step5_set_wait_polls(uint32_t polls);
 
 /* Selection path of step5_index_score_topk: 0 = automatic, 1 = one block per
  * (row, group) scoring and selecting in shared memory, 2 = many blocks per

@@ -218,3 +218,10 @@ def test_select_path_switch_roundtrip(s5):
     assert s5.step5_set_select_path(prev) == 2
     assert s5.step5_set_select_path(7) == prev   # out-of-range modes are ignored
     assert s5.step5_set_select_path(prev) == prev
+
+
+def test_wait_polls_switch_roundtrip(s5):
+    prev = s5.step5_set_wait_polls(1000)
+    assert prev > 0
+    assert s5.step5_set_wait_polls(0) == 1000      # 0 restores the default ...
+    assert s5.step5_set_wait_polls(0) == prev      # ... which the next call reports

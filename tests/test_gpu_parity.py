@@ -496,8 +496,9 @@ def _bf16_ulps(a_codes, b_codes):
 def test_indexer_front_end(s5, rope):
     """step5_indexer_front against the oracle: normalised q and k within one bf16 step
     (fp32 against fp64 sums) and equal almost everywhere, z and every untouched cache
-    row bit for bit, and the summaries of the regions that rows complete equal to
-    step5_region_summarize over the same caches."""
+    row bit for bit, and the summaries of the regions that rows complete equal to the
+    oracle's summary step over the caches the GPU wrote (e4m3 midpoint rule) and bit for
+    bit to step5_region_summarize over the same caches."""
     geom = s5.STEP5_GEOMETRY
     G, H, D, B, t_cap, r_cap = 4, geom.idx_heads, 64, 3, 256, 32
     gen = torch.Generator().manual_seed(67)
@@ -532,7 +533,21 @@ def test_indexer_front_end(s5, rope):
         ulps = _bf16_ulps(got, ref)
         assert ulps.max() <= 1 and (ulps > 0).mean() < 0.01
     assert np.array_equal(gz, ref_z)
-    # the completed regions' summaries: the summary kernel over the same (GPU) caches
+    # the completed regions' summaries against the oracle's summary step run on the
+    # caches the GPU wrote (teacher-forced): values through the e4m3 midpoint rule
+    rb_h = np.array([0, 31, 1], dtype=np.int32)
+    re_h = np.array([0, 32, 2], dtype=np.int32)
+    _, s64, _ = oracle.summarize_batch(gk, gz, None if cos is None else S.codes16(cos),
+                                       None if sin is None else S.codes16(sin), rb_h, re_h, r_cap,
+                                       32 if rope else 0, want_f64=True)
+    for b, r in ((1, 31), (2, 1)):
+        k_reg = gk[b, :, 8 * r:8 * r + 8, :]
+        check_summaries(gs[b, :, r], None, s64[b, :, r], k_reg, 32 if rope else 0, where=f"front seq {b}")
+    # both front ends write the completed regions only
+    untouched = np.ones(gs.shape[:3], bool)
+    untouched[1, :, 31] = untouched[2, :, 1] = False
+    assert not gs[untouched].any() and not ref_s[untouched].any()
+    # and the summary kernel over the same (GPU) caches writes them bit for bit
     chk = torch.zeros_like(d["summ"])
     rb = torch.tensor([0, 0, 0], dtype=torch.int32, device=dev)
     re = torch.tensor([0, 0, 0], dtype=torch.int32, device=dev)
