@@ -33,7 +33,7 @@ __all__ = [
     "step5_index_score_topk_shard", "step5_merge_topk", "step5_sparse_attn_shard", "step5_attn_combine",
     "RowsLayout", "step5_rows_layout_for", "HostRows", "step5_decode_step_host", "step5_set_host_copies",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
-    "step5_set_select_path", "step5_set_wait_polls", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
+    "step5_set_select_path", "step5_set_wait_polls", "step5_set_attention_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
     "Workspace", "decode_step",
 ]
 
@@ -115,6 +115,7 @@ def load():
         "step5_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32), P]),
         "step5_set_select_path": (i32, [i32]),
         "step5_set_wait_polls": (ctypes.c_uint32, [ctypes.c_uint32]),
+        "step5_set_attention_path": (i32, [i32]),
         "step5_set_prologue_overlap": (i32, [i32]),
         "step5_set_host_copies": (i32, [i32]),
         "step5_select_path_for": (i32, [G, i32, i32]),
@@ -156,6 +157,12 @@ def step5_status_string(status: int) -> str:
 def step5_set_select_path(mode: int) -> int:
     """0 = automatic, 1 = one block per (row, group), 2 = histogram split path."""
     return load().step5_set_select_path(mode)
+
+
+def step5_set_attention_path(mode: int) -> int:
+    """Step (4) without a split: 0 = automatic, 1 = warp-level MMA kernel, 2 = tcgen05
+    kernel; returns the previous value."""
+    return load().step5_set_attention_path(mode)
 
 
 def step5_set_wait_polls(polls: int) -> int:

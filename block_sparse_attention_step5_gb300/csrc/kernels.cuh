@@ -194,6 +194,11 @@ cudaError_t launch_attention(const AttnParams& p, int N, const CUtensorMap& kmap
 cudaError_t launch_attention_shard(const AttnParams& p, int N, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                    cudaStream_t stream, bool pdl);
 size_t attention_smem_bytes();  // dynamic part
+// The tcgen05 kernel: one 128-thread CTA per (row, group), no split (p.splits == 1), the
+// whole-row output only (no shard states).
+cudaError_t launch_attention_tc(const AttnParams& p, int N, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                cudaStream_t stream, bool pdl);
+size_t attention_tc_smem_bytes(int top_k);
 constexpr size_t kAttnStaticSmem = (kMaxTopK + 2) * 4 + 16384;  // picked ids + merge scratch
 
 // ----------------------------------------------------------------- sequence shards

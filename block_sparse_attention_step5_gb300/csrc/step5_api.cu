@@ -21,6 +21,7 @@ int32_t g_select_path = 0;  // 0 auto, 1 fused, 2 split
 int32_t g_overlap_prologue = 0;
 int32_t g_host_copies = 0;  // step5_decode_step_host: 1 = always through copies
 uint32_t g_wait_polls = 0;  // split path's waits on other blocks: 0 = kBarrierPolls
+int32_t g_attn_path = 0;    // step (4) without a split: 0 auto (tensor cores), 1 warp MMA kernel, 2 tensor cores
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -306,6 +307,12 @@ uint32_t step5_set_wait_polls(uint32_t polls) {
     return prev;
 }
 
+int32_t step5_set_attention_path(int32_t mode) {
+    const int32_t prev = g_attn_path;
+    if (mode >= 0 && mode <= 2) g_attn_path = mode;
+    return prev;
+}
+
 int32_t step5_set_select_path(int32_t mode) {
     const int32_t prev = g_select_path;
     if (mode >= 0 && mode <= 2) g_select_path = mode;
@@ -524,8 +531,13 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     p.flags = splits > 1 ? reinterpret_cast<uint32_t*>(ws + A.flags) : nullptr;
     p.part = splits > 1 ? reinterpret_cast<float*>(ws + A.part) : nullptr;
     p.scale_log2 = geom->softmax_scale * 1.4426950408889634f;
-    cudaError_t e = states != nullptr ? launch_attention_shard(p, N, kmap, vmap, (cudaStream_t)stream, use_pdl())
-                                      : launch_attention(p, N, kmap, vmap, (cudaStream_t)stream, use_pdl());
+    cudaError_t e;
+    if (states != nullptr)
+        e = launch_attention_shard(p, N, kmap, vmap, (cudaStream_t)stream, use_pdl());
+    else if (splits == 1 && g_attn_path != 1)
+        e = launch_attention_tc(p, N, kmap, vmap, (cudaStream_t)stream, use_pdl());
+    else
+        e = launch_attention(p, N, kmap, vmap, (cudaStream_t)stream, use_pdl());
     return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
 }
 

@@ -375,6 +375,14 @@ step5_status step5_device_status(uint32_t* flags_out, step5_stream_t stream);
  * seconds).  Process-wide, read when a call is enqueued.  Returns the previous limit. */
 uint32_t step5_set_wait_polls(uint32_t polls);
 
+/* Kernel of step5_sparse_attn (and the gated call) when a (row, group)'s keys are not
+ * split over several blocks (many (row, group) pairs, or no workspace): 0 = automatic
+ * (the tensor-core kernel), 1 = the warp-level MMA kernel, 2 = the tcgen05 tensor-core
+ * kernel.  Both give the output within rounding of each other (different fp32 summation
+ * orders); a testing and tuning switch.  Process-wide; other values are ignored.  Returns
+ * the previous value. */
+int32_t step5_set_attention_path(int32_t mode);
+
 /* Selection path of step5_index_score_topk: 0 = automatic, 1 = one block per
  * (row, group) scoring and selecting in shared memory, 2 = many blocks per
  * (row, group) with a histogram threshold pass.  Both give identical results; this is a
