@@ -225,7 +225,7 @@ def run_ours(args, rank, world, local_rank):
         flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
         stream = torch.cuda.current_stream()
         span = w.max_span
-        path = s5.step5_select_path_for(geom, N, w.r_cap)
+        path = s5.step5_select_path_for(geom, N, w.r_cap, w.B)
         launches_per_step = (1 if span > 0 else 0) + 1 + 1  # summarize, score + select, attention
 
         def call_sum():
@@ -481,7 +481,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "e4m3+bf16 (fp32 accumulate)", "data": "synthetic (seeded)",
         "config": {"workload": w.name, "rows_per_gpu": w.N, "context": int(w.row_pos.max()),
                    "regions_per_group": int(w.row_pos.max()) // 8, "kv_groups": 4, "q_heads": 32,
-                   "idx_heads": 16, "top_k": 512, "select_path": "fused" if head["path"] == 1 else "split",
+                   "idx_heads": 16, "top_k": 512, "select_path": {1: "fused", 2: "split", 3: "tensor-core"}[head["path"]],
                    "l2": "flushed between timed steps (256 MiB write, untimed)",
                    "timing": "CUDA events around a CUDA-graph replay of the whole step",
                    "parallelism": f"replicas x{world}"},
@@ -519,7 +519,7 @@ def run_ours(args, rank, world, local_rank):
         line["secondary"] = {"workload": sec["w"].name, "value": round(whole_job_rate(sec["w"].N, world, sec["ms"]), 2),
                              "unit": UNIT, "ms_per_step": round(sec["ms"], 5),
                              "achieved_gbs": round(sgbs, 1), "frac": round(sgbs / peak, 4),
-                             "select_path": "fused" if sec["path"] == 1 else "split",
+                             "select_path": {1: "fused", 2: "split", 3: "tensor-core"}[sec["path"]],
                              "breakdown_us": {"summarize": round(sec["per_sum"] * 1e3, 2),
                                               "score_select": round(sec["per_score"] * 1e3, 2),
                                               "attention": round(sec["per_attn"] * 1e3, 2),

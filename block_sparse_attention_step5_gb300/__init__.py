@@ -118,7 +118,7 @@ def load():
         "step5_set_attention_path": (i32, [i32]),
         "step5_set_prologue_overlap": (i32, [i32]),
         "step5_set_host_copies": (i32, [i32]),
-        "step5_select_path_for": (i32, [G, i32, i32]),
+        "step5_select_path_for": (i32, [G, i32, i32, i32]),
         "step5_status_string": (ctypes.c_char_p, [i32]),
         "step5_convert_bf16_to_e4m3": (i32, [P, P, i64, P]),
     }
@@ -155,7 +155,8 @@ def step5_status_string(status: int) -> str:
 
 
 def step5_set_select_path(mode: int) -> int:
-    """0 = automatic, 1 = one block per (row, group), 2 = histogram split path."""
+    """0 = automatic, 1 = one block per (row, group), 2 = histogram split path, 3 =
+    tensor-core scoring then one selecting block per (row, group)."""
     return load().step5_set_select_path(mode)
 
 
@@ -183,9 +184,10 @@ def step5_set_host_copies(always: int) -> int:
     return load().step5_set_host_copies(int(always))
 
 
-def step5_select_path_for(geom, N: int, r_cap: int) -> int:
-    """1 (fused: one kernel) or 2 (split: three kernels) for this N and r_cap."""
-    return load().step5_select_path_for(ctypes.byref(Geometry.of(geom)), N, r_cap)
+def step5_select_path_for(geom, N: int, r_cap: int, B: int = None) -> int:
+    """1 (fused), 2 (split) or 3 (tensor-core scoring, then selection) for N rows of B
+    sequences (default: one row per sequence) and r_cap."""
+    return load().step5_select_path_for(ctypes.byref(Geometry.of(geom)), N, N if B is None else B, r_cap)
 
 
 def step5_workspace_bytes(geom, N: int, r_cap: int) -> int:

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libstep5sa.so")
 OBJDIR = os.path.join(PKG, "_build")
-SOURCES = ["step5_api.cu", "summarize.cu", "score_select.cu", "attention.cu", "noalloc.cu", "front.cu", "shard.cu", "attention_shard.cu", "attention_tc.cu"]
+SOURCES = ["step5_api.cu", "summarize.cu", "score_select.cu", "attention.cu", "noalloc.cu", "front.cu", "shard.cu", "attention_shard.cu", "attention_tc.cu", "score_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

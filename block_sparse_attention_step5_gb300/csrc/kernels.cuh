@@ -150,7 +150,27 @@ struct ScoreParams {
     const int32_t* defer_begin;
     const int32_t* defer_end;
 };
+// Validated (sequence, R) of row n, or R = -1 when the row is out of range.
+// Candidate regions of row n in this call's summaries: region_lo + [0, R).  A whole-row
+// call needs a slot for every candidate; a shard takes those of its slots.
+__device__ __forceinline__ int row_regions(const ScoreParams& p, int n, int& b, int& pos) {
+    b = p.row_seq[n];
+    pos = p.row_pos[n];
+    if (b < 0 || b >= p.B || pos < 0 || pos >= p.t_cap) return -1;
+    const int R = pos / 8 - p.region_lo;
+    if (!p.shard) return R > p.r_cap ? -1 : R;
+    return R < 0 ? 0 : (R > p.r_cap ? p.r_cap : R);
+}
+
 cudaError_t launch_score_fused(const ScoreParams& p, cudaStream_t stream, bool pdl);
+// The selection of every (row, group) from the scores already in p.scores (one block
+// each, as the fused path selects).
+cudaError_t launch_select_scores(const ScoreParams& p, cudaStream_t stream, bool pdl);
+// Tensor-core scoring (tcgen05, e4m3 x e4m3 into fp32 TMEM) of every candidate region of
+// every row into p.scores, for launches with many rows: one CTA per (block of 128 / HPG
+// rows, group).  smap: the summaries' 2-D tensor map (box 64 bytes x 256 rows, 64-byte
+// swizzle).
+cudaError_t launch_score_tc(const ScoreParams& p, const CUtensorMap& smap, cudaStream_t stream, bool pdl);
 // Split path: one persistent launch (score, candidates, ranks) with grid barriers.
 // smap: 2-D tensor map of the summaries, [B*G*r_cap rows][64 bytes], box 64 x 256,
 // 64-byte swizzle (used when idx_heads / G == 4).

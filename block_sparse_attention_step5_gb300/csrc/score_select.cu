@@ -400,23 +400,13 @@ __device__ void write_selection(const ScoreParams& p, int n, int g, int take, co
     if (threadIdx.x == 0) p.sel_count[ng] = take;
 }
 
-// Validated (sequence, R) of row n, or R = -1 when the row is out of range.
-// Candidate regions of row n in this call's summaries: region_lo + [0, R).  A whole-row
-// call needs a slot for every candidate; a shard takes those of its slots.
-__device__ __forceinline__ int row_regions(const ScoreParams& p, int n, int& b, int& pos) {
-    b = p.row_seq[n];
-    pos = p.row_pos[n];
-    if (b < 0 || b >= p.B || pos < 0 || pos >= p.t_cap) return -1;
-    const int R = pos / 8 - p.region_lo;
-    if (!p.shard) return R > p.r_cap ? -1 : R;
-    return R < 0 ? 0 : (R > p.r_cap ? p.r_cap : R);
-}
-
 // ----------------------------------------------------------------- fused path
 
 constexpr int kFusedThreads = 256;
 
-template <int HPG>
+// FROM_SCORES: the scores are already in p.scores (written by the tensor-core scoring
+// kernel); the block only selects.
+template <int HPG, bool FROM_SCORES>
 __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams p, int P2, int key_cap) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint64_t* s_sel = reinterpret_cast<uint64_t*>(smem);                 // P2
@@ -437,7 +427,9 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
     }
     const uint4* base = reinterpret_cast<const uint4*>(p.summ + ((int64_t)b * p.G + g) * p.r_cap * 64);
     float* exp_scores = p.scores ? p.scores + ((int64_t)n * p.G + g) * p.r_cap : nullptr;
-    if constexpr (HPG == 4) {
+    if constexpr (FROM_SCORES) {
+        for (int r = threadIdx.x; r < R; r += kFusedThreads) s_key[r] = desc_key(__ldcg(exp_scores + r));
+    } else if constexpr (HPG == 4) {
         __shared__ uint4 s_qh[32];
         float w[4];
 #pragma unroll
@@ -1386,12 +1378,12 @@ cudaError_t launch_ex2(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
     return cudaLaunchKernelEx(&cfg, kernel, p, a, b);
 }
 
-template <int HPG>
+template <int HPG, bool FROM_SCORES = false>
 cudaError_t fused_for(const ScoreParams& p, cudaStream_t stream, bool pdl) {
     const int P2 = pow2_at_least(p.top_k);
     const int key_cap = (p.r_cap < kFusedMaxRegions ? p.r_cap : kFusedMaxRegions);
     const size_t smem = (size_t)P2 * 8 + (size_t)((key_cap + 3) & ~3) * 4 + HPG * 64 * 4;
-    auto kern = score_fused_kernel<HPG>;
+    auto kern = score_fused_kernel<HPG, FROM_SCORES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_ex2(kern, dim3(p.G, p.N), dim3(kFusedThreads), smem, stream, pdl, p, P2,
@@ -1476,6 +1468,10 @@ cudaError_t launch_score_fused(const ScoreParams& p, cudaStream_t stream, bool p
         case 8: return fused_for<8>(p, stream, pdl);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_select_scores(const ScoreParams& p, cudaStream_t stream, bool pdl) {
+    return fused_for<1, true>(p, stream, pdl);  // (HPG is not used when selecting from scores)
 }
 
 cudaError_t launch_score_split(const ScoreParams& p, const CUtensorMap& smap, cudaStream_t stream, bool pdl) {

@@ -236,27 +236,33 @@ bool use_pdl() { return true; }
 
 
 
-// Fused (one block per (row, group), keys in shared memory) when there are many rows or
-// few regions; the histogram split path when a few rows have many regions.  Measured on
-// GB300 (eager calls after an L2 flush, summaries built from k and z): the split path's
-// time grows with the (row, group) count NG (23-25 us at NG = 4, 33 at 16, 37 at 32, 42
-// at 64), the fused path's with the regions per row (25 us at 2,050, 31 at 4,000, 41 at
-// 6,000); the crossover moves from ~3,000 regions at NG = 4 to past 3,842 at NG = 64.
-bool choose_fused(const step5_geometry* geom, int N, int r_cap) {
+// Selection paths of steps (2)-(3): 1 = fused (one block per (row, group) scores on the
+// CUDA cores and selects in shared memory), 2 = split (one persistent launch whose blocks
+// share each (row, group)'s regions), 3 = tensor-core scoring of blocks of rows that share
+// a sequence, then one selecting block per (row, group).
+// Fused vs split was measured on GB300 (eager calls after an L2 flush, summaries built
+// from k and z): the split path's time grows with the (row, group) count NG (23-25 us at
+// NG = 4, 33 at 16, 37 at 32, 42 at 64), the fused path's with the regions per row (25 us
+// at 2,050, 31 at 4,000, 41 at 6,000); the crossover moves from ~3,000 regions at NG = 4
+// to past 3,842 at NG = 64.  The tensor-core path needs rows that share their sequence's
+// summaries (it scores a block of rows against one sequence's summaries at a time): taken
+// for many rows (NG >= 128) with at least 8 rows per sequence on average.
+int choose_path(const step5_geometry* geom, int N, int B, int r_cap) {
     const int G = geom->num_kv_groups;
     const int hpg = geom->idx_heads / G;
     int P2 = 1;
     while (P2 < geom->top_k) P2 <<= 1;
     const int fused_need = P2 * 8 + ((r_cap + 3) & ~3) * 4 + hpg * 64 * 4;
-    bool fused;
-    if (g_select_path == 1)
-        fused = true;
-    else if (g_select_path == 2)
-        fused = false;
+    const bool fused_fits = r_cap <= kFusedMaxRegions && fused_need <= 200 * 1024;
+    int path;
+    if (g_select_path == 1 || g_select_path == 2 || g_select_path == 3)
+        path = g_select_path;
+    else if ((int64_t)N * G >= 128 && (int64_t)N >= 8 * (int64_t)B)
+        path = 3;
     else
-        fused = (int64_t)N * G >= 128 || r_cap <= 2800 + 45 * N * G;
-    if (r_cap > kFusedMaxRegions || fused_need > 200 * 1024) fused = false;
-    return fused;
+        path = ((int64_t)N * G >= 128 || r_cap <= 2800 + 45 * N * G) ? 1 : 2;
+    if (path != 2 && !fused_fits) path = 2;  // the selecting block keeps a row's keys on chip
+    return path;
 }
 
 }  // namespace
@@ -315,13 +321,13 @@ int32_t step5_set_attention_path(int32_t mode) {
 
 int32_t step5_set_select_path(int32_t mode) {
     const int32_t prev = g_select_path;
-    if (mode >= 0 && mode <= 2) g_select_path = mode;
+    if (mode >= 0 && mode <= 3) g_select_path = mode;
     return prev;
 }
 
-int32_t step5_select_path_for(const step5_geometry* geom, int32_t N, int32_t r_cap) {
-    if (check_geometry(geom) != STEP5_OK || N <= 0 || r_cap <= 0) return 0;
-    return choose_fused(geom, N, r_cap) ? 1 : 2;
+int32_t step5_select_path_for(const step5_geometry* geom, int32_t N, int32_t B, int32_t r_cap) {
+    if (check_geometry(geom) != STEP5_OK || N <= 0 || B <= 0 || r_cap <= 0) return 0;
+    return choose_path(geom, N, B, r_cap);
 }
 
 size_t step5_workspace_bytes(const step5_geometry* geom, int32_t N, int32_t r_cap) {
@@ -416,13 +422,18 @@ step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_
     if (!aligned16(summaries_e4m3) || !aligned16(idx_q_bf16)) return STEP5_ERR_INVALID_ARGUMENT;
     const int G = geom->num_kv_groups;
     const int hpg = geom->idx_heads / G;
-    const bool fused = choose_fused(geom, N, r_cap);
+    int path = choose_path(geom, N, B, r_cap);
     const Layout L = layout(geom, N, r_cap);
-    if (!fused) {
+    // the tensor-core path keeps every score in the workspace (or the caller's export);
+    // without either, the fused path runs
+    if (path == 3 && scores_or_null == nullptr && (workspace == nullptr || workspace_bytes < L.end)) path = 1;
+    const bool fused = path == 1;
+    if (path == 2) {
         if (workspace == nullptr) return STEP5_ERR_WORKSPACE;
         if (workspace_bytes < L.end) return STEP5_ERR_WORKSPACE;
-        if ((uint64_t)B * G * r_cap > (uint64_t)INT32_MAX - kSplitTileRegions) return STEP5_ERR_INVALID_ARGUMENT;
     }
+    if (path != 1 && (uint64_t)B * G * r_cap > (uint64_t)INT32_MAX - kSplitTileRegions)
+        return STEP5_ERR_INVALID_ARGUMENT;
     if (!launch) return STEP5_OK;
     uint32_t* st = status_ptr();
     if (!st) return STEP5_ERR_CUDA;
@@ -438,13 +449,14 @@ step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_
     p.sel_ids = sel_ids;
     p.sel_count = sel_count;
     p.sel_scores = sel_scores_or_null;
+    const bool split = path == 2;
     p.scores = scores_or_null ? scores_or_null : (fused ? nullptr : reinterpret_cast<float*>(ws + L.scores));
-    p.hist = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.hist);
-    p.cand_count = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.cand_count);
-    p.cand = fused ? nullptr : reinterpret_cast<uint64_t*>(ws + L.cand);
-    p.arrive1 = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.arrive1);
-    p.thr = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.thr);
-    p.bar2 = fused ? nullptr : reinterpret_cast<uint32_t*>(ws + L.bar2);
+    p.hist = split ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr;
+    p.cand_count = split ? reinterpret_cast<uint32_t*>(ws + L.cand_count) : nullptr;
+    p.cand = split ? reinterpret_cast<uint64_t*>(ws + L.cand) : nullptr;
+    p.arrive1 = split ? reinterpret_cast<uint32_t*>(ws + L.arrive1) : nullptr;
+    p.thr = split ? reinterpret_cast<uint32_t*>(ws + L.thr) : nullptr;
+    p.bar2 = split ? reinterpret_cast<uint32_t*>(ws + L.bar2) : nullptr;
     p.num_sms = num_sms();
     p.overlap_prologue = overlap;
     p.wait_polls = g_wait_polls ? g_wait_polls : kBarrierPolls;
@@ -469,7 +481,12 @@ step5_status score_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_
         CUtensorMap smap;
         const uint64_t srows = (uint64_t)B * G * r_cap;
         if (!cache_summary_map(summaries_e4m3, srows, &smap)) return STEP5_ERR_CUDA;
-        e = launch_score_split(p, smap, (cudaStream_t)stream, use_pdl());
+        if (split) {
+            e = launch_score_split(p, smap, (cudaStream_t)stream, use_pdl());
+        } else {
+            e = launch_score_tc(p, smap, (cudaStream_t)stream, use_pdl());
+            if (e == cudaSuccess) e = launch_select_scores(p, (cudaStream_t)stream, true);
+        }
     }
     return e == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
 }

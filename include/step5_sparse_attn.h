@@ -384,9 +384,14 @@ uint32_t step5_set_wait_polls(uint32_t polls);
 int32_t step5_set_attention_path(int32_t mode);
 
 /* Selection path of step5_index_score_topk: 0 = automatic, 1 = one block per
- * (row, group) scoring and selecting in shared memory, 2 = many blocks per
- * (row, group) with a histogram threshold pass.  Both give identical results; this is a
- * tuning and testing switch.  Returns the previous value. */
+ * (row, group) scoring on the CUDA cores and selecting in shared memory, 2 = many blocks
+ * per (row, group) with a histogram threshold pass, 3 = tcgen05 tensor-core scoring of
+ * blocks of rows that share a sequence (the scores go to the workspace or the caller's
+ * export, and without either path 1 runs), then one selecting block per (row, group).
+ * Paths 1 and 2 give identical results; path 3's scores differ from theirs only by the
+ * fp32 summation order of each dot product (the e4m3 products are exact in both), so
+ * its picks are the same but at near-equal scores.  A tuning and testing switch.
+ * Returns the previous value. */
 int32_t step5_set_select_path(int32_t mode);
 
 /* Opt-in overlap of the scoring prologue with the launch before it (no counterpart in
@@ -405,12 +410,11 @@ int32_t step5_set_prologue_overlap(int32_t enable);
  * through copies.  Process-wide; other values are ignored.  Returns the previous value. */
 int32_t step5_set_host_copies(int32_t always);
 
-/* The selection path step5_index_score_topk takes for this geometry, N and r_cap under
- * the current step5_set_select_path setting: 1 (fused: one block per (row, group)) or 2
- * (split: one persistent launch whose blocks share each (row, group)'s regions, publish
- * a histogram threshold, and rank the candidates together); 0 for an unsupported
- * geometry. */
-int32_t step5_select_path_for(const step5_geometry* geom, int32_t N, int32_t r_cap);
+/* The selection path step5_index_score_topk takes for this geometry, N rows, B sequences
+ * and r_cap under the current step5_set_select_path setting (1, 2 or 3 as above; path 3
+ * falls back to 1 at the call when neither a workspace nor a score export is passed); 0
+ * for an unsupported geometry or non-positive sizes. */
+int32_t step5_select_path_for(const step5_geometry* geom, int32_t N, int32_t B, int32_t r_cap);
 
 /* Human-readable name of a status code (static string). */
 const char* step5_status_string(step5_status status);

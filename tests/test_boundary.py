@@ -186,14 +186,16 @@ def test_rows_layout_and_host_step_rejections(s5):
 def test_select_path_rule(s5):
     """The automatic scoring path at the measured points: fused for one row up to ~3,000
     regions and for sixteen rows at 16K-32K tokens, split for single rows beyond that and
-    for the 128K / 1M decodes, fused for prefill chunks (many (row, group)s)."""
+    for the 128K / 1M decodes, tensor-core scoring for prefill chunks (many rows of one
+    sequence), fused for many rows of as many sequences."""
     g = s5.STEP5_GEOMETRY
     prev = s5.step5_set_select_path(0)
     try:
-        for N, r_cap, want in ((1, 577, 1), (1, 2051, 1), (1, 3001, 2), (1, 6001, 2), (4, 6001, 2),
-                               (16, 3842, 1), (16, 4097, 1), (16, 8000, 2), (4, 16385, 2), (1, 131073, 2),
-                               (2048, 8449, 1)):
-            assert s5.step5_select_path_for(g, N, r_cap) == want, (N, r_cap)
+        for N, B, r_cap, want in ((1, 1, 577, 1), (1, 1, 2051, 1), (1, 1, 3001, 2), (1, 1, 6001, 2),
+                                  (4, 4, 6001, 2), (16, 16, 3842, 1), (16, 16, 4097, 1), (16, 16, 8000, 2),
+                                  (4, 4, 16385, 2), (1, 1, 131073, 2), (2048, 1, 8449, 3), (2048, 2048, 8449, 1),
+                                  (256, 32, 4000, 3), (256, 64, 4000, 1), (2048, 1, 16385, 2)):
+            assert s5.step5_select_path_for(g, N, r_cap, B) == want, (N, B, r_cap)
     finally:
         s5.step5_set_select_path(prev)
 
@@ -216,6 +218,8 @@ def test_select_path_switch_roundtrip(s5):
     prev = s5.step5_set_select_path(1)
     assert s5.step5_set_select_path(2) == 1
     assert s5.step5_set_select_path(prev) == 2
+    assert s5.step5_set_select_path(3) == prev
+    assert s5.step5_set_select_path(prev) == 3
     assert s5.step5_set_select_path(7) == prev   # out-of-range modes are ignored
     assert s5.step5_set_select_path(prev) == prev
 

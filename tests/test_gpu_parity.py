@@ -131,12 +131,25 @@ SMALL_POS = [0, 1, 7, 8, 9, 15, 16, 17, 129, 4095, 4096, 4097, 4103, 4104, 4600]
 
 
 @pytest.mark.parametrize("seed", [17, 41])
-@pytest.mark.parametrize("path", [1, 2])
-def test_small_cases_both_paths(s5, seed, path):
+@pytest.mark.parametrize("path", [1, 2, 3])
+def test_small_cases_every_path(s5, seed, path):
     geom = s5.STEP5_GEOMETRY
     w = S.workload({"positions": SMALL_POS, "B": 3}, seed=seed)
     t = S.materialize(w, device="cuda")
     full_check(s5, geom, w, t, path=path)
+
+
+@pytest.mark.parametrize("cfg", [{"positions": [9000 + 7 * i for i in range(150)], "B": 1},
+                                 {"positions": [3000 + 11 * i for i in range(96)] + [700, 12, 0], "B": 3}])
+def test_tensor_core_scoring_many_rows(s5, cfg):
+    """Path 3 on blocks of rows that share a sequence (a prefill chunk) and on blocks that
+    mix three sequences (a pass per sequence), against the oracle: scores within the term
+    tolerance, the selection of the GPU's scores exact, near-ties only against the
+    oracle's own scores of the GPU's summaries."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload(cfg, seed=53)
+    t = S.materialize(w, device="cuda")
+    full_check(s5, geom, w, t, path=3, chain=False)
 
 
 def test_paths_agree_bit_for_bit(s5):
@@ -166,7 +179,7 @@ def test_geometry_variants(s5, over):
                     top_k=geom.top_k, softmax_scale=base.softmax_scale)
     w = S.workload({"positions": [17, 600, 4100, 20000], "B": 2}, seed=41, geom=sg)
     t = S.materialize(w, device="cuda")
-    for path in (1, 2):
+    for path in (1, 2, 3):
         full_check(s5, geom, w, t, path=path, chain=(path == 1))
 
 
