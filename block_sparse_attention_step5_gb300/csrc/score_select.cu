@@ -23,6 +23,7 @@
 //    the bin holding the k-th key into a candidate list; after a second barrier the
 //    blocks place every candidate at its rank (a count of the smaller candidates).
 #include "kernels.cuh"
+#include "tcgen05.cuh"
 
 namespace step5 {
 
@@ -505,14 +506,17 @@ constexpr int kBinsPerThread = kHistBins / kSplitThreads;  // histogram bins a t
 // while the previous tile is scored.  Each run of tiles of one (row, group) adds its
 // shared-memory histogram to the global one.
 
-constexpr int kTileRegions = 2 * kSplitThreads;   // 64 KB of summaries, two rows per thread
+constexpr int kTileRegions = 2 * kSplitThreads;   // 64 KB of summaries
 static_assert(kTileRegions == kSplitTileRegions, "host and device tile sizes differ");
 constexpr int kTileBytes = kTileRegions * 64;
 constexpr int kBoxRows = 256;                     // rows of one summary tensor-map box
 constexpr int kSlots = kSplitThreads / 4;         // region slots of the 4-lane layout
 constexpr int kTileU = kTileRegions / kSlots;     // regions per slot per tile (8)
 constexpr int kScoreStages = 2;
-constexpr size_t kScoreSmem = kScoreStages * kTileBytes + 1024;
+constexpr uint32_t kQeBytes = 16 * 64;              // a group's e4m3 query tile (B operand)
+constexpr size_t kScoreSmem = kScoreStages * kTileBytes + 2 * kQeBytes + 1024;
+constexpr uint32_t kScoreTmemCols = 256;            // two accumulators of 8 subtiles x 16 columns
+constexpr uint32_t kScoreIdesc = tc::instr_desc(tc::kFmtE4M3, false, false, 128, 16);
 
 struct Tile {
     int valid, ng, n, g, b, pos, R, c0, c1;
@@ -665,7 +669,7 @@ struct QBuf {
 // caller synchronises before reading it.
 template <int HPG>
 __device__ __forceinline__ void finish_query(const ScoreParams& p, const QRaw<HPG>& r, const QRope<HPG>& ro,
-                                             QBuf<HPG>& qb) {
+                                             QBuf<HPG>& qb, uint8_t* qe = nullptr) {
     const int half = p.rope_dims >> 1;
 #pragma unroll
     for (int j = 0; j < QRaw<HPG>::kPer; ++j) {
@@ -676,14 +680,19 @@ __device__ __forceinline__ void finish_query(const ScoreParams& p, const QRaw<HP
             if (p.cos != nullptr && d < p.rope_dims)
                 rb = neox_rotate(bf16_to_f32(rb), bf16_to_f32(r.qp[j]), bf16_to_f32(ro.c[j]), bf16_to_f32(ro.s[j]),
                                  d < half);
-            const float v = e4m3x2_to_f32x2(f32_to_e4m3(bf16_to_f32(rb))).x;
-            if constexpr (HPG == 4)
+            const uint8_t code = f32_to_e4m3(bf16_to_f32(rb));
+            const float v = e4m3x2_to_f32x2(code).x;
+            if constexpr (HPG == 4) {
                 qb.qh[(d >> 1) * 8 + h * 2 + (d & 1)] = __half_as_ushort(__float2half_rn(v));
-            else
+                // the tensor cores' B operand: head h = row h, K-major, 64-byte swizzle
+                if (qe) qe[h * 64 + ((((d >> 4) ^ ((h >> 1) & 3))) << 4) + (d & 15)] = code;
+            } else {
                 qb.q[i] = v;
+            }
         }
     }
     if (threadIdx.x < HPG) qb.w[threadIdx.x] = r.w;
+    if (qe) fence_proxy_async();  // the MMAs read the tile through the async proxy
 }
 
 // The 4-lanes-per-region query registers from a staged buffer (after a __syncthreads).
@@ -707,72 +716,53 @@ __device__ __forceinline__ int row_pos_or0(const ScoreParams& p, int n) {
     return row_regions(p, n, b, pos) < 0 ? 0 : pos;
 }
 
-// Score of one region whose 64 summary bytes are a[0..3] (the one-row form of
-// score_rows2, same arithmetic and order).
-__device__ __forceinline__ float score_row1(const uint4 (&a)[4], const uint4* qh, const float (&w)[4]) {
-    float ae[4], ao[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) ae[h] = ao[h] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t wa[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-#pragma unroll
-            for (int hw = 0; hw < 2; ++hw) {
-                const uint32_t xa = e4m3x2_to_f16x2((uint16_t)(hw ? wa[qq] >> 16 : wa[qq] & 0xffffu));
-                const uint4 q = qh[8 * k + 2 * qq + hw];
-                const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) fma_f16x2_f32(ae[h], ao[h], qw[h], xa);
-            }
-        }
+// One staged tile on the tensor cores (4 indexer heads per group), in two halves so that
+// the products of the next tile overlap the epilogue of this one:
+//  * tc_tile_issue (thread 0): for each 128-region subtile that holds regions, two e4m3
+//    MMAs (K = 32 each) of the subtile against the group's query tile (heads as rows 0-3
+//    of N = 16) into TMEM columns d + 16 m .. d + 16 m + 3, then a commit to dbar;
+//  * tc_tile_epilogue (all threads, after dbar): the 16 warps read their regions' head
+//    sums (warp w: subtiles w / 4 and w / 4 + 4, lanes 32 (w % 4) ..) and finish each score as the
+//    CUDA-core path does: sum_h relu(dot_h) * w_h in fp32, heads in order.
+// The e4m3 products are exact, so the scores differ from the CUDA-core path's only by the
+// summation order of each 64-term dot product.
+__device__ __forceinline__ void tc_tile_issue(const uint8_t* tile, const uint8_t* qe, int nreg, uint32_t d,
+                                              uint64_t* dbar) {
+    tc::fence_after_sync();
+    const int nsub = (nreg + 127) >> 7;
+    const uint64_t db = tc::smem_desc(smem_u32(qe), 16, 512, tc::kSwizzle64);
+    const uint64_t da0 = tc::smem_desc(smem_u32(tile), 16, 512, tc::kSwizzle64);
+    for (int m = 0; m < nsub; ++m) {
+        const uint64_t da = da0 + (uint64_t)(512 * m);  // + m * 8 KB, in 16-byte units
+        tc::mma_f8(d + 16u * m, da, db, kScoreIdesc, false);
+        tc::mma_f8(d + 16u * m, da + 2, db + 2, kScoreIdesc, true);  // dims 32-63 (+32 bytes)
     }
-    return finish_score4(ae, ao, w);
+    tc::commit(dbar);
 }
 
-// One thread per region (HPG == 4): thread t scores rows t and t + kSplitThreads of a
-// tile that arrived as 256-row boxes through the summaries' tensor map with 64-byte swizzle
-// (16-byte chunk k of row r sits at chunk k ^ ((r >> 1) & 3)), so the 8 rows a quarter
-// warp reads at once fall in 8 different bank groups.  Rows at or past nreg are skipped
-// a warp at a time.
-__device__ __forceinline__ void score_tile_rows(const uint8_t* tile, int nreg, const uint4* qh,
-                                                const float (&w)[4], float* scores, float* keep,
-                                                uint32_t* s_hist) {
-    const int t = threadIdx.x;
-    const int wbase = t & ~31;
-    if (wbase >= nreg) return;
-    const int sw = (t >> 1) & 3;
-    const uint4* ra = reinterpret_cast<const uint4*>(tile + t * 64);
-    uint4 a[4];
-    if (wbase + kSplitThreads < nreg) {
-        const uint4* rb = reinterpret_cast<const uint4*>(tile + kSplitThreads * 64 + t * 64);
-        uint4 b[4];
+__device__ __forceinline__ void tc_tile_epilogue(int nreg, uint32_t d, const float* wsm, float* scores, float* keep,
+                                                 uint32_t* s_hist) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nsub = (nreg + 127) >> 7;
+    const int q = warp & 3;
+    float w[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            a[k] = ra[k ^ sw];
-            b[k] = rb[k ^ sw];
-        }
-        float sa, sb;
-        score_rows2(a, b, qh, w, sa, sb);
-        scores[t] = sa;  // t < kSplitThreads < nreg
-        if (keep) keep[t] = sa;
-        atomicAdd(&s_hist[desc_key(sa) >> (32 - kHistBits)], 1u);
-        if (t + kSplitThreads < nreg) {
-            scores[t + kSplitThreads] = sb;
-            if (keep) keep[t + kSplitThreads] = sb;
-            atomicAdd(&s_hist[desc_key(sb) >> (32 - kHistBits)], 1u);
-        }
-    } else {
+    for (int h = 0; h < 4; ++h) w[h] = wsm[h];
+    for (int m = warp >> 2; m < nsub; m += kSplitWarps / 4) {  // (uniform per warp)
+        float dv[4];
+        tc::ld4(tc::taddr(d, 32 * q, 16u * m), dv);
+        const int lr = m * 128 + 32 * q + lane;
+        if (lr < nreg) {
+            float sc = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) a[k] = ra[k ^ sw];
-        const float sa = score_row1(a, qh, w);
-        if (t < nreg) {
-            scores[t] = sa;
-            if (keep) keep[t] = sa;
-            atomicAdd(&s_hist[desc_key(sa) >> (32 - kHistBits)], 1u);
+            for (int h = 0; h < 4; ++h) sc = fmaf(fmaxf(dv[h], 0.0f), w[h], sc);
+            sc = __fadd_rn(sc, 0.0f);  // -0 -> +0
+            scores[lr] = sc;
+            if (keep) keep[lr] = sc;
+            atomicAdd(&s_hist[desc_key(sc) >> (32 - kHistBits)], 1u);
         }
     }
+    tc::fence_before_sync();
 }
 
 // ----------------------------------------------------------------- grid-wide steps
@@ -1006,6 +996,20 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
         if constexpr (HPG == 4) prefetch_tmap(&smap);
     }
     for (int i = tid; i < kHistBins; i += kSplitThreads) s_hist[i] = 0;
+    // the tensor cores' query tiles (rows 4-15 stay zero) and accumulators (HPG == 4)
+    uint8_t* qe_tiles = ring + kScoreStages * kTileBytes;
+    __shared__ __align__(8) uint64_t s_dbar2[2];
+    __shared__ uint32_t s_tmem;
+    if constexpr (HPG == 4) {
+        for (int i = tid; i < (int)(2 * kQeBytes / 16); i += kSplitThreads)
+            reinterpret_cast<uint4*>(qe_tiles)[i] = make_uint4(0, 0, 0, 0);
+        if (tid == 0) {
+            mbar_init(&s_dbar2[0], 1);
+            mbar_init(&s_dbar2[1], 1);
+        }
+        if (tid < 32) tc::alloc(&s_tmem, kScoreTmemCols);
+        tc::fence_before_sync();
+    }
     STEP5_STAMP(1, 0);
     __syncthreads();
     // With overlap_prologue the launch before this one writes none of the query,
@@ -1049,14 +1053,18 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
             // a short first tile, so that every SM starts scoring before the first
             // requests of all SMs have drained
             s_tile[0] = next_tile(p, wk, kBoxRows);
-            s_tile[1] = next_tile(p, wk);
+            for (int k = 1; k < kScoreStages; ++k) s_tile[k] = next_tile(p, wk);
         }
         const int pos0 = row_pos_or0(p, n0);
         const int pos1 = n1 == n0 ? pos0 : row_pos_or0(p, n1);
         load_rope<HPG>(p, pos0, o0);
         if (staged1 >= 0) load_rope<HPG>(p, pos1, o1);
     }
-    __syncthreads();  // s_tile, s_def
+    __syncthreads();  // s_tile, s_def (and the TMEM base)
+    if constexpr (HPG == 4) tc::fence_after_sync();
+    const uint32_t tmem = HPG == 4 ? s_tmem : 0u;
+    uint8_t* const qe0 = HPG == 4 ? qe_tiles : nullptr;
+    uint8_t* const qe1 = HPG == 4 ? qe_tiles + kQeBytes : nullptr;
     // thread 0 (the only one that reads summaries, through the copies it issues) waits
     // for the launch before once a tile may hold summaries that launch writes
     bool waited = !p.overlap_prologue;
@@ -1091,11 +1099,11 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
         }
     };
     if (tid == 0) {
-        if (s_tile[0].valid) issue(s_tile[0], 0);
-        if (s_tile[1].valid) issue(s_tile[1], 1);
+        for (int k = 0; k < kScoreStages; ++k)
+            if (s_tile[k].valid) issue(s_tile[k], k);
     }
-    finish_query<HPG>(p, r0, o0, s_qb[0]);
-    if (staged1 >= 0) finish_query<HPG>(p, r1, o1, s_qb[1]);
+    finish_query<HPG>(p, r0, o0, s_qb[0], qe0);
+    if (staged1 >= 0) finish_query<HPG>(p, r1, o1, s_qb[1], qe1);
     __syncthreads();  // staged queries visible
     STEP5_STAMP(1, 2);
 
@@ -1111,7 +1119,7 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
             QRope<HPG> o;
             load_query_raw<HPG>(p, x.n, x.g, r);
             load_rope<HPG>(p, x.pos, o);
-            finish_query<HPG>(p, r, o, s_qb[bsel]);
+            finish_query<HPG>(p, r, o, s_qb[bsel], bsel ? qe1 : qe0);
             if (bsel) staged1 = x.ng; else staged0 = x.ng;
             __syncthreads();
         }
@@ -1137,10 +1145,98 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
     };
 
     // ---------------- phase 1: scores and histograms
-    uint32_t ph0 = 0, ph1 = 0;
+    uint32_t phases = 0;  // bit k: the phase stage k waits for
     int st = 0, ntile = 0;
     bool ok = true;
-    for (;;) {
+    uint32_t dphases = 0;  // bit b: the phase accumulator b waits for
+    bool mma_fail = false;
+    if constexpr (HPG == 4) {
+        // Software pipeline over the tiles: tile t's products were issued in the previous
+        // iteration; once they are done its stage is refilled at once (the epilogue reads
+        // TMEM, not the stage), tile t + 1's products are issued into the other
+        // accumulator, and only then tile t's epilogue runs.
+        auto buffer_for = [&](const Tile& x, int busy) -> int {  // stages x's query if needed
+            int bsel = staged0 == x.ng ? 0 : staged1 == x.ng ? 1 : -1;
+            if (bsel < 0) {
+                bsel = busy == 0 ? 1 : 0;  // not the buffer the tile in flight reads
+                QRaw<HPG> r;
+                QRope<HPG> o;
+                load_query_raw<HPG>(p, x.n, x.g, r);
+                load_rope<HPG>(p, x.pos, o);
+                finish_query<HPG>(p, r, o, s_qb[bsel], bsel ? qe1 : qe0);
+                if (bsel) staged1 = x.ng; else staged0 = x.ng;
+                __syncthreads();
+            }
+            return bsel;
+        };
+        // waits (thread 0) for the copy of the tile in stage k, issues its products
+        auto start_tile = [&](int k, const Tile& x, int buf, int acc) -> bool {
+            bool got = true;
+            if (tid == 0) {
+                got = mbar_wait(&s_bar[k], (phases >> k) & 1u);
+                if (got) tc_tile_issue(ring + k * kTileBytes, buf ? qe1 : qe0, x.c1 - x.c0, tmem + 128u * acc,
+                                       &s_dbar2[acc]);
+            }
+            phases ^= 1u << k;
+            return !__syncthreads_or(!got);
+        };
+        Tile cur = s_tile[0];
+        int buf = -1, hist_ng = -1;
+        if (cur.valid) {
+            buf = buffer_for(cur, -1);
+            if (!start_tile(0, cur, buf, 0)) ok = false;
+        }
+        for (int t = 0; ok && cur.valid; ++t) {
+            if (ntile < 3) STEP5_STAMP(1, 3 + 2 * ntile);
+            // tile t's products done: its stage takes the walk's next tile
+            const int acc = t & 1;
+            const bool got = mbar_wait(&s_dbar2[acc], (dphases >> acc) & 1u);
+            dphases ^= 1u << acc;
+            tc::fence_after_sync();
+            if (tid == 0) {
+                const Tile nx = next_tile(p, wk);
+                s_tile[st] = nx;
+                if (nx.valid) {
+                    fence_proxy_async();
+                    issue(nx, st);
+                }
+            }
+            if (ntile < 3) STEP5_STAMP(1, 4 + 2 * ntile);
+            ++ntile;
+            // tile t + 1's products into the other accumulator (its last reader, tile t - 1's
+            // epilogue, finished before the end of the previous iteration)
+            const int nst = st + 1 == kScoreStages ? 0 : st + 1;
+            const Tile nxt = s_tile[nst];
+            int nbuf = -1;
+            bool ok2 = true;
+            if (nxt.valid) {
+                nbuf = buffer_for(nxt, buf);
+                ok2 = start_tile(nst, nxt, nbuf, acc ^ 1);
+            }
+            // tile t's epilogue (the shared histogram counts one (row, group) at a time)
+            if (cur.ng != hist_ng) {
+                if (hist_ng >= 0) {
+                    flush_hist(hist_ng);
+                    __syncthreads();  // every bin is flushed before it is cleared
+                    for (int i = tid; i < kHistBins; i += kSplitThreads) s_hist[i] = 0;
+                    __syncthreads();
+                }
+                hist_ng = cur.ng;
+            }
+            const int64_t x0 = (int64_t)cur.ng * p.r_cap + cur.c0;
+            float* keep = keep_all ? s_keep + (int)(x0 - xbeg) : nullptr;
+            tc_tile_epilogue(cur.c1 - cur.c0, tmem + 128u * acc, s_qb[buf].w, p.scores + x0, keep, s_hist);
+            if (__syncthreads_or(!got || !ok2)) {
+                mma_fail = true;
+                ok = false;
+                break;
+            }
+            cur = nxt;
+            buf = nbuf;
+            st = nst;
+        }
+        seg_ng = hist_ng;
+    } else for (;;) {
         const Tile cur = s_tile[st];
         if (!cur.valid) break;
         if (cur.ng != seg_ng) {
@@ -1155,29 +1251,30 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
         // one thread waits for the tile; the barrier releases the others (they do not
         // spin on the issue slots the other block of the SM is computing with)
         bool got = true;
-        if (tid == 0) got = mbar_wait(&s_bar[st], st ? ph1 : ph0);
+        if (tid == 0) got = mbar_wait(&s_bar[st], (phases >> st) & 1u);
         if (__syncthreads_or(!got)) {
             ok = false;
             break;
         }
         if (ntile < 3) STEP5_STAMP(1, 4 + 2 * ntile);
         ++ntile;
-        if (st) ph1 ^= 1u; else ph0 ^= 1u;
+        phases ^= 1u << st;
         const int64_t x0 = (int64_t)cur.ng * p.r_cap + cur.c0;
         float* scores = p.scores + x0;
         float* keep = keep_all ? s_keep + (int)(x0 - xbeg) : nullptr;
         const int nreg = cur.c1 - cur.c0;
-        if constexpr (HPG == 4) {
-            score_tile_rows(ring + st * kTileBytes, nreg, reinterpret_cast<const uint4*>(s_qb[qbuf].qh), w4,
-                            scores, keep, s_hist);
-        } else {
+        {
             const uint4* tile = reinterpret_cast<const uint4*>(ring + st * kTileBytes);
             if (nreg == kTileRegions)
                 score_tile<HPG, true>(f, tile, nreg, scores, keep, s_hist, qd, slot);
             else
                 score_tile<HPG, false>(f, tile, nreg, scores, keep, s_hist, qd, slot);
         }
-        __syncthreads();  // every thread is done with this stage before it is refilled
+        // every thread is done with this stage (and the accumulators) before it is refilled
+        if (__syncthreads_or(mma_fail)) {
+            ok = false;
+            break;
+        }
         if (tid == 0) {
             const Tile nx = next_tile(p, wk);
             s_tile[st] = nx;
@@ -1186,16 +1283,30 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
                 issue(nx, st);
             }
         }
-        st ^= 1;
+        st = st + 1 == kScoreStages ? 0 : st + 1;
     }
     if (!ok) {
         if (tid == 0) {
             raise_status(p.status, kDevTimeout);
             // give copies still in flight a bounded chance to land before the block exits
-            if (s_tile[st].valid) mbar_wait(&s_bar[st], st ? ph1 : ph0);
-            if (s_tile[st ^ 1].valid) mbar_wait(&s_bar[st ^ 1], st ? ph0 : ph1);
+            for (int k = 0; k < kScoreStages; ++k)
+                if (s_tile[k].valid) mbar_wait(&s_bar[k], (phases >> k) & 1u);
+            if (HPG == 4 && mma_fail) {  // the products in flight
+                mbar_wait(&s_dbar2[0], dphases & 1u);
+                mbar_wait(&s_dbar2[1], (dphases >> 1) & 1u);
+            }
+        }
+        if constexpr (HPG == 4) {
+            tc::fence_before_sync();
+            __syncthreads();
+            if (tid < 32) tc::dealloc(tmem, kScoreTmemCols);
         }
         return;
+    }
+    if constexpr (HPG == 4) {  // the accumulators are not needed past the scoring
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid < 32) tc::dealloc(tmem, kScoreTmemCols);
     }
     STEP5_STAMP(1, 9);
     if (seg_ng >= 0) flush_hist(seg_ng);

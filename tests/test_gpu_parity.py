@@ -152,17 +152,41 @@ def test_tensor_core_scoring_many_rows(s5, cfg):
     full_check(s5, geom, w, t, path=3, chain=False)
 
 
-def test_paths_agree_bit_for_bit(s5):
+def test_paths_agree(s5):
+    """The three scoring paths on the same inputs: the e4m3 products are exact on the CUDA
+    cores and on the tensor cores, so the scores agree to fp32 summation order (within
+    the score tolerance of each other); the picks agree except where two regions' scores
+    are within that tolerance, and each path's picks are exactly the oracle's selection
+    of its own scores."""
     geom = s5.STEP5_GEOMETRY
     w = S.workload({"positions": [5000, 9000, 12001, 700, 3], "B": 2}, seed=17)
     t = S.materialize(w, device="cuda")
-    a = run_path(s5, geom, w, t, path=1)
-    b = run_path(s5, geom, w, t, path=2)
-    for k in ("sel_ids", "sel_count", "sel_scores", "out"):
-        assert np.array_equal(a[k], b[k]), k
+    res = {path: run_path(s5, geom, w, t, path=path) for path in (1, 2, 3)}
+    h = host_inputs(t)
     R = w.row_pos // 8
-    for n in range(w.N):
-        assert np.array_equal(a["scores"][n, :, :R[n]], b["scores"][n, :, :R[n]])
+    hpg = geom.idx_heads // geom.num_kv_groups
+    for path, g in res.items():
+        assert g["status"] == 0
+        ids, cnt, _ = oracle.select_batch(g["scores"], w.row_pos, K=geom.top_k)
+        assert np.array_equal(ids, g["sel_ids"]) and np.array_equal(cnt, g["sel_count"]), path
+    a = res[1]
+    for path in (2, 3):
+        b = res[path]
+        assert np.array_equal(a["sel_count"], b["sel_count"])
+        for n in range(w.N):
+            bb = int(w.row_seq[n])
+            for gg in range(geom.num_kv_groups):
+                if R[n] == 0:
+                    continue
+                bound = score_term_bound(h["idx_q"][n, gg * hpg:(gg + 1) * hpg], h["w"][n, gg * hpg:(gg + 1) * hpg],
+                                         int(w.row_pos[n]), geom.rope_dims, a["summaries"][bb, gg, :R[n]],
+                                         h["cos"], h["sin"])
+                check_scores(b["scores"][n, gg, :R[n]], a["scores"][n, gg, :R[n]].astype(np.float64), 2 * bound,
+                             where=f"path {path} row {n} group {gg}")
+                check_selection_near_ties(b["sel_ids"][n, gg], int(b["sel_count"][n, gg]), a["sel_ids"][n, gg],
+                                          int(a["sel_count"][n, gg]), a["scores"][n, gg].astype(np.float64),
+                                          where=f"path {path} row {n} group {gg}")
+        check_out(b["out"], a["out"].astype(np.float64), where=f"path {path} vs 1")
 
 
 @pytest.mark.parametrize("over", [

@@ -152,7 +152,10 @@ def test_sharded_decode_matches_the_whole_row(s5, cfg, n_shards, seed):
 @pytest.mark.parametrize("workspace", [True, False])
 def test_one_shard_is_the_whole_row_bit_for_bit(s5, workspace):
     """One shard holding every token: the state, combined, is step5_sparse_attn's output
-    bit for bit (the same blocks and merge order; the combine's weight is exactly 1)."""
+    bit for bit (the same blocks and merge order; the combine's weight is exactly 1) when
+    the whole-row call takes the warp-level kernel the shard call takes (without a
+    workspace the whole-row call would otherwise take the tensor-core kernel, whose fp32
+    sums run in another order)."""
     geom = s5.STEP5_GEOMETRY
     w = S.workload({"positions": [30000, 4100, 70, 15], "B": 2}, seed=83)
     t = S.materialize(w, device="cuda")
@@ -167,8 +170,12 @@ def test_one_shard_is_the_whole_row_bit_for_bit(s5, workspace):
     out = torch.empty((w.N, geom.num_q_heads, geom.head_dim), dtype=torch.bfloat16, device=dev)
     s5.step5_attn_combine(geom, states, out)
     plain = torch.empty_like(out)
-    s5.step5_sparse_attn(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"], sel_ids, sel_count,
-                         plain, ws)
+    prev = s5.step5_set_attention_path(1)
+    try:
+        s5.step5_sparse_attn(geom, t["q"], t["k_cache"], t["v_cache"], t["row_seq"], t["row_pos"], sel_ids,
+                             sel_count, plain, ws)
+    finally:
+        s5.step5_set_attention_path(prev)
     torch.cuda.synchronize()
     assert s5.step5_device_status() == 0
     assert torch.equal(out.view(torch.int16), plain.view(torch.int16))
