@@ -152,6 +152,43 @@ def test_tensor_core_scoring_many_rows(s5, cfg):
     full_check(s5, geom, w, t, path=3, chain=False)
 
 
+def test_bulk_and_decode_summary_forms_agree_bit_for_bit(s5):
+    """Step (1) in one call over hundreds of regions per sequence (the vectorised bulk
+    form) and over the same regions a few at a time (the one-dim-per-thread form) write
+    the same codes and the same fp32 values, with and without rotation, and match the
+    oracle within the summary tolerance."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload({"positions": [2500, 2100], "B": 2}, seed=29)
+    t = S.materialize(w, device="cuda", with_kv=False)
+    h = host_inputs(t)
+    dev = t["idx_k"].device
+    R = [int(p) // 8 for p in w.row_pos]
+    for rope in (True, False):
+        cos, sin = (t["cos"], t["sin"]) if rope else (None, None)
+        outs = []
+        for step in (max(R), 5):
+            summ = torch.zeros_like(t["summaries"])
+            f32 = torch.full(t["summaries"].shape, float("nan"), dtype=torch.float32, device=dev)
+            for r0 in range(0, max(R), step):
+                rb = torch.tensor([min(r0, R[b]) for b in range(w.B)], dtype=torch.int32, device=dev)
+                re = torch.tensor([min(r0 + step, R[b]) for b in range(w.B)], dtype=torch.int32, device=dev)
+                s5.step5_region_summarize(geom, t["idx_k"], t["idx_z"], cos, sin, rb, re, summ, f32,
+                                          max_regions_per_seq=step)
+            torch.cuda.synchronize()
+            assert s5.step5_device_status() == 0
+            outs.append((summ.cpu().numpy(), f32.cpu().numpy()))
+        assert np.array_equal(outs[0][0], outs[1][0])
+        assert np.array_equal(outs[0][1].view(np.uint32), outs[1][1].view(np.uint32))
+        _, s64, _ = oracle.summarize_batch(h["idx_k"], h["idx_z"], h["cos"] if rope else None,
+                                           h["sin"] if rope else None, np.zeros(w.B, np.int32),
+                                           np.array(R, np.int32), w.r_cap, geom.rope_dims if rope else 0,
+                                           want_f64=True)
+        for b in range(w.B):
+            kreg = h["idx_k"][b, :, :8 * R[b]].reshape(4, R[b], 8, 64)
+            check_summaries(outs[0][0][b, :, :R[b]], outs[0][1][b, :, :R[b]], s64[b, :, :R[b]], kreg,
+                            geom.rope_dims if rope else 0, where=f"bulk seq {b}")
+
+
 def test_paths_agree(s5):
     """The three scoring paths on the same inputs: the e4m3 products are exact on the CUDA
     cores and on the tensor cores, so the scores agree to fp32 summation order (within
