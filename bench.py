@@ -395,10 +395,17 @@ def run_ours(args, rank, world, local_rank):
                     geom, t["q"], d["kc"], d["vc"], d["lo_t"], t["row_seq"], t["row_pos"], m_ids, m_cnt,
                     sh_states[i], d["ws"].tensor)
 
+            def shard_merge_attn(i):
+                d = parts[i]
+                return lambda: s5.step5_merge_attend_shard(
+                    geom, sh_ids, sh_sc, sh_cnt, t["q"], d["kc"], d["vc"], d["lo_t"], t["row_seq"], t["row_pos"],
+                    m_ids, m_cnt, sh_states[i], d["ws"].tensor)
+
             calls_s = ([shard_score(i) for i in range(n_shards)] +
                        [lambda: s5.step5_merge_topk(geom, sh_ids, sh_sc, sh_cnt, m_ids, m_cnt)] +
                        [shard_attn(i) for i in range(n_shards)] +
-                       [lambda: s5.step5_attn_combine(geom, sh_states, out_sh)])
+                       [lambda: s5.step5_attn_combine(geom, sh_states, out_sh)] +
+                       [shard_merge_attn(i) for i in range(n_shards)])
             for _ in range(warmup):
                 for fn in calls_s:
                     fn()
@@ -407,17 +414,22 @@ def run_ours(args, rank, world, local_rank):
             times_s, _ = time_calls(calls_s, steps_b)
             ts = times_s.mean(axis=0) * 1e3
             sc_us, at_us = ts[:n_shards], ts[n_shards + 1:2 * n_shards + 1]
+            comb_us = ts[2 * n_shards + 1]
+            ma_us = ts[2 * n_shards + 2:]
             res["shards"] = {
                 "shards": n_shards, "tokens_per_shard": cuts[1] - cuts[0],
                 "score_select_us": [round(float(x), 2) for x in sc_us],
                 "merge_us": round(float(ts[n_shards]), 2),
                 "attention_us": [round(float(x), 2) for x in at_us],
-                "combine_us": round(float(ts[-1]), 2),
-                "per_gpu_critical_path_us": round(float(sc_us.max() + ts[n_shards] + at_us.max() + ts[-1]), 2),
+                "combine_us": round(float(comb_us), 2),
+                "merge_attend_us": [round(float(x), 2) for x in ma_us],
+                "per_gpu_critical_path_us": round(float(sc_us.max() + ma_us.max() + comb_us), 2),
+                "per_gpu_critical_path_separate_calls_us": round(float(sc_us.max() + ts[n_shards] + at_us.max() +
+                                                                       comb_us), 2),
                 "picks_equal_whole_row": bool(torch.equal(m_ids, sel_ids) and torch.equal(m_cnt, sel_count)),
                 "out_max_abs_diff_vs_whole_row": float((out_sh.float() - out.float()).abs().max()),
-                "how": "calls timed one by one on one GPU; critical path = slowest shard's score + merge + "
-                       "slowest shard's attention + combine, without the exchange between GPUs"}
+                "how": "calls timed one by one on one GPU; critical path = slowest shard's score + slowest "
+                       "shard's step5_merge_attend_shard + combine, without the exchanges between GPUs"}
             del parts
             torch.cuda.empty_cache()
 

@@ -31,6 +31,7 @@ __all__ = [
     "step5_indexer_front",
     "step5_index_score_topk_noalloc",
     "step5_index_score_topk_shard", "step5_merge_topk", "step5_sparse_attn_shard", "step5_attn_combine",
+    "step5_merge_attend_shard",
     "RowsLayout", "step5_rows_layout_for", "HostRows", "step5_decode_step_host", "step5_set_host_copies",
     "step5_workspace_bytes", "step5_workspace_init", "step5_device_status",
     "step5_set_select_path", "step5_set_wait_polls", "step5_set_attention_path", "step5_select_path_for", "step5_set_prologue_overlap", "step5_decode_step", "step5_status_string", "step5_convert_bf16_to_e4m3",
@@ -107,6 +108,7 @@ def load():
         "step5_merge_topk": (i32, [G, i32, i32, P, P, P, P, P, P, P]),
         "step5_sparse_attn_shard": (i32, [G, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, sz, P]),
         "step5_attn_combine": (i32, [G, i32, i32, P, P, P, P]),
+        "step5_merge_attend_shard": (i32, [G, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]),
         "step5_rows_layout_for": (i32, [G, i32, i32, ctypes.POINTER(RowsLayout)]),
         "step5_decode_step_host": (i32, [G, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P, P,
                                          P, sz, P]),
@@ -331,6 +333,19 @@ def step5_sparse_attn_shard(geom, q, k_cache, v_cache, token_lo, row_seq, row_po
         ctypes.byref(Geometry.of(geom)), N, B, t_cap, int(token_lo), _ptr(q), _ptr(k_cache), _ptr(v_cache),
         _ptr(row_seq), _ptr(row_pos), _ptr(sel_ids), _ptr(sel_count), _ptr(states), _ptr(workspace),
         ws_bytes, _stream(stream)))
+
+
+def step5_merge_attend_shard(geom, shard_ids, shard_scores, shard_counts, q, k_cache, v_cache, token_lo, row_seq,
+                             row_pos, sel_ids, sel_count, states, workspace, stream=None):
+    """The merge of S shards' picks [S][N][G][K] into sel_ids/sel_count, then this shard's
+    attention states [N][Hq][130], in one call (see the header)."""
+    S, N = shard_ids.shape[0], shard_ids.shape[1]
+    B, _, t_cap, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("step5_merge_attend_shard", load().step5_merge_attend_shard(
+        ctypes.byref(Geometry.of(geom)), S, N, B, t_cap, int(token_lo), _ptr(shard_ids), _ptr(shard_scores),
+        _ptr(shard_counts), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(row_seq), _ptr(row_pos), _ptr(sel_ids),
+        _ptr(sel_count), _ptr(states), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def step5_attn_combine(geom, states, out, gate=None, stream=None):

@@ -236,7 +236,7 @@ struct MergeParams {
     uint32_t* status;
     int S, NG, top_k;
 };
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t stream, bool pdl);
 
 // out = (sum_s 2^(m_s - M) o_s) / (sum_s 2^(m_s - M) l_s), M = max_s m_s, per head row.
 struct CombineParams {

@@ -10,9 +10,9 @@
 // picks and the own region inside it (step5_sparse_attn_shard), each leaving a softmax
 // state (m, l, o per query head), and the states combine into the output.
 //
-// Merge: one block per (row, KV group); the S lists (each in key order) are staged in
-// shared memory and every key's rank in the union is its place in its own list plus a
-// binary search in each other list; a key ranked below K is written at its rank.
+// Merge: up to 16 blocks per (row, KV group); each stages the S lists (each in key order)
+// in shared memory, and every key's rank in the union is its place in its own list plus
+// a binary search in each other list; a key ranked below K is written at its rank.
 // Combine: one warp per (row, query head), lanes over 4 output dims each.
 #include "kernels.cuh"
 
@@ -31,11 +31,17 @@ __device__ __forceinline__ int count_below(const uint64_t* lst, int n, int top, 
     return at;
 }
 
+// Grid (splits, NG): every block of a (row, group) stages all S lists and ranks the keys
+// of its slice of them (keys j with j % splits == its index), so that a (row, group)'s
+// ranking is spread over several SMs; block 0 writes the padding and the count.
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint64_t* keys = reinterpret_cast<uint64_t*>(smem_raw);  // [S][K], unused slots ~0
     __shared__ int s_cnt[kMaxShards];
-    const int ng = blockIdx.x, tid = threadIdx.x;
+    const int ng = blockIdx.y, tid = threadIdx.x;
+    const int part = blockIdx.x, parts = gridDim.x;
+    pdl_wait();
+    pdl_launch_dependents();  // the attention after the merge may take its SMs now
     const int K = p.top_k, S = p.S;
     const int64_t NGK = (int64_t)p.NG * K;
     if (tid < S) {
@@ -65,7 +71,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeParams p) {
     while (2 * top <= K) top *= 2;
     // a key's rank in the union: its place in its own list plus the keys below it in
     // each other list (keys are distinct: ids are)
-    for (int j = tid; j < S * K; j += kMergeThreads) {
+    for (int j = part + parts * tid; j < S * K; j += parts * kMergeThreads) {
         const int s = j / K, i = j - s * K;
         if (i >= s_cnt[s]) continue;
         const uint64_t key = keys[j];
@@ -77,6 +83,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(MergeParams p) {
             if (ss) ss[rank] = score_of_desc_key((uint32_t)(key >> 32));
         }
     }
+    if (part != 0) return;
     const int take = total < K ? total : K;
     for (int i = take + tid; i < K; i += kMergeThreads) {
         ids[i] = -1;
@@ -120,15 +127,27 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
 
 }  // namespace
 
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+cudaError_t launch_merge(const MergeParams& p, int num_sms, cudaStream_t stream, bool pdl) {
     static std::atomic<uint64_t> attr{0};
     cudaError_t e = once_per_device(attr, [] {
         return cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)((size_t)kMaxShardKeys * 8));
     });
     if (e != cudaSuccess) return e;
-    merge_kernel<<<p.NG, kMergeThreads, (size_t)p.S * p.top_k * 8, stream>>>(p);
-    return cudaGetLastError();
+    // blocks per (row, group): as many as fill the SMs once, up to 16
+    int parts = p.NG > 0 ? num_sms / p.NG : 1;
+    parts = parts < 1 ? 1 : (parts > 16 ? 16 : parts);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)parts, (unsigned)p.NG, 1);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = (size_t)p.S * p.top_k * 8;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr1[1];
+    attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr1[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr1;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, merge_kernel, p);
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {

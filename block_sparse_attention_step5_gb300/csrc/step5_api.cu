@@ -625,16 +625,21 @@ step5_status step5_sparse_attn_shard(const step5_geometry* geom, int32_t N, int3
                      sel_count, nullptr, workspace, workspace_bytes, stream, true, nullptr, states_f32, token_lo);
 }
 
-step5_status step5_merge_topk(const step5_geometry* geom, int32_t S, int32_t N, const int32_t* shard_ids,
-                              const float* shard_scores, const int32_t* shard_counts, int32_t* sel_ids,
-                              int32_t* sel_count, float* sel_scores_or_null, step5_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+step5_status merge_impl(const step5_geometry* geom, int32_t S, int32_t N, const int32_t* shard_ids,
+                        const float* shard_scores, const int32_t* shard_counts, int32_t* sel_ids, int32_t* sel_count,
+                        float* sel_scores_or_null, step5_stream_t stream, bool launch) {
     step5_status s = check_geometry(geom);
     if (s != STEP5_OK) return s;
     if (S <= 0 || N <= 0) return STEP5_ERR_INVALID_ARGUMENT;
     if (!shard_ids || !shard_scores || !shard_counts || !sel_ids || !sel_count) return STEP5_ERR_INVALID_ARGUMENT;
     const int64_t NG = (int64_t)N * geom->num_kv_groups;
-    if (NG > INT32_MAX) return STEP5_ERR_INVALID_ARGUMENT;
+    if (NG > 65535) return STEP5_ERR_UNSUPPORTED;
     if (S > kMaxShards || (int64_t)S * geom->top_k > kMaxShardKeys) return STEP5_ERR_UNSUPPORTED;
+    if (!launch) return STEP5_OK;
     uint32_t* st = status_ptr();
     if (!st) return STEP5_ERR_CUDA;
     MergeParams p;
@@ -648,7 +653,40 @@ step5_status step5_merge_topk(const step5_geometry* geom, int32_t S, int32_t N, 
     p.S = S;
     p.NG = (int)NG;
     p.top_k = geom->top_k;
-    return launch_merge(p, (cudaStream_t)stream) == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
+    return launch_merge(p, num_sms(), (cudaStream_t)stream, use_pdl()) == cudaSuccess ? STEP5_OK : STEP5_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+step5_status step5_merge_topk(const step5_geometry* geom, int32_t S, int32_t N, const int32_t* shard_ids,
+                              const float* shard_scores, const int32_t* shard_counts, int32_t* sel_ids,
+                              int32_t* sel_count, float* sel_scores_or_null, step5_stream_t stream) {
+    return merge_impl(geom, S, N, shard_ids, shard_scores, shard_counts, sel_ids, sel_count, sel_scores_or_null,
+                      stream, true);
+}
+
+step5_status step5_merge_attend_shard(const step5_geometry* geom, int32_t S, int32_t N, int32_t B,
+                                      int32_t t_cap_local, int32_t token_lo, const int32_t* shard_ids,
+                                      const float* shard_scores, const int32_t* shard_counts, const void* q_bf16,
+                                      const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
+                                      const int32_t* row_pos, int32_t* sel_ids, int32_t* sel_count,
+                                      float* states_f32, void* workspace, size_t workspace_bytes,
+                                      step5_stream_t stream) {
+    // every argument is checked before anything is enqueued
+    step5_status s = merge_impl(geom, S, N, shard_ids, shard_scores, shard_counts, sel_ids, sel_count, nullptr,
+                                stream, false);
+    if (s != STEP5_OK) return s;
+    if (states_f32 == nullptr) return STEP5_ERR_INVALID_ARGUMENT;
+    s = attn_impl(geom, N, B, t_cap_local, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids, sel_count,
+                  nullptr, workspace, workspace_bytes, stream, false, nullptr, states_f32, token_lo);
+    if (s != STEP5_OK) return s;
+    s = merge_impl(geom, S, N, shard_ids, shard_scores, shard_counts, sel_ids, sel_count, nullptr, stream, true);
+    if (s != STEP5_OK) return s;
+    // the attention launch waits for the merge through its programmatic-launch wait
+    return attn_impl(geom, N, B, t_cap_local, q_bf16, k_cache_bf16, v_cache_bf16, row_seq, row_pos, sel_ids,
+                     sel_count, nullptr, workspace, workspace_bytes, stream, true, nullptr, states_f32, token_lo);
 }
 
 step5_status step5_attn_combine(const step5_geometry* geom, int32_t S, int32_t N, const float* states_f32,

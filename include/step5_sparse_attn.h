@@ -252,11 +252,27 @@ step5_status step5_index_score_topk_shard(const step5_geometry* geom, int32_t N,
  * it; ids distinct across shards), in ascending key order; the rest of sel_ids is -1
  * (sel_scores -inf).  shard_ids, shard_scores: [S][N][G][top_k]; shard_counts [S][N][G];
  * sel_ids [N][G][top_k]; sel_count [N][G]; sel_scores_or_null [N][G][top_k] or NULL.
- * 1 <= S <= 32 and S * top_k <= 16384, else STEP5_ERR_UNSUPPORTED.  A count outside
- * [0, top_k] raises STEP5_DEV_RANGE and is clamped. */
+ * 1 <= S <= 32, S * top_k <= 16384 and N * G <= 65535, else STEP5_ERR_UNSUPPORTED.  A
+ * count outside [0, top_k] raises STEP5_DEV_RANGE and is clamped. */
 step5_status step5_merge_topk(const step5_geometry* geom, int32_t S, int32_t N, const int32_t* shard_ids,
                               const float* shard_scores, const int32_t* shard_counts, int32_t* sel_ids,
                               int32_t* sel_count, float* sel_scores_or_null, step5_stream_t stream);
+
+/* step5_merge_topk, then step5_sparse_attn_shard on the merged pick, in one call (no
+ * counterpart in the pages: the composition a shard runs once the shards' picks have
+ * been exchanged): sel_ids [N][G][top_k] and sel_count [N][G] receive the row's pick
+ * (as step5_merge_topk writes them; no picked-score export), and states_f32 this
+ * shard's attention states (as step5_sparse_attn_shard writes them).  The attention
+ * launch starts while the merge runs and waits for it on the device.  Every argument of
+ * both calls is checked before anything is enqueued; layouts, limits and errors are
+ * those of the two calls. */
+step5_status step5_merge_attend_shard(const step5_geometry* geom, int32_t S, int32_t N, int32_t B,
+                                      int32_t t_cap_local, int32_t token_lo, const int32_t* shard_ids,
+                                      const float* shard_scores, const int32_t* shard_counts, const void* q_bf16,
+                                      const void* k_cache_bf16, const void* v_cache_bf16, const int32_t* row_seq,
+                                      const int32_t* row_pos, int32_t* sel_ids, int32_t* sel_count,
+                                      float* states_f32, void* workspace, size_t workspace_bytes,
+                                      step5_stream_t stream);
 
 /* Step (4) on one shard: the shard's caches k_cache_bf16, v_cache_bf16
  * [B][G][t_cap_local][head_dim] hold tokens token_lo .. token_lo + t_cap_local - 1 of

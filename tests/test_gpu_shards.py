@@ -235,3 +235,38 @@ def test_merge_at_its_limits(s5, S_, K):
             assert c == len(ref)
             assert np.array_equal(got_ids[n, g, :c], ref)
             assert np.all(got_ids[n, g, c:] == -1) and np.all(np.isneginf(got_sc[n, g, c:]))
+
+
+@pytest.mark.parametrize("cfg,n_shards,seed", CASES[:2])
+def test_merge_attend_composition_matches_the_two_calls(s5, cfg, n_shards, seed):
+    """step5_merge_attend_shard (the merge, then the shard's attention, launched back to
+    back with the attention waiting on the device) writes the merged pick and each shard's
+    states bit for bit as step5_merge_topk and step5_sparse_attn_shard do."""
+    geom = s5.STEP5_GEOMETRY
+    w = S.workload(cfg, seed=seed)
+    t = S.materialize(w, device="cuda")
+    g = run_path(s5, geom, w, t, path=0)
+    dev = t["q"].device
+    sel_ids = torch.from_numpy(g["sel_ids"]).to(dev)
+    sel_count = torch.from_numpy(g["sel_count"]).to(dev)
+    cuts = token_cuts(w.t_cap, n_shards, seed)
+    r = run_shards(s5, geom, w, t, cuts, sel_ids, sel_count)
+    N, G, K = w.N, geom.num_kv_groups, geom.top_k
+    for s in range(n_shards):
+        lo_t, hi_t = cuts[s], cuts[s + 1]
+        kc = t["k_cache"][:, :, lo_t:hi_t].contiguous()
+        vc = t["v_cache"][:, :, lo_t:hi_t].contiguous()
+        ws = s5.Workspace.create(geom, N, w.r_cap, device=dev).tensor if s % 2 == 0 else None
+        c_ids = torch.full((N, G, K), -7, dtype=torch.int32, device=dev)
+        c_cnt = torch.full((N, G), -7, dtype=torch.int32, device=dev)
+        c_states = torch.full((N, geom.num_q_heads, SLOT), float("nan"), dtype=torch.float32, device=dev)
+        s5.step5_merge_attend_shard(geom, r["ids"], r["scs"], r["cnt"], t["q"], kc, vc, lo_t, t["row_seq"],
+                                    t["row_pos"], c_ids, c_cnt, c_states, ws)
+        # the reference states with the same workspace choice
+        ref_states = torch.empty_like(c_states)
+        s5.step5_sparse_attn_shard(geom, t["q"], kc, vc, lo_t, t["row_seq"], t["row_pos"], r["m_ids"], r["m_cnt"],
+                                   ref_states, ws)
+        torch.cuda.synchronize()
+        assert s5.step5_device_status() == 0
+        assert torch.equal(c_ids, r["m_ids"]) and torch.equal(c_cnt, r["m_cnt"])
+        assert torch.equal(c_states.view(torch.int32), ref_states.view(torch.int32))
