@@ -50,8 +50,11 @@ static_assert((16 * 128 + kAttnMaxSplits) * 4 <= kStageBytes, "split merge area 
 static_assert((kMaxTopK + 2) * 4 + (kAttnWarps * 16 + 32 + 16 * kAttnMaxSplits + 16) * 4 <= kAttnStaticSmem,
               "static shared memory");
 
-// Dynamic shared memory: [stage area | barriers]
-size_t attn_smem_bytes() { return 1024 + kStageBytes + kBarBytes; }
+// Dynamic shared memory: [stage area | barriers | (cluster form) this block's state]
+constexpr int kClusterStateBytes = 16 * kAttnSlotFloats * 4;
+size_t attn_smem_bytes(bool cluster = false) {
+    return 1024 + kStageBytes + kBarBytes + (cluster ? kClusterStateBytes : 0);
+}
 
 // Shared-memory byte offset of (token row t, 16-byte chunk c16 of the 256-byte row) in a
 // region tile written by two 64-dim TMA boxes with 128-byte swizzle.
@@ -71,7 +74,9 @@ __device__ __forceinline__ float gate_factor(const AttnParams& p, int n, int h) 
 // kShard: a shard of the rows' tokens (tokens tok_lo .. tok_lo + t_cap - 1 of each
 // sequence in the caches; keys outside are skipped; softmax states out instead of the
 // output).  A separate instantiation, so that the whole-row kernel carries none of it.
-template <bool kShard>
+// kCluster: the S blocks of a (row, group) form one thread-block cluster and exchange
+// their states through distributed shared memory instead of the workspace (S <= 16).
+template <bool kShard, bool kCluster = false>
 __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                 const __grid_constant__ CUtensorMap vmap,
                                                                 AttnParams p) {
@@ -104,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     const int b = p.row_seq[n];
     const int pos = p.row_pos[n];
     int cnt = p.sel_count[ng];
-    const uint32_t epoch = S > 1 ? __ldcg(p.bar + ng) : 0u;
+    const uint32_t epoch = (S > 1 && !kCluster) ? __ldcg(p.bar + ng) : 0u;
     __syncthreads();
     STEP5_STAMP(4, 8);
     // (a shard's position may lie past its tokens)
@@ -414,6 +419,70 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
         return;
     }
 
+    if constexpr (kCluster) {
+        // ---- S blocks per (row, group) in one cluster: this block's state into its own
+        // shared memory, a cluster barrier, then a slice of the outputs merged over the S
+        // states read through distributed shared memory, and a second barrier so that no
+        // block leaves while another still reads its state.  Every block of the cluster
+        // reaches both barriers (the early exits above are the same for all of them).
+        float* st = reinterpret_cast<float*>(smem + kStageBytes + kBarBytes);  // [hq_g][130]
+        for (int r = rpar; r < hq_g; r += 2) {
+            float O = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kAttnWarps; ++w) O += mall[w * kMergeFloatsPerWarp + r * kMergeRow + d] * s_wsc[w][r];
+            st[r * kSlotFloats + 2 + d] = O;
+            if (d == 0) {
+                st[r * kSlotFloats] = s_M[r];
+                st[r * kSlotFloats + 1] = s_L[r];
+            }
+        }
+        STEP5_STAMP(4, 11);
+        cluster_sync();
+        STEP5_STAMP(4, 6);
+        const uint32_t st_addr = smem_u32(st);
+        const int EO = hq_g * 128;
+        const int e_lo = EO * split / S, e_hi = EO * (split + 1) / S, nout = e_hi - e_lo;
+        __shared__ float s_cw[16][16], s_cL[16];  // weight of split sp for a slice row; row sums
+        const int r_lo = e_lo >> 7, r_hi = (e_hi - 1) >> 7;
+        for (int r = r_lo + warp; r <= r_hi; r += kAttnWarps) {  // lanes take splits
+            const bool on = lane < S;
+            const uint32_t at = st_addr + (uint32_t)(r * kSlotFloats) * 4u;
+            const float m = on ? ld_cluster_f32(map_cluster(at, lane)) : -INFINITY;
+            const float l = on ? ld_cluster_f32(map_cluster(at + 4u, lane)) : 0.0f;
+            float M = m;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float sc = exp2f(m - ((M == -INFINITY) ? 0.0f : M));
+            float L = l * sc;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+            if (on) s_cw[r - r_lo][lane] = sc;
+            if (lane == 0) {
+                s_cL[r - r_lo] = L;
+                if constexpr (kShard) {
+                    float* gs = p.states + ((int64_t)n * p.Hq + (int64_t)g * hq_g + r) * kSlotFloats;
+                    gs[0] = M;
+                    gs[1] = L;
+                }
+            }
+        }
+        __syncthreads();
+        for (int t = tid; t < nout; t += kThreads) {
+            const int e = e_lo + t, r = e >> 7;
+            const uint32_t at = st_addr + (uint32_t)(r * kSlotFloats + 2 + (e & 127)) * 4u;
+            float O = 0.0f;
+            for (int sp = 0; sp < S; ++sp) O += ld_cluster_f32(map_cluster(at, sp)) * s_cw[r - r_lo][sp];
+            const int64_t hrow = (int64_t)n * p.Hq + (int64_t)g * hq_g + r;
+            if constexpr (kShard)
+                p.states[hrow * kSlotFloats + 2 + (e & 127)] = O;
+            else
+                p.out[hrow * 128 + (e & 127)] = f32_to_bf16_bits(O / s_cL[r - r_lo] * gate_factor(p, n, g * hq_g + r));
+        }
+        STEP5_STAMP(4, 7);
+        cluster_sync();
+        return;
+    }
+
     // ---- S blocks per (row, group): this block's state into the workspace
     const float* pall = p.part + ng * S * hq_g * kSlotFloats;  // [S][hq_g][130]
     {
@@ -530,14 +599,20 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     STEP5_STAMP(4, 7);
 }
 
-// Sets the kernel's shared-memory limit once, then launches it.
-template <bool kShard>
+// Sets the kernel's shared-memory limit once, then launches it (kCluster: the split
+// blocks of a (row, group) as one cluster of p.splits blocks).
+template <bool kShard, bool kCluster = false>
 cudaError_t launch_sparse_attn(const AttnParams& p, int N, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t stream, bool pdl) {
     static std::atomic<uint64_t> attr_set{0};
     cudaError_t e = once_per_device(attr_set, [] {
-        return cudaFuncSetAttribute(sparse_attn_kernel<kShard>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)attn_smem_bytes());
+        cudaError_t e1 = cudaFuncSetAttribute(sparse_attn_kernel<kShard, kCluster>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)attn_smem_bytes(kCluster));
+        if (e1 == cudaSuccess && kCluster)
+            e1 = cudaFuncSetAttribute(sparse_attn_kernel<kShard, kCluster>,
+                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return e1;
     });
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -545,14 +620,25 @@ cudaError_t launch_sparse_attn(const AttnParams& p, int N, const CUtensorMap& km
     // prefill chunk, 1/G of the K/V it reads), which then stays in L2
     cfg.gridDim = dim3(p.splits, N, p.G);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = attn_smem_bytes();
+    cfg.dynamicSmemBytes = attn_smem_bytes(kCluster);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (kCluster) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.splits;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, sparse_attn_kernel<kShard>, kmap, vmap, p);
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, sparse_attn_kernel<kShard, kCluster>, kmap, vmap, p);
 }
 
 }  // namespace

@@ -210,6 +210,12 @@ struct AttnParams {
 static_assert(sizeof(AttnParams) == 128, "attention parameter block");
 cudaError_t launch_attention(const AttnParams& p, int N, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream, bool pdl);
+// the split blocks of a (row, group) as one thread-block cluster (p.splits <= 16), their
+// states merged through distributed shared memory (no workspace area used)
+cudaError_t launch_attention_cluster(const AttnParams& p, int N, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                     cudaStream_t stream, bool pdl);
+constexpr int kAttnMaxCluster = 16;
+int attention_max_clusters(int splits);  // clusters of this many blocks the GPU holds at once
 // the shard instantiation (p.states in place of p.out)
 cudaError_t launch_attention_shard(const AttnParams& p, int N, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                    cudaStream_t stream, bool pdl);

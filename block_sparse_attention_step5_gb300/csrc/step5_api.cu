@@ -21,7 +21,7 @@ int32_t g_select_path = 0;  // 0 auto, 1 fused, 2 split
 int32_t g_overlap_prologue = 0;
 int32_t g_host_copies = 0;  // step5_decode_step_host: 1 = always through copies
 uint32_t g_wait_polls = 0;  // split path's waits on other blocks: 0 = kBarrierPolls
-int32_t g_attn_path = 0;    // step (4) without a split: 0 auto (tensor cores), 1 warp MMA kernel, 2 tensor cores
+int32_t g_attn_path = 0;    // step (4): 0 auto (split: cluster; one block per pair: tensor cores), 1 warp MMA kernel, 2 tensor cores
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -520,6 +520,23 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     if (!st) return STEP5_ERR_CUDA;
     int splits, eps;
     attn_plan(geom, N, use_area, &splits, &eps, true);
+    // the split blocks of a (row, group) as one cluster merging through distributed
+    // shared memory (whole rows, automatic path): the largest cluster of at most 16
+    // blocks whose clusters for every pair fit the GPCs at once (a cluster must sit in
+    // one GPC; a second wave of clusters would cost more than the merge saves)
+    bool cluster = false;
+    if (states == nullptr && g_attn_path == 0 && splits > 1) {
+        const int64_t pairs = (int64_t)N * geom->num_kv_groups;
+        for (int cs = splits < kAttnMaxCluster ? splits : kAttnMaxCluster; cs >= 2; --cs) {
+            if (attention_max_clusters(cs) >= pairs) {
+                cluster = true;
+                splits = cs;
+                eps = (geom->top_k + 1 + splits - 1) / splits;
+                eps = (eps + 1) / 2 * 2;
+                break;
+            }
+        }
+    }
     CUtensorMap kmap, vmap;
     if (!cache_maps(k_cache_bf16, v_cache_bf16, rows, &kmap, &vmap)) return STEP5_ERR_CUDA;
     AttnParams p;
@@ -551,6 +568,8 @@ step5_status attn_impl(const step5_geometry* geom, int32_t N, int32_t B, int32_t
     cudaError_t e;
     if (states != nullptr)
         e = launch_attention_shard(p, N, kmap, vmap, (cudaStream_t)stream, use_pdl());
+    else if (cluster)
+        e = launch_attention_cluster(p, N, kmap, vmap, (cudaStream_t)stream, use_pdl());
     else if (splits == 1 && g_attn_path != 1)
         e = launch_attention_tc(p, N, kmap, vmap, (cudaStream_t)stream, use_pdl());
     else

@@ -391,12 +391,15 @@ step5_status step5_device_status(uint32_t* flags_out, step5_stream_t stream);
  * seconds).  Process-wide, read when a call is enqueued.  Returns the previous limit. */
 uint32_t step5_set_wait_polls(uint32_t polls);
 
-/* Kernel of step5_sparse_attn (and the gated call) when a (row, group)'s keys are not
- * split over several blocks (many (row, group) pairs, or no workspace): 0 = automatic
- * (the tensor-core kernel), 1 = the warp-level MMA kernel, 2 = the tcgen05 tensor-core
- * kernel.  Both give the output within rounding of each other (different fp32 summation
- * orders); a testing and tuning switch.  Process-wide; other values are ignored.  Returns
- * the previous value. */
+/* Kernels of step5_sparse_attn (and the gated call): 0 = automatic: with few
+ * (row, group) pairs and a workspace, each pair's keys split over up to 16 blocks of one
+ * thread-block cluster that merge their softmax states through distributed shared
+ * memory (the workspace area is not used); otherwise one tcgen05 tensor-core CTA per
+ * pair.  1 = the warp-level MMA kernel throughout, its splits (up to 64 blocks per pair)
+ * merged through the workspace.  2 = one tensor-core CTA per pair, never split.  The
+ * outputs agree within rounding (the fp32 sums run in different orders); each path is
+ * deterministic.  A testing and tuning switch; process-wide; other values are ignored.
+ * Returns the previous value. */
 int32_t step5_set_attention_path(int32_t mode);
 
 /* Selection path of step5_index_score_topk: 0 = automatic, 1 = one block per
