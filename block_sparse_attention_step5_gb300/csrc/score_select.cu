@@ -209,12 +209,25 @@ __device__ __forceinline__ float score_from_vec(const QFrag<HPG>& f, uint4 v) {
 constexpr int kRadixBits = 11;
 constexpr int kRadixBins = 1 << kRadixBits;
 
+// The candidates (the K-th key's bin, once it holds at most kSelCands keys) live in the
+// first half of hist, and the counts of their own descent (kCandBits digits) after them.
+constexpr int kCandBits = 8;
+constexpr int kCandBins = 1 << kCandBits;
+constexpr int kSelCands = 512;
+constexpr int kSelRankMax = 24;  // a bin or a sort segment this small is ranked pairwise
+static_assert(kSelCands * 2 + kCandBins <= kRadixBins, "candidates and their counts fit the histogram");
+
 struct TopkSmem {
     uint32_t hist[kRadixBins];
     uint32_t wsum[32];
-    uint32_t count;
+    uint32_t count, ncand, nmem;
     uint32_t v, before, inbin;
+    uint32_t kmin, kmax;  // range of the score keys
+    uint32_t segmax;      // longest segment of the counting sort
 };
+
+// Scratch of the selection and its sort, in 64-bit keys.
+__host__ __device__ constexpr int sel_aux_slots(int P2) { return P2 > kSelCands ? P2 : kSelCands; }
 
 // Bitonic sort, ascending, of P2 (a power of two >= 32) keys in shared memory.  Stages
 // whose partner distance is below 32 run in registers with warp shuffles; the others
@@ -255,131 +268,423 @@ __device__ void block_bitonic_sort(uint64_t* s, int P2) {
     }
 }
 
-// Gathers the K smallest of cnt unique 64-bit keys (all of them if cnt <= K) into
-// s_sel[0..min(cnt, K)) in no particular order, pads s_sel up to P2 (a power of two >=
-// max(K, 32)) with ~0, returns min(cnt, K).  A radix descent over 11-bit digits (most
-// significant first) finds the K-th key; every key at or below it is gathered.  get(i)
-// returns key i.  Must be called by all NT threads of the block.
-template <int NT, class Get>
-__device__ int block_select_set(Get get, int cnt, int K, int P2, uint64_t* s_sel, TopkSmem& ts) {
+// The bin holding the need-th smallest key (need >= 1) of the NB digit counts in hist:
+// ts.v = the bin, ts.before = keys in lower bins, ts.inbin = keys in the bin.  Called by
+// all NT threads once the counts are complete; ends with a barrier.
+template <int NT, int NB>
+__device__ void block_find_bin(const uint32_t* hist, uint32_t need, TopkSmem& ts) {
+    constexpr int PER = NB >= NT ? NB / NT : 1;  // bins per thread (threads past NB own none)
+    constexpr int NW = NT / 32;
+    static_assert(NB % NT == 0 || NT % NB == 0, "bins divide among the threads");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint64_t bound = ~0ull;
+    uint32_t loc[PER];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        loc[q] = tid * PER < NB ? hist[tid * PER + q] : 0u;
+        sum += loc[q];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) ts.wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < NW ? ts.wsum[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        if (lane < NW) ts.wsum[lane] = w;  // inclusive warp prefix
+    }
+    __syncthreads();
+    incl += warp ? ts.wsum[warp - 1] : 0u;
+    const uint32_t excl = incl - sum;
+    if (excl < need && need <= incl) {
+        uint32_t c = excl;
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            if (c + loc[q] >= need) {
+                ts.v = tid * PER + q;
+                ts.before = c;
+                ts.inbin = loc[q];
+                break;
+            }
+            c += loc[q];
+        }
+    }
+    __syncthreads();
+}
+
+// Exclusive scan, in place, of the NB counts in hist; the largest count goes to
+// ts.segmax (set to 0 beforehand).  Called by all NT threads; ends with a barrier.
+template <int NT, int NB>
+__device__ void block_excl_scan_bins(uint32_t* hist, TopkSmem& ts) {
+    constexpr int PER = NB / NT;
+    constexpr int NW = NT / 32;
+    static_assert(NB % NT == 0 && PER >= 1, "bins divide among the threads");  // NB >= NT here
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t loc[PER];
+    uint32_t sum = 0, mx = 0;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        loc[q] = hist[tid * PER + q];
+        sum += loc[q];
+        mx = max(mx, loc[q]);
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) atomicMax(&ts.segmax, mx);
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) ts.wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < NW ? ts.wsum[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        if (lane < NW) ts.wsum[lane] = w;
+    }
+    __syncthreads();
+    uint32_t c = incl - sum + (warp ? ts.wsum[warp - 1] : 0u);
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        hist[tid * PER + q] = c;
+        c += loc[q];
+    }
+    __syncthreads();
+}
+
+// Appends the keys of the lanes with `act` set to list[*ctr ...] (slots past cap dropped).
+__device__ __forceinline__ void warp_append(bool act, uint64_t key, uint64_t* list, uint32_t* ctr, uint32_t cap) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t am = __ballot_sync(0xffffffffu, act);
+    uint32_t slot = 0;
+    if (lane == 0 && am) slot = atomicAdd(ctr, (uint32_t)__popc(am));
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    if (act) {
+        const uint32_t idx = slot + __popc(am & ((1u << lane) - 1u));
+        if (idx < cap) list[idx] = key;
+    }
+}
+
+// Appends, for each set bit c of m, the key (u[c] << 32 | id0 + c) to list[*ctr ...]
+// (slots past cap dropped): one count scan and one atomic per warp, nothing when no lane
+// of the warp has a key.  Called by whole warps.
+__device__ __forceinline__ void warp_append4(uint32_t m, const uint32_t (&u)[4], int id0, uint64_t* list,
+                                             uint32_t* ctr, uint32_t cap) {
+    if (!__any_sync(0xffffffffu, m != 0u)) return;
+    const int lane = threadIdx.x & 31;
+    const uint32_t c = (uint32_t)__popc(m);
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    uint32_t slot = 0;
+    if (lane == 31) slot = atomicAdd(ctr, incl);
+    slot = __shfl_sync(0xffffffffu, slot, 31) + incl - c;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (m & (1u << q)) {
+            if (slot < cap) list[slot] = ((uint64_t)u[q] << 32) | (uint32_t)(id0 + q);
+            ++slot;
+        }
+    }
+}
+
+// Gathers the K smallest keys (desc(score) << 32 | id, i.e. by score key and then by id)
+// of ids 0..cnt-1 (all of them if cnt <= K) into s_sel[0..min(cnt, K)) in no particular
+// order, pads s_sel up to P2 (a power of two >= max(K, 32)) with ~0, returns min(cnt, K).
+// src(i) returns the 32-bit score key of id i and src.get4(j, cnt) those of ids 4j..4j+3
+// (entries past cnt undefined); s_aux holds sel_aux_slots(P2) keys of scratch.  Passes
+// over all keys, four per thread at a time: the range [smallest, largest] of the score
+// keys; then 11-bit digits below the bits that range fixes (scores of one row mostly
+// share sign and exponent), one pass each, until the K-th key's bin is taken whole,
+// holds at most kSelCands keys, or is one key value; then one pass that takes every key
+// below the bin and keeps the bin's keys as candidates.  The candidates descend by 8-bit
+// digits until their bin is taken whole or holds at most kSelRankMax keys, which are
+// ranked against each other by (key, id).  A single key value shared by more than
+// kSelCands keys is resolved by one warp taking the smallest ids in id order.  Must be
+// called by all NT threads of the block.
+template <int NT, class Src>
+__device__ int block_select_set(const Src& src, int cnt, int K, int P2, uint64_t* s_sel, uint64_t* s_aux,
+                                TopkSmem& ts) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n4 = (cnt + 3) >> 2;
+    uint64_t lo = 1ull << 32, hi_excl = 1ull << 32;  // keys below lo taken; [lo, hi_excl) the bin
+    int need = 0;                                   // keys still needed from the bin
+    int hi = 0;                                     // bits of the bin's keys at and above hi agree
+    int mode = 0;                                   // 0 bin taken whole, 1 candidates, 2 ties
     if (cnt > K) {
-        uint64_t prefix = 0;
-        int need = K;
-        int hi = 64;  // key bits at and above `hi` are fixed by `prefix`
-        while (hi > 0) {
+        if (tid == 0) {
+            ts.kmin = ~0u;
+            ts.kmax = 0u;
+        }
+        uint32_t mn = ~0u, mx = 0u;
+        for (int j = tid; j < n4; j += NT) {
+            const uint4 k = src.get4(j, cnt);
+            const int i0 = 4 * j;
+            mn = min(mn, k.x);
+            mx = max(mx, k.x);
+            if (i0 + 3 < cnt) {
+                mn = min(min(mn, k.y), min(k.z, k.w));
+                mx = max(max(mx, k.y), max(k.z, k.w));
+            } else {
+                if (i0 + 1 < cnt) { mn = min(mn, k.y); mx = max(mx, k.y); }
+                if (i0 + 2 < cnt) { mn = min(mn, k.z); mx = max(mx, k.z); }
+            }
+        }
+        mn = __reduce_min_sync(0xffffffffu, mn);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        __syncthreads();  // the range is initialised
+        if (lane == 0) {
+            atomicMin(&ts.kmin, mn);
+            atomicMax(&ts.kmax, mx);
+        }
+        __syncthreads();
+        const uint32_t kmin = ts.kmin, kmax = ts.kmax;
+        need = K;
+        uint32_t prefix = kmin;
+        if (kmin != kmax) {
+            hi = 32 - __clz(kmin ^ kmax);
+            prefix = hi >= 32 ? 0u : (kmin & (~0u << hi));
+        }
+        uint32_t inbin = (uint32_t)cnt;  // keys sharing the fixed bits
+        while (hi > 0 && inbin > (uint32_t)kSelCands) {
             const int width = hi >= kRadixBits ? kRadixBits : hi;
             const int shift = hi - width;
             const uint32_t dmask = (1u << width) - 1u;
             for (int i = tid; i < kRadixBins; i += NT) ts.hist[i] = 0;
             __syncthreads();
-            const uint64_t mask = (hi == 64) ? 0ull : (~0ull << hi);
-            for (int i = tid; i < cnt; i += NT) {
-                const uint64_t k = get(i);
-                if ((k & mask) == prefix) atomicAdd(&ts.hist[(uint32_t)(k >> shift) & dmask], 1u);
+            const uint32_t mask = hi >= 32 ? 0u : (~0u << hi);
+            for (int j = tid; j < n4; j += NT) {
+                const uint4 k = src.get4(j, cnt);
+                const uint32_t u[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (4 * j + q < cnt && (u[q] & mask) == prefix) atomicAdd(&ts.hist[(u[q] >> shift) & dmask], 1u);
             }
             __syncthreads();
-            {
-                // block-wide scan: each thread owns PER consecutive bins
-                constexpr int PER = kRadixBins / NT;
-                constexpr int NW = NT / 32;
-                uint32_t loc[PER];
-                uint32_t sum = 0;
-#pragma unroll
-                for (int q = 0; q < PER; ++q) {
-                    loc[q] = ts.hist[tid * PER + q];
-                    sum += loc[q];
-                }
-                uint32_t incl = sum;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += t;
-                }
-                if (lane == 31) ts.wsum[warp] = incl;
-                __syncthreads();
-                if (warp == 0) {
-                    uint32_t w = lane < NW ? ts.wsum[lane] : 0u;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint32_t t = __shfl_up_sync(0xffffffffu, w, o);
-                        if (lane >= o) w += t;
-                    }
-                    if (lane < NW) ts.wsum[lane] = w;  // inclusive warp prefix
-                }
-                __syncthreads();
-                incl += warp ? ts.wsum[warp - 1] : 0u;
-                const uint32_t excl = incl - sum;
-                if (excl < (uint32_t)need && (uint32_t)need <= incl) {
-                    uint32_t c = excl;
-#pragma unroll
-                    for (int q = 0; q < PER; ++q) {
-                        if (c + loc[q] >= (uint32_t)need) {
-                            ts.v = tid * PER + q;
-                            ts.before = c;
-                            ts.inbin = loc[q];
-                            break;
-                        }
-                        c += loc[q];
-                    }
-                }
-            }
-            __syncthreads();
-            const uint32_t v = ts.v, before = ts.before, inbin = ts.inbin;
-            __syncthreads();
-            prefix |= (uint64_t)v << shift;
-            need -= (int)before;
-            if ((int)inbin == need) {
-                bound = prefix | ((shift == 0) ? 0ull : ((1ull << shift) - 1ull));
-                break;
-            }
+            block_find_bin<NT, kRadixBins>(ts.hist, (uint32_t)need, ts);
+            prefix |= ts.v << shift;
+            need -= (int)ts.before;
+            inbin = ts.inbin;
             hi = shift;
+            if ((int)inbin == need) break;
+        }
+        lo = prefix;
+        hi_excl = lo + (1ull << hi);
+        if ((int)inbin == need) {
+            lo = hi_excl;  // the whole bin is taken
+            need = 0;
+        } else {
+            mode = inbin <= (uint32_t)kSelCands ? 1 : 2;  // mode 2: hi == 0, one key value
         }
     }
-    if (tid == 0) ts.count = 0;
+    uint64_t* cand = reinterpret_cast<uint64_t*>(ts.hist);
+    const uint32_t aux_cap = (uint32_t)sel_aux_slots(P2);
+    if (tid == 0) {
+        ts.count = 0;
+        ts.ncand = 0;
+        ts.nmem = 0;
+    }
     for (int i = tid; i < P2; i += NT) s_sel[i] = ~0ull;
     __syncthreads();
-    for (int base = 0; base < cnt; base += NT) {
-        const int i = base + tid;
-        bool act = false;
-        uint64_t k = 0;
-        if (i < cnt) {
-            k = get(i);
-            act = k <= bound;
+    for (int base = 0; base < n4; base += NT) {
+        const int j = base + tid;
+        uint32_t u[4] = {0u, 0u, 0u, 0u};
+        uint32_t am = 0u, bm = 0u;
+        if (j < n4) {
+            const uint4 k = src.get4(j, cnt);
+            u[0] = k.x;
+            u[1] = k.y;
+            u[2] = k.z;
+            u[3] = k.w;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (4 * j + q < cnt) {
+                    if ((uint64_t)u[q] < lo) am |= 1u << q;
+                    else if ((uint64_t)u[q] < hi_excl) bm |= 1u << q;
+                }
+            }
+            if (mode != 1) bm = 0u;
         }
-        const uint32_t am = __ballot_sync(0xffffffffu, act);
-        uint32_t slot = 0;
-        if (lane == 0 && am) slot = atomicAdd(&ts.count, (uint32_t)__popc(am));
-        slot = __shfl_sync(0xffffffffu, slot, 0);
-        if (act) {
-            const uint32_t idx = slot + __popc(am & ((1u << lane) - 1u));
-            if (idx < (uint32_t)P2) s_sel[idx] = k;
+        warp_append4(am, u, 4 * j, s_sel, &ts.count, (uint32_t)P2);
+        if (mode == 1) warp_append4(bm, u, 4 * j, cand, &ts.ncand, (uint32_t)kSelCands);
+    }
+    __syncthreads();
+    if (mode == 1) {
+        // the candidates' own descent, on 8-bit digits
+        const int nc = min((int)ts.ncand, kSelCands);
+        uint32_t* chist = ts.hist + 2 * kSelCands;
+        uint32_t cprefix = (uint32_t)lo;
+        int chi = hi;
+        int cin = nc;
+        while (chi > 0 && cin > kSelRankMax) {
+            const int width = chi >= kCandBits ? kCandBits : chi;
+            const int shift = chi - width;
+            const uint32_t dmask = (1u << width) - 1u;
+            for (int i = tid; i < kCandBins; i += NT) chist[i] = 0;
+            __syncthreads();
+            const uint32_t mask = chi >= 32 ? 0u : (~0u << chi);
+            for (int j = tid; j < nc; j += NT) {
+                const uint32_t u = (uint32_t)(cand[j] >> 32);
+                if ((u & mask) == cprefix) atomicAdd(&chist[(u >> shift) & dmask], 1u);
+            }
+            __syncthreads();
+            block_find_bin<NT, kCandBins>(chist, (uint32_t)need, ts);
+            cprefix |= ts.v << shift;
+            need -= (int)ts.before;
+            cin = (int)ts.inbin;
+            chi = shift;
+            if (cin == need) break;
+        }
+        const uint64_t c_lo = cprefix, c_hi = c_lo + (1ull << chi);
+        const bool whole = cin == need;
+        // candidates below the bin are taken (and the bin, when all of it is needed); the
+        // bin's keys otherwise go to a member list ranked pairwise
+        for (int base = 0; base < nc; base += NT) {
+            const int j = base + tid;
+            uint64_t key = 0;
+            bool tk = false, mem = false;
+            if (j < nc) {
+                key = cand[j];
+                const uint64_t u = key >> 32;
+                tk = u < c_lo || (whole && u < c_hi);
+                mem = !tk && u < c_hi;
+            }
+            warp_append(tk, key, s_sel, &ts.count, (uint32_t)P2);
+            warp_append(mem, key, s_aux, &ts.nmem, aux_cap);
+        }
+        __syncthreads();
+        const uint32_t taken = ts.count;
+        const int m = min((int)ts.nmem, (int)aux_cap);
+        for (int j = tid; j < m; j += NT) {
+            const uint64_t key = s_aux[j];
+            int r = 0;
+            for (int i = 0; i < m; ++i) r += s_aux[i] < key;
+            if (r < need && taken + r < (uint32_t)P2) s_sel[taken + r] = key;
+        }
+    } else if (mode == 2 && warp == 0) {
+        // keys equal to the K-th key: the smallest ids, scanned in id order
+        const uint32_t tie_key = (uint32_t)lo;
+        uint32_t taken = ts.count;
+        int left = need;
+        for (int base = 0; base < cnt && left > 0; base += 32) {
+            const int i = base + lane;
+            const bool eq = i < cnt && src(i) == tie_key;
+            const uint32_t m = __ballot_sync(0xffffffffu, eq);
+            const int r = __popc(m & ((1u << lane) - 1u));
+            if (eq && r < left && taken + r < (uint32_t)P2)
+                s_sel[taken + r] = ((uint64_t)tie_key << 32) | (uint32_t)i;
+            const int c = min(__popc(m), left);
+            taken += c;
+            left -= c;
         }
     }
     __syncthreads();
     return cnt < K ? cnt : K;
 }
 
+// Ascending sort of the take unique keys in s_sel[0..take) (s_sel padded with ~0 up to
+// P2).  A counting sort on the 11 bits below those the selected score keys share: the
+// digit counts, their exclusive scan, a scatter into s_aux, then each key's place in its
+// segment by counting the segment's smaller keys.  When a segment is longer than
+// kSelRankMax (or every score key is equal) the bitonic sort runs instead.  Must be
+// called by all NT threads.
+template <int NT>
+__device__ void block_sort_selected(uint64_t* s_sel, int take, int P2, uint64_t* s_aux, TopkSmem& ts) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (take <= 1) return;
+    if (tid == 0) {
+        ts.kmin = ~0u;
+        ts.kmax = 0u;
+        ts.segmax = 0u;
+    }
+    uint32_t mn = ~0u, mx = 0u;
+    for (int j = tid; j < take; j += NT) {
+        const uint32_t u = (uint32_t)(s_sel[j] >> 32);
+        mn = min(mn, u);
+        mx = max(mx, u);
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    __syncthreads();
+    if (lane == 0) {
+        atomicMin(&ts.kmin, mn);
+        atomicMax(&ts.kmax, mx);
+    }
+    for (int i = tid; i < kRadixBins; i += NT) ts.hist[i] = 0;
+    __syncthreads();
+    const uint32_t kmin = ts.kmin, kmax = ts.kmax;
+    bool counting = kmin != kmax;
+    if (counting) {
+        const int hi = 32 - __clz(kmin ^ kmax);
+        const int shift = hi > kRadixBits ? hi - kRadixBits : 0;
+        const uint32_t dmask = (1u << (hi - shift)) - 1u;
+        for (int j = tid; j < take; j += NT)
+            atomicAdd(&ts.hist[(uint32_t)(s_sel[j] >> (32 + shift)) & dmask], 1u);
+        __syncthreads();
+        block_excl_scan_bins<NT, kRadixBins>(ts.hist, ts);
+        counting = ts.segmax <= (uint32_t)kSelRankMax;
+        if (counting) {
+            for (int j = tid; j < take; j += NT) {
+                const uint64_t key = s_sel[j];
+                const uint32_t d = (uint32_t)(key >> (32 + shift)) & dmask;
+                s_aux[atomicAdd(&ts.hist[d], 1u)] = key;
+            }
+            __syncthreads();
+            // hist[d] is now the end of segment d, and hist[d - 1] its start
+            for (int j = tid; j < take; j += NT) {
+                const uint64_t key = s_aux[j];
+                const uint32_t d = (uint32_t)(key >> (32 + shift)) & dmask;
+                const int s0 = d ? (int)ts.hist[d - 1] : 0;
+                const int s1 = (int)ts.hist[d];
+                int r = s0;
+                for (int i = s0; i < s1; ++i) r += s_aux[i] < key;
+                s_sel[r] = key;
+            }
+            __syncthreads();
+        }
+    }
+    if (!counting) block_bitonic_sort<NT>(s_sel, P2);
+}
+
 // block_select_set followed by an ascending sort of the gathered keys.
-template <int NT, class Get>
-__device__ int block_topk(Get get, int cnt, int K, int P2, uint64_t* s_sel, TopkSmem& ts) {
-    const int take = block_select_set<NT>(get, cnt, K, P2, s_sel, ts);
-    block_bitonic_sort<NT>(s_sel, P2);
+template <int NT, class Src>
+__device__ int block_topk(const Src& src, int cnt, int K, int P2, uint64_t* s_sel, uint64_t* s_aux, TopkSmem& ts) {
+    const int take = block_select_set<NT>(src, cnt, K, P2, s_sel, s_aux, ts);
+    block_sort_selected<NT>(s_sel, take, P2, s_aux, ts);
     return take;
 }
 
-// Key getters for block_topk.
-struct SmemKeys {  // keys indexed by region id: desc(score) << 32 | id
+// Key sources for block_topk: the 32-bit score key desc(score) of id i, and of ids
+// 4j..4j+3 at once (entries at or past cnt undefined).
+struct SmemKeys {  // keys in shared memory, indexed by region id, 16-byte aligned and
+                   // readable up to the next multiple of 4
     const uint32_t* key;
-    __device__ __forceinline__ uint64_t operator()(int i) const {
-        return ((uint64_t)key[i] << 32) | (uint32_t)i;
-    }
+    __device__ __forceinline__ uint32_t operator()(int i) const { return key[i]; }
+    __device__ __forceinline__ uint4 get4(int j, int) const { return reinterpret_cast<const uint4*>(key)[j]; }
 };
 struct ScoreKeys {  // every score of the row, from global memory
     const float* scores;
-    __device__ __forceinline__ uint64_t operator()(int i) const {
-        return ((uint64_t)desc_key(scores[i]) << 32) | (uint32_t)i;
+    __device__ __forceinline__ uint32_t operator()(int i) const { return desc_key(scores[i]); }
+    __device__ __forceinline__ uint4 get4(int j, int cnt) const {
+        const int i = 4 * j;
+        return make_uint4(desc_key(scores[i]), i + 1 < cnt ? desc_key(scores[i + 1]) : 0u,
+                          i + 2 < cnt ? desc_key(scores[i + 2]) : 0u, i + 3 < cnt ? desc_key(scores[i + 3]) : 0u);
     }
 };
 
@@ -411,7 +716,8 @@ template <int HPG, bool FROM_SCORES>
 __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams p, int P2, int key_cap) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint64_t* s_sel = reinterpret_cast<uint64_t*>(smem);                 // P2
-    uint32_t* s_key = reinterpret_cast<uint32_t*>(s_sel + P2);           // key_cap
+    uint64_t* s_aux = s_sel + P2;                                        // sel_aux_slots(P2)
+    uint32_t* s_key = reinterpret_cast<uint32_t*>(s_aux + sel_aux_slots(P2));  // key_cap
     float* s_q = reinterpret_cast<float*>(s_key + key_cap);              // HPG * 64
     __shared__ TopkSmem ts;
 
@@ -429,7 +735,29 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
     const uint4* base = reinterpret_cast<const uint4*>(p.summ + ((int64_t)b * p.G + g) * p.r_cap * 64);
     float* exp_scores = p.scores ? p.scores + ((int64_t)n * p.G + g) * p.r_cap : nullptr;
     if constexpr (FROM_SCORES) {
-        for (int r = threadIdx.x; r < R; r += kFusedThreads) s_key[r] = desc_key(__ldcg(exp_scores + r));
+        // the row's scores: 16 bytes a thread and four loads in flight, where aligned
+        int r_done = 0;
+        if ((reinterpret_cast<uintptr_t>(exp_scores) & 15u) == 0) {
+            const float4* s4 = reinterpret_cast<const float4*>(exp_scores);
+            uint4* k4 = reinterpret_cast<uint4*>(s_key);
+            const int R4 = R >> 2;
+            constexpr int U = 4;
+            for (int j0 = 0; j0 < R4; j0 += U * kFusedThreads) {
+                float4 v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = j0 + u * kFusedThreads + threadIdx.x;
+                    v[u] = j < R4 ? __ldcg(s4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = j0 + u * kFusedThreads + threadIdx.x;
+                    if (j < R4) k4[j] = make_uint4(desc_key(v[u].x), desc_key(v[u].y), desc_key(v[u].z), desc_key(v[u].w));
+                }
+            }
+            r_done = R4 << 2;
+        }
+        for (int r = r_done + threadIdx.x; r < R; r += kFusedThreads) s_key[r] = desc_key(__ldcg(exp_scores + r));
     } else if constexpr (HPG == 4) {
         __shared__ uint4 s_qh[32];
         float w[4];
@@ -482,7 +810,7 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
         }
     }
     __syncthreads();
-    const int take = block_topk<kFusedThreads>(SmemKeys{s_key}, R, p.top_k, P2, s_sel, ts);
+    const int take = block_topk<kFusedThreads>(SmemKeys{s_key}, R, p.top_k, P2, s_sel, s_aux, ts);
     write_selection<kFusedThreads>(p, n, g, take, s_sel);
 }
 
@@ -895,7 +1223,9 @@ __device__ __noinline__ void select_all_scores(const ScoreParams& p, int ng, uin
     while (P2 < p.top_k) P2 <<= 1;
     uint64_t* s_sel = reinterpret_cast<uint64_t*>(ring);
     TopkSmem& ts = *reinterpret_cast<TopkSmem*>(ring + kMaxTopK * 8);
-    const int take = block_topk<kSplitThreads>(ScoreKeys{p.scores + (int64_t)ng * p.r_cap}, R, p.top_k, P2, s_sel, ts);
+    uint64_t* s_aux = reinterpret_cast<uint64_t*>(ring + kMaxTopK * 8 + ((sizeof(TopkSmem) + 15) & ~(size_t)15));
+    const int take = block_topk<kSplitThreads>(ScoreKeys{p.scores + (int64_t)ng * p.r_cap}, R, p.top_k, P2, s_sel,
+                                               s_aux, ts);
     write_selection<kSplitThreads>(p, n, ng - n * p.G, take, s_sel);
 }
 
@@ -1493,7 +1823,7 @@ template <int HPG, bool FROM_SCORES = false>
 cudaError_t fused_for(const ScoreParams& p, cudaStream_t stream, bool pdl) {
     const int P2 = pow2_at_least(p.top_k);
     const int key_cap = (p.r_cap < kFusedMaxRegions ? p.r_cap : kFusedMaxRegions);
-    const size_t smem = (size_t)P2 * 8 + (size_t)((key_cap + 3) & ~3) * 4 + HPG * 64 * 4;
+    const size_t smem = (size_t)(P2 + sel_aux_slots(P2)) * 8 + (size_t)((key_cap + 3) & ~3) * 4 + HPG * 64 * 4;
     auto kern = score_fused_kernel<HPG, FROM_SCORES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

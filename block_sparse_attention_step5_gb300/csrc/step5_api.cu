@@ -252,7 +252,7 @@ int choose_path(const step5_geometry* geom, int N, int B, int r_cap) {
     const int hpg = geom->idx_heads / G;
     int P2 = 1;
     while (P2 < geom->top_k) P2 <<= 1;
-    const int fused_need = P2 * 8 + ((r_cap + 3) & ~3) * 4 + hpg * 64 * 4;
+    const int fused_need = (P2 + (P2 > 512 ? P2 : 512)) * 8 + ((r_cap + 3) & ~3) * 4 + hpg * 64 * 4;
     const bool fused_fits = r_cap <= kFusedMaxRegions && fused_need <= 200 * 1024;
     int path;
     if (g_select_path == 1 || g_select_path == 2 || g_select_path == 3)
