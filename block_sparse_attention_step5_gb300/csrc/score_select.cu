@@ -378,32 +378,6 @@ __device__ __forceinline__ void warp_append(bool act, uint64_t key, uint64_t* li
     }
 }
 
-// Appends, for each set bit c of m, the key (u[c] << 32 | id0 + c) to list[*ctr ...]
-// (slots past cap dropped): one count scan and one atomic per warp, nothing when no lane
-// of the warp has a key.  Called by whole warps.
-__device__ __forceinline__ void warp_append4(uint32_t m, const uint32_t (&u)[4], int id0, uint64_t* list,
-                                             uint32_t* ctr, uint32_t cap) {
-    if (!__any_sync(0xffffffffu, m != 0u)) return;
-    const int lane = threadIdx.x & 31;
-    const uint32_t c = (uint32_t)__popc(m);
-    uint32_t incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    uint32_t slot = 0;
-    if (lane == 31) slot = atomicAdd(ctr, incl);
-    slot = __shfl_sync(0xffffffffu, slot, 31) + incl - c;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (m & (1u << q)) {
-            if (slot < cap) list[slot] = ((uint64_t)u[q] << 32) | (uint32_t)(id0 + q);
-            ++slot;
-        }
-    }
-}
-
 // Gathers the K smallest keys (desc(score) << 32 | id, i.e. by score key and then by id)
 // of ids 0..cnt-1 (all of them if cnt <= K) into s_sel[0..min(cnt, K)) in no particular
 // order, pads s_sel up to P2 (a power of two >= max(K, 32)) with ~0, returns min(cnt, K).
@@ -412,8 +386,9 @@ __device__ __forceinline__ void warp_append4(uint32_t m, const uint32_t (&u)[4],
 // over all keys, four per thread at a time: the range [smallest, largest] of the score
 // keys; then 11-bit digits below the bits that range fixes (scores of one row mostly
 // share sign and exponent), one pass each, until the K-th key's bin is taken whole,
-// holds at most kSelCands keys, or is one key value; then one pass that takes every key
-// below the bin and keeps the bin's keys as candidates.  The candidates descend by 8-bit
+// holds at most kSelCands keys, or is one key value; then a pass counting each thread's
+// keys below the bin and in it, and one writing them (every key below the bin taken, the
+// bin's keys kept as candidates), with one slot reservation per thread in between.  The candidates descend by 8-bit
 // digits until their bin is taken whole or holds at most kSelRankMax keys, which are
 // ranked against each other by (key, id).  A single key value shared by more than
 // kSelCands keys is resolved by one warp taking the smallest ids in id order.  Must be
@@ -502,27 +477,42 @@ __device__ int block_select_set(const Src& src, int cnt, int K, int P2, uint64_t
     }
     for (int i = tid; i < P2; i += NT) s_sel[i] = ~0ull;
     __syncthreads();
-    for (int base = 0; base < n4; base += NT) {
-        const int j = base + tid;
-        uint32_t u[4] = {0u, 0u, 0u, 0u};
-        uint32_t am = 0u, bm = 0u;
-        if (j < n4) {
+    {
+        // a thread counts its keys below the bin (taken) and in it (candidates), reserves
+        // its slots with one atomic per list, then writes them in a second sweep
+        const uint64_t b_hi = mode == 1 ? hi_excl : lo;
+        uint32_t na = 0, nb = 0;
+        for (int j = tid; j < n4; j += NT) {
             const uint4 k = src.get4(j, cnt);
-            u[0] = k.x;
-            u[1] = k.y;
-            u[2] = k.z;
-            u[3] = k.w;
+            const uint32_t u[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                if (4 * j + q < cnt) {
-                    if ((uint64_t)u[q] < lo) am |= 1u << q;
-                    else if ((uint64_t)u[q] < hi_excl) bm |= 1u << q;
+                const bool ok = 4 * j + q < cnt;
+                na += ok && (uint64_t)u[q] < lo;
+                nb += ok && (uint64_t)u[q] >= lo && (uint64_t)u[q] < b_hi;
+            }
+        }
+        uint32_t sa = na ? atomicAdd(&ts.count, na) : 0u;
+        uint32_t sb = nb ? atomicAdd(&ts.ncand, nb) : 0u;
+        for (int j = tid; j < n4 && (na | nb) != 0u; j += NT) {
+            const uint4 k = src.get4(j, cnt);
+            const uint32_t u[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = 4 * j + q;
+                if (i >= cnt) continue;
+                const uint64_t key = ((uint64_t)u[q] << 32) | (uint32_t)i;
+                if ((uint64_t)u[q] < lo) {
+                    if (sa < (uint32_t)P2) s_sel[sa] = key;
+                    ++sa;
+                    --na;
+                } else if ((uint64_t)u[q] < b_hi) {
+                    if (sb < (uint32_t)kSelCands) cand[sb] = key;
+                    ++sb;
+                    --nb;
                 }
             }
-            if (mode != 1) bm = 0u;
         }
-        warp_append4(am, u, 4 * j, s_sel, &ts.count, (uint32_t)P2);
-        if (mode == 1) warp_append4(bm, u, 4 * j, cand, &ts.ncand, (uint32_t)kSelCands);
     }
     __syncthreads();
     if (mode == 1) {
