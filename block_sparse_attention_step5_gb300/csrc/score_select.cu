@@ -1306,7 +1306,6 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
     __shared__ uint32_t s_w[kRankWarps * 32];
     __shared__ int s_thr[2], s_R[2];
     __shared__ uint32_t s_base[2];
-    __shared__ uint32_t s_gen1[kMaxShareSegs], s_gen2[kMaxShareSegs];
     const int tid = threadIdx.x;
     const int qd = tid & 3, slot = tid >> 2;
 
@@ -1375,18 +1374,6 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
             // requests of all SMs have drained
             s_tile[0] = next_tile(p, wk, kBoxRows);
             for (int k = 1; k < kScoreStages; ++k) s_tile[k] = next_tile(p, wk);
-        }
-        // with the first reads: the generation of each (row, group)'s threshold word (this
-        // launch publishes no threshold before every block covering it has arrived, and
-        // the launch before has finished) and the region counts of the first and last
-        // rows, so that neither is a round trip of its own after the scoring
-        if (tid <= ngB - ngA && tid < kMaxShareSegs) s_gen1[tid] = ld_relaxed_u32(p.thr + ngA + tid) >> 12;
-        if (tid == kSplitThreads - 1) {
-            int b, pos;
-            const int RA = row_regions(p, ngA / p.G, b, pos);
-            const int RB = row_regions(p, ngB / p.G, b, pos);
-            s_R[0] = RA < 0 ? 0 : RA;
-            s_R[1] = RB < 0 ? 0 : RB;
         }
         const int pos0 = row_pos_or0(p, n0);
         const int pos1 = n1 == n0 ? pos0 : row_pos_or0(p, n1);
@@ -1647,18 +1634,21 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
     // Every block that covers part of a (row, group) arrives once its histogram share is
     // in; the last one computes and publishes the (row, group)'s threshold bin.  The
     // threshold word's generation is read before arriving.
-    __shared__ int s_last[kMaxShareSegs];
+    __shared__ int s_last;
     __shared__ int s_tmp;
+    __shared__ uint32_t s_gen1[kMaxShareSegs], s_gen2[kMaxShareSegs];
     auto seg_first = [&](int ng) { return block_of((int64_t)ng * p.r_cap, total, gridDim.x); };
     auto seg_blocks = [&](int ng) { return block_of((int64_t)(ng + 1) * p.r_cap - 1, total, gridDim.x) - seg_first(ng) + 1; };
-    // (arrivals at every (row, group) of the share first, then the publications)
-    __syncthreads();  // the block's histogram additions come before its arrivals
-    if (tid == 0)
-        for (int ng = ngA; ng <= ngB; ++ng)
-            s_last[ng - ngA] = arrive_last(p.arrive1 + ng, (uint32_t)seg_blocks(ng));
-    __syncthreads();
-    for (int ng = ngA; ng <= ngB; ++ng)
-        if (s_last[ng - ngA]) publish_threshold(p, ng, s_gen1[ng - ngA], s_w, &s_tmp);
+    for (int ng = ngA; ng <= ngB; ++ng) {
+        __syncthreads();  // the block's histogram additions come before its arrival
+        if (tid == 0) {
+            const uint32_t gen = ld_acquire_u32(p.thr + ng) >> 12;
+            s_gen1[ng - ngA] = gen;
+            s_last = arrive_last(p.arrive1 + ng, (uint32_t)seg_blocks(ng));
+        }
+        __syncthreads();
+        if (s_last) publish_threshold(p, ng, s_gen1[ng - ngA], s_w, &s_tmp);
+    }
     STEP5_STAMP(1, 11);
     pdl_launch_dependents();
 
@@ -1666,6 +1656,11 @@ __global__ void __maxnreg__(kSplitMaxRegs) score_select_kernel(const __grid_cons
     if (keep_all) {
         // the thresholds (and R) of the share's one or two (row, group)s
         if (tid == 0) {
+            int b, pos;
+            const int RA = row_regions(p, ngA / p.G, b, pos);
+            const int RB = row_regions(p, ngB / p.G, b, pos);
+            s_R[0] = RA < 0 ? 0 : RA;
+            s_R[1] = RB < 0 ? 0 : RB;
             s_thr[0] = wait_threshold(p, ngA, s_gen1[0]);
             s_thr[1] = ngB != ngA ? wait_threshold(p, ngB, s_gen1[1]) : s_thr[0];
         }
