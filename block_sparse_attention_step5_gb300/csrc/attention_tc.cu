@@ -39,8 +39,9 @@ namespace {
 constexpr int kTcSoftmaxWarps = 4;                   // one thread per key of a tile
 constexpr int kTcSoftmaxThreads = kTcSoftmaxWarps * 32;
 constexpr int kTcMmaWarp = kTcSoftmaxWarps;           // issues the MMAs (lane 0)
-constexpr int kTcLoadWarp = kTcSoftmaxWarps + 1;      // issues the copies (16 lanes)
-constexpr int kTcThreads = kTcSoftmaxThreads + 64;
+constexpr int kTcLoadWarp = kTcSoftmaxWarps + 1;      // first of the warps issuing the copies
+constexpr int kTcLoadWarps = 2;                       // each issues 8 of a tile's 16 boxes
+constexpr int kTcThreads = kTcSoftmaxThreads + 32 + 32 * kTcLoadWarps;
 constexpr int kTcTileRegions = 16;
 constexpr int kTcSlots = 3;
 constexpr uint32_t kTcSlotBytes = kTcTileRegions * 2048;
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kTcThreads) sparse_attn_tc_kernel(const __grid
         prefetch_tmap(&kmap);
         prefetch_tmap(&vmap);
         for (int s = 0; s < kTcSlots; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], kTcLoadWarps);
             mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -218,9 +219,13 @@ __global__ void __launch_bounds__(kTcThreads) sparse_attn_tc_kernel(const __grid
         isv = !(j & 1);
         return (j & 1) ? (j + 1) >> 1 : (j - 2) >> 1;
     };
-    if (warp == kTcLoadWarp) {
-        // ---------------- load warp: every item in order, each into its slot once the
-        // product that read the slot's previous item is done; 16 lanes issue a tile's boxes
+    if (warp >= kTcLoadWarp) {
+        // ---------------- load warps: every item in order, each into its slot once the
+        // product that read the slot's previous item is done; load warp lw issues boxes
+        // 8 lw .. 8 lw + 7 of each tile (one per lane), so that a tile's copies are issued
+        // by two warps at once
+        constexpr int per = kTcTileRegions / kTcLoadWarps;
+        const int lw = warp - kTcLoadWarp;
         bool ok = true;
         int j = 0;
         for (; j <= last_item && ok; ++j) {
@@ -237,12 +242,13 @@ __global__ void __launch_bounds__(kTcThreads) sparse_attn_tc_kernel(const __grid
                 break;
             }
             int rid = -1;
-            const int ntok = lane < kTcTileRegions ? entry(tile * kTcTileRegions + lane, rid) : 0;
+            const int q = lw * per + lane;  // the tile entry this lane copies
+            const int ntok = lane < per ? entry(tile * kTcTileRegions + q, rid) : 0;
             const uint32_t have = __ballot_sync(0xffffffffu, ntok > 0);
             if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)__popc(have) * 2048u);
             __syncwarp();
             if (ntok > 0)
-                tma_load_3d(slots + slot * kTcSlotBytes + lane * 2048, isv ? &vmap : &kmap, &full[slot], 0,
+                tma_load_3d(slots + slot * kTcSlotBytes + q * 2048, isv ? &vmap : &kmap, &full[slot], 0,
                             (int)(row_base + (int64_t)rid * 8), 0);
         }
         if (!ok && lane == 0) {
