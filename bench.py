@@ -65,6 +65,27 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def bf16_peak():
+    """Dense bf16 tensor throughput (TFLOP/s, burst) and where it comes from."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        return float(json.load(open(path))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def attention_flops(w, geom):
+    """Tensor FLOPs of step (4): per row and KV group, S = Q K^T and O = P V over the
+    picked regions' tokens plus the own region's, for the group's query heads."""
+    hq_g = geom.num_q_heads // geom.num_kv_groups
+    f = 0
+    for n in range(w.N):
+        p = int(w.row_pos[n])
+        R = p // 8
+        keys = min(R, geom.top_k) * 8 + (p - 8 * R + 1)
+        f += geom.num_kv_groups * hq_g * keys * geom.head_dim * 2 * 2
+    return f
+
+
 class ClockSampler:
     """nvidia-smi samples (200 ms) of SM clock and throttle reasons during a region."""
 
@@ -561,6 +582,18 @@ def run_ours(args, rank, world, local_rank):
     rows = w.N * world
     value = whole_job_rate(w.N, world, head["ms"])
     score_gbs = head["bytes_score"] / (head["per_score"] / 1e3) / 1e9
+    if head["path"] == 3:
+        # many rows per sequence (prefill chunks): the attention dominates, on the tensor
+        # cores; its rows share regions through L2, so per-row bytes exceed DRAM's
+        tpeak, tkind = bf16_peak()
+        attn_tf = attention_flops(w, geom) / (head["per_attn"] / 1e3) / 1e12
+        roofline = {"kernel": "sparse_attn_tc_kernel (step5_sparse_attn, tcgen05 bf16)", "bound": "tensor",
+                    "achieved": round(attn_tf, 2), "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": round(attn_tf / tpeak, 4), "peak_kind": f"{tkind} dense bf16 (burst)",
+                    "algorithmic_flops_per_launch": attention_flops(w, geom), "traffic": None,
+                    "note": "the gathers come from L2 (a chunk's rows share their sequence's regions)"}
+    else:
+        roofline = None
     step_gbs = head["bytes_step"] / (head["ms"] / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -574,14 +607,16 @@ def run_ours(args, rank, world, local_rank):
                    "timing": "CUDA events around a CUDA-graph replay of the whole step",
                    "parallelism": f"replicas x{world}"},
         "step_hbm": {"bytes_per_step": head["bytes_step"], "achieved_gbs": round(step_gbs, 1),
-                     "peak_gbs": peak, "frac": round(step_gbs / peak, 4), "peak_kind": peak_kind},
+                     "peak_gbs": peak, "frac": round(step_gbs / peak, 4), "peak_kind": peak_kind,
+                     **({"note": "bytes counted per row; a chunk's rows share regions through L2, so this "
+                                 "exceeds what DRAM moves"} if head["path"] == 3 else {})},
         "breakdown_us": {"summarize": round(head["per_sum"] * 1e3, 2),
                          "score_select": round(head["per_score"] * 1e3, 2),
                          "attention": round(head["per_attn"] * 1e3, 2),
                          "attention_gated": round(head["per_gated"] * 1e3, 2),
                          "indexer_front": round(head["per_front"] * 1e3, 2),
                          "how": head["breakdown_how"]},
-        "roofline": {"kernel": {1: "score_fused_kernel (step5_index_score_topk, fused path)",
+        "roofline": roofline or {"kernel": {1: "score_fused_kernel (step5_index_score_topk, fused path)",
                                 2: "score_select_kernel (step5_index_score_topk, split path)",
                                 3: "score_tc_kernel + score_fused_kernel<select> (step5_index_score_topk, "
                                    "tensor-core path)"}[head["path"]],
