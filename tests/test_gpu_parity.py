@@ -297,6 +297,56 @@ def test_injected_ties_order_by_id(s5):
         full_check(s5, geom, w, t, path=path)
 
 
+def _cluster_summaries(summ, w, rng, copy=0.55, nudge=0.40):
+    """Most regions' summaries replaced by one base row (exact ties) or by the base row
+    with one code moved to its neighbouring finite e4m3 code (scores a hair apart), the
+    rest left as built: one (row, group)'s scores crowd into a sliver of their range."""
+    for b in range(w.B):
+        R = int(w.row_pos[w.row_seq == b].max()) // 8
+        for gg in range(summ.shape[1]):
+            base = summ[b, gg, 0].copy()
+            u = rng.random(R)
+            for r in range(1, R):
+                if u[r] < copy:
+                    summ[b, gg, r] = base
+                elif u[r] < copy + nudge:
+                    row = base.copy()
+                    d = int(rng.integers(0, row.shape[0]))
+                    c = int(row[d])
+                    mag = c & 0x7F
+                    row[d] = c + 1 if mag < 0x7E else c - 1  # never the NaN code 0x7F
+                    summ[b, gg, r] = row
+
+
+@pytest.mark.parametrize("case", ["fused_split", "tensor_core"])
+def test_clustered_scores_deep_descent(s5, case):
+    """Scores crowded into a sliver of their range with thousands of exact ties: the
+    block top-k's first digit leaves more than 512 keys in the K-th key's bin, so its
+    descent takes further levels (and, at a tie value, picks the smallest ids in order);
+    every path's picks must equal the oracle's selection from the same scores."""
+    geom = s5.STEP5_GEOMETRY
+    if case == "fused_split":
+        w = S.workload({"positions": [48001, 40003], "B": 2}, seed=43)
+        paths = (1, 2)
+    else:  # many rows of one sequence: the tensor-core scoring and the selection from scores
+        w = S.workload({"positions": list(range(44000, 44032)), "B": 1}, seed=43)
+        paths = (3,)
+    t = S.materialize(w, device="cuda")
+    h = host_inputs(t)
+    summ, _, _ = oracle.summarize_batch(h["idx_k"], h["idx_z"], h["cos"], h["sin"], w.sum_begin,
+                                        w.sum_end, w.r_cap, geom.rope_dims)
+    _cluster_summaries(summ, w, np.random.default_rng(5))
+    t["summaries"].copy_(torch.from_numpy(summ))
+    w.sum_end[:] = w.sum_begin
+    t["sum_end"].copy_(t["sum_begin"])
+    for path in paths:
+        g = full_check(s5, geom, w, t, path=path)
+        # the crowding worked: many exact ties among each row's scores
+        R = int(w.row_pos[0]) // 8
+        sc = g["scores"][0, 0, :R]
+        assert np.unique(sc).size < R // 4
+
+
 def test_repeat_calls_reuse_workspace(s5):
     geom = s5.STEP5_GEOMETRY
     w = S.workload({"positions": [30000, 4100, 70], "B": 3}, seed=17)
