@@ -61,3 +61,14 @@ def test_reference_arm_runs_on_rank_zero_only():
         steps = 1
 
     assert bench.run_reference(Args(), 1, 2) is None  # returns before any work
+
+
+def test_attention_flops_count_the_attended_keys():
+    """The tensor roofline's FLOPs: per row and KV group, 8 query heads x (picked regions'
+    tokens + own-region tokens) x 128 dims x 4 (Q K^T and P V, multiply and add).  Rows at
+    7, 8, 4,100 and 40,000 attend 8, 9, 4,101 and 4,097 keys."""
+    import bench
+    import synthetic as S
+    import block_sparse_attention_step5_gb300 as s5
+    w = S.workload({"positions": [7, 8, 4100, 40000], "B": 4})
+    assert bench.attention_flops(w, s5.STEP5_GEOMETRY) == (8 + 9 + 4101 + 4097) * 4 * 8 * 128 * 4
