@@ -5,18 +5,22 @@
 // indexer heads; the 512 smallest (-score, id) keys are kept, in key order.  Provider groups own contiguous blocks of indexer heads (vLLM Step5 DSA
 // geometry: the indexer's scores are summed within each provider group).
 //
-// Scoring runs on the CUDA cores.  With 4 indexer heads per group a thread scores whole
-// regions (two at a time against a shared-memory query broadcast); otherwise each region
-// is read as four 16-byte vectors, one per thread, and a butterfly completes the 64-dim
-// dot products.  Every e4m3 pair is widened to an f16 pair (exact: f16 holds every e4m3
-// value) and multiplied by the mixed-precision fma (f16 products, fp32 addend and
-// result, one rounding), which gives the bits of an fp32 fma on the decoded values.
-// Selection works on 64-bit keys (desc(score) << 32 | id), which are unique, so any
-// exact selection yields the same ordered ids.
+// Scoring: on the CUDA cores for the fused path (with 4 indexer heads per group a thread
+// scores whole regions, two at a time against a shared-memory query broadcast; otherwise
+// each region is read as four 16-byte vectors, one per thread, and a butterfly completes
+// the 64-dim dot products; every e4m3 pair is widened to an f16 pair, exact, and
+// multiplied by the mixed-precision fma, f16 products into an fp32 addend, which gives
+// the bits of an fp32 fma on the decoded values), and on the tensor cores (e4m3 MMAs into
+// TMEM) in the split path with 4 heads per group and in score_tc.cu.
+// Selection orders 64-bit keys (desc(score) << 32 | id), which are unique, so any exact
+// selection yields the same ordered ids.
 //
-// Two selection paths with identical results:
-//  * fused: one block per (row, group) scores every region into shared memory, then
-//    runs an 11-bit radix descent over the keys and a bitonic sort of the k winners.
+// Selection paths with identical picks from the same scores:
+//  * fused (and path 3's selection from stored scores): one block per (row, group)
+//    keeps the row's 32-bit score keys in shared memory and runs the block top-k: the
+//    keys' range, 11-bit digits below the bits the range fixes until the k-th key's bin
+//    is small, the keys below it taken, the bin's keys ranked on chip, then a counting
+//    sort of the picks.
 //  * split: one persistent launch for few rows with many regions (decode at 128K-1M
 //    tokens).  Blocks score an even share each and add a 12-bit histogram of the keys
 //    into global memory; after a grid barrier each block copies its keys in or above
