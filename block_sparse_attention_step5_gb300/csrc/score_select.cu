@@ -1207,7 +1207,7 @@ __device__ int wait_threshold(const ScoreParams& p, int ng, uint32_t gen) {
 }
 
 // The selection of (row, group) ng from every score of its row, by one block (the
-// candidate list overflowed): radix descent + bitonic sort.  Out of line: rarely run.
+// candidate list overflowed): the block top-k.  Out of line: rarely run.
 __device__ __noinline__ void select_all_scores(const ScoreParams& p, int ng, uint8_t* ring) {
     const int n = ng / p.G;
     int b, pos;
