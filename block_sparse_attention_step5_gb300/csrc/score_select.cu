@@ -399,7 +399,7 @@ __device__ __forceinline__ void warp_append(bool act, uint64_t key, uint64_t* li
 // called by all NT threads of the block.
 template <int NT, class Src>
 __device__ int block_select_set(const Src& src, int cnt, int K, int P2, uint64_t* s_sel, uint64_t* s_aux,
-                                TopkSmem& ts) {
+                                TopkSmem& ts, bool have_range = false, uint32_t mn_in = ~0u, uint32_t mx_in = 0u) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n4 = (cnt + 3) >> 2;
     uint64_t lo = 1ull << 32, hi_excl = 1ull << 32;  // keys below lo taken; [lo, hi_excl) the bin
@@ -411,8 +411,10 @@ __device__ int block_select_set(const Src& src, int cnt, int K, int P2, uint64_t
             ts.kmin = ~0u;
             ts.kmax = 0u;
         }
-        uint32_t mn = ~0u, mx = 0u;
-        for (int j = tid; j < n4; j += NT) {
+        // (have_range: the caller already holds this thread's share of the range, from
+        // the pass that wrote the keys)
+        uint32_t mn = mn_in, mx = mx_in;
+        for (int j = have_range ? n4 : tid; j < n4; j += NT) {
             const uint4 k = src.get4(j, cnt);
             const int i0 = 4 * j;
             mn = min(mn, k.x);
@@ -658,8 +660,9 @@ __device__ void block_sort_selected(uint64_t* s_sel, int take, int P2, uint64_t*
 
 // block_select_set followed by an ascending sort of the gathered keys.
 template <int NT, class Src>
-__device__ int block_topk(const Src& src, int cnt, int K, int P2, uint64_t* s_sel, uint64_t* s_aux, TopkSmem& ts) {
-    const int take = block_select_set<NT>(src, cnt, K, P2, s_sel, s_aux, ts);
+__device__ int block_topk(const Src& src, int cnt, int K, int P2, uint64_t* s_sel, uint64_t* s_aux, TopkSmem& ts,
+                          bool have_range = false, uint32_t mn = ~0u, uint32_t mx = 0u) {
+    const int take = block_select_set<NT>(src, cnt, K, P2, s_sel, s_aux, ts, have_range, mn, mx);
     block_sort_selected<NT>(s_sel, take, P2, s_aux, ts);
     return take;
 }
@@ -728,8 +731,10 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
     }
     const uint4* base = reinterpret_cast<const uint4*>(p.summ + ((int64_t)b * p.G + g) * p.r_cap * 64);
     float* exp_scores = p.scores ? p.scores + ((int64_t)n * p.G + g) * p.r_cap : nullptr;
+    uint32_t r_mn = ~0u, r_mx = 0u;  // this thread's share of the keys' range (selection from scores)
     if constexpr (FROM_SCORES) {
-        // the row's scores: 16 bytes a thread and four loads in flight, where aligned
+        // the row's scores: 16 bytes a thread and four loads in flight, where aligned; each
+        // thread keeps the range of the keys it wrote (the selection's first pass)
         int r_done = 0;
         if ((reinterpret_cast<uintptr_t>(exp_scores) & 15u) == 0) {
             const float4* s4 = reinterpret_cast<const float4*>(exp_scores);
@@ -746,12 +751,23 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int j = j0 + u * kFusedThreads + threadIdx.x;
-                    if (j < R4) k4[j] = make_uint4(desc_key(v[u].x), desc_key(v[u].y), desc_key(v[u].z), desc_key(v[u].w));
+                    if (j < R4) {
+                        const uint4 kk = make_uint4(desc_key(v[u].x), desc_key(v[u].y), desc_key(v[u].z),
+                                                    desc_key(v[u].w));
+                        k4[j] = kk;
+                        r_mn = min(r_mn, min(min(kk.x, kk.y), min(kk.z, kk.w)));
+                        r_mx = max(r_mx, max(max(kk.x, kk.y), max(kk.z, kk.w)));
+                    }
                 }
             }
             r_done = R4 << 2;
         }
-        for (int r = r_done + threadIdx.x; r < R; r += kFusedThreads) s_key[r] = desc_key(__ldcg(exp_scores + r));
+        for (int r = r_done + threadIdx.x; r < R; r += kFusedThreads) {
+            const uint32_t kk = desc_key(__ldcg(exp_scores + r));
+            s_key[r] = kk;
+            r_mn = min(r_mn, kk);
+            r_mx = max(r_mx, kk);
+        }
     } else if constexpr (HPG == 4) {
         __shared__ uint4 s_qh[32];
         float w[4];
@@ -804,7 +820,8 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
         }
     }
     __syncthreads();
-    const int take = block_topk<kFusedThreads>(SmemKeys{s_key}, R, p.top_k, P2, s_sel, s_aux, ts);
+    const int take = block_topk<kFusedThreads>(SmemKeys{s_key}, R, p.top_k, P2, s_sel, s_aux, ts, FROM_SCORES,
+                                               r_mn, r_mx);
     write_selection<kFusedThreads>(p, n, g, take, s_sel);
 }
 
