@@ -399,22 +399,28 @@ __device__ __forceinline__ void warp_append(bool act, uint64_t key, uint64_t* li
 // called by all NT threads of the block.
 template <int NT, class Src>
 __device__ int block_select_set(const Src& src, int cnt, int K, int P2, uint64_t* s_sel, uint64_t* s_aux,
-                                TopkSmem& ts, bool have_range = false, uint32_t mn_in = ~0u, uint32_t mx_in = 0u) {
+                                TopkSmem& ts, bool first_given = false) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n4 = (cnt + 3) >> 2;
     uint64_t lo = 1ull << 32, hi_excl = 1ull << 32;  // keys below lo taken; [lo, hi_excl) the bin
     int need = 0;                                   // keys still needed from the bin
     int hi = 0;                                     // bits of the bin's keys at and above hi agree
     int mode = 0;                                   // 0 bin taken whole, 1 candidates, 2 ties
-    if (cnt > K) {
+    // first_given: ts.hist already holds the counts of the keys' top kRadixBits bits (taken
+    // by the caller's pass that wrote the keys): they are the descent's first level, and
+    // no pass for the keys' range is needed
+    bool given = first_given;
+    if (cnt > K && given) {
+        need = K;
+        hi = 32;
+    }
+    if (cnt > K && !given) {
         if (tid == 0) {
             ts.kmin = ~0u;
             ts.kmax = 0u;
         }
-        // (have_range: the caller already holds this thread's share of the range, from
-        // the pass that wrote the keys)
-        uint32_t mn = mn_in, mx = mx_in;
-        for (int j = have_range ? n4 : tid; j < n4; j += NT) {
+        uint32_t mn = ~0u, mx = 0u;
+        for (int j = tid; j < n4; j += NT) {
             const uint4 k = src.get4(j, cnt);
             const int i0 = 4 * j;
             mn = min(mn, k.x);
@@ -435,29 +441,31 @@ __device__ int block_select_set(const Src& src, int cnt, int K, int P2, uint64_t
             atomicMax(&ts.kmax, mx);
         }
         __syncthreads();
-        const uint32_t kmin = ts.kmin, kmax = ts.kmax;
         need = K;
-        uint32_t prefix = kmin;
-        if (kmin != kmax) {
-            hi = 32 - __clz(kmin ^ kmax);
-            prefix = hi >= 32 ? 0u : (kmin & (~0u << hi));
-        }
+        if (ts.kmin != ts.kmax) hi = 32 - __clz(ts.kmin ^ ts.kmax);
+    }
+    if (cnt > K) {
+        uint32_t prefix = given ? 0u : (hi >= 32 ? 0u : (hi == 0 ? ts.kmin : (ts.kmin & (~0u << hi))));
         uint32_t inbin = (uint32_t)cnt;  // keys sharing the fixed bits
         while (hi > 0 && inbin > (uint32_t)kSelCands) {
             const int width = hi >= kRadixBits ? kRadixBits : hi;
             const int shift = hi - width;
             const uint32_t dmask = (1u << width) - 1u;
-            for (int i = tid; i < kRadixBins; i += NT) ts.hist[i] = 0;
-            __syncthreads();
-            const uint32_t mask = hi >= 32 ? 0u : (~0u << hi);
-            for (int j = tid; j < n4; j += NT) {
-                const uint4 k = src.get4(j, cnt);
-                const uint32_t u[4] = {k.x, k.y, k.z, k.w};
+            if (!given) {
+                for (int i = tid; i < kRadixBins; i += NT) ts.hist[i] = 0;
+                __syncthreads();
+                const uint32_t mask = hi >= 32 ? 0u : (~0u << hi);
+                for (int j = tid; j < n4; j += NT) {
+                    const uint4 k = src.get4(j, cnt);
+                    const uint32_t u[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (4 * j + q < cnt && (u[q] & mask) == prefix) atomicAdd(&ts.hist[(u[q] >> shift) & dmask], 1u);
+                    for (int q = 0; q < 4; ++q)
+                        if (4 * j + q < cnt && (u[q] & mask) == prefix)
+                            atomicAdd(&ts.hist[(u[q] >> shift) & dmask], 1u);
+                }
+                __syncthreads();
             }
-            __syncthreads();
+            given = false;
             block_find_bin<NT, kRadixBins>(ts.hist, (uint32_t)need, ts);
             prefix |= ts.v << shift;
             need -= (int)ts.before;
@@ -661,8 +669,8 @@ __device__ void block_sort_selected(uint64_t* s_sel, int take, int P2, uint64_t*
 // block_select_set followed by an ascending sort of the gathered keys.
 template <int NT, class Src>
 __device__ int block_topk(const Src& src, int cnt, int K, int P2, uint64_t* s_sel, uint64_t* s_aux, TopkSmem& ts,
-                          bool have_range = false, uint32_t mn = ~0u, uint32_t mx = 0u) {
-    const int take = block_select_set<NT>(src, cnt, K, P2, s_sel, s_aux, ts, have_range, mn, mx);
+                          bool first_given = false) {
+    const int take = block_select_set<NT>(src, cnt, K, P2, s_sel, s_aux, ts, first_given);
     block_sort_selected<NT>(s_sel, take, P2, s_aux, ts);
     return take;
 }
@@ -731,10 +739,12 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
     }
     const uint4* base = reinterpret_cast<const uint4*>(p.summ + ((int64_t)b * p.G + g) * p.r_cap * 64);
     float* exp_scores = p.scores ? p.scores + ((int64_t)n * p.G + g) * p.r_cap : nullptr;
-    uint32_t r_mn = ~0u, r_mx = 0u;  // this thread's share of the keys' range (selection from scores)
     if constexpr (FROM_SCORES) {
-        // the row's scores: 16 bytes a thread and four loads in flight, where aligned; each
-        // thread keeps the range of the keys it wrote (the selection's first pass)
+        // the row's scores: 16 bytes a thread and four loads in flight, where aligned; the
+        // counts of the keys' top kRadixBits bits are taken on the way (the selection's
+        // first digit)
+        for (int i = threadIdx.x; i < kRadixBins; i += kFusedThreads) ts.hist[i] = 0;
+        __syncthreads();
         int r_done = 0;
         if ((reinterpret_cast<uintptr_t>(exp_scores) & 15u) == 0) {
             const float4* s4 = reinterpret_cast<const float4*>(exp_scores);
@@ -755,8 +765,10 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
                         const uint4 kk = make_uint4(desc_key(v[u].x), desc_key(v[u].y), desc_key(v[u].z),
                                                     desc_key(v[u].w));
                         k4[j] = kk;
-                        r_mn = min(r_mn, min(min(kk.x, kk.y), min(kk.z, kk.w)));
-                        r_mx = max(r_mx, max(max(kk.x, kk.y), max(kk.z, kk.w)));
+                        atomicAdd(&ts.hist[kk.x >> (32 - kRadixBits)], 1u);
+                        atomicAdd(&ts.hist[kk.y >> (32 - kRadixBits)], 1u);
+                        atomicAdd(&ts.hist[kk.z >> (32 - kRadixBits)], 1u);
+                        atomicAdd(&ts.hist[kk.w >> (32 - kRadixBits)], 1u);
                     }
                 }
             }
@@ -765,8 +777,7 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
         for (int r = r_done + threadIdx.x; r < R; r += kFusedThreads) {
             const uint32_t kk = desc_key(__ldcg(exp_scores + r));
             s_key[r] = kk;
-            r_mn = min(r_mn, kk);
-            r_mx = max(r_mx, kk);
+            atomicAdd(&ts.hist[kk >> (32 - kRadixBits)], 1u);
         }
     } else if constexpr (HPG == 4) {
         __shared__ uint4 s_qh[32];
@@ -820,8 +831,7 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
         }
     }
     __syncthreads();
-    const int take = block_topk<kFusedThreads>(SmemKeys{s_key}, R, p.top_k, P2, s_sel, s_aux, ts, FROM_SCORES,
-                                               r_mn, r_mx);
+    const int take = block_topk<kFusedThreads>(SmemKeys{s_key}, R, p.top_k, P2, s_sel, s_aux, ts, FROM_SCORES);
     write_selection<kFusedThreads>(p, n, g, take, s_sel);
 }
 
