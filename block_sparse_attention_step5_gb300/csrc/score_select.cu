@@ -739,12 +739,12 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
     }
     const uint4* base = reinterpret_cast<const uint4*>(p.summ + ((int64_t)b * p.G + g) * p.r_cap * 64);
     float* exp_scores = p.scores ? p.scores + ((int64_t)n * p.G + g) * p.r_cap : nullptr;
+    // the counts of the keys' top kRadixBits bits are taken as the keys are written (the
+    // selection's first digit)
+    for (int i = threadIdx.x; i < kRadixBins; i += kFusedThreads) ts.hist[i] = 0;
+    __syncthreads();
     if constexpr (FROM_SCORES) {
-        // the row's scores: 16 bytes a thread and four loads in flight, where aligned; the
-        // counts of the keys' top kRadixBits bits are taken on the way (the selection's
-        // first digit)
-        for (int i = threadIdx.x; i < kRadixBins; i += kFusedThreads) ts.hist[i] = 0;
-        __syncthreads();
+        // the row's scores: 16 bytes a thread and four loads in flight, where aligned
         int r_done = 0;
         if ((reinterpret_cast<uintptr_t>(exp_scores) & 15u) == 0) {
             const float4* s4 = reinterpret_cast<const float4*>(exp_scores);
@@ -797,11 +797,15 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
             float sa, sb;
             score_rows2(va, vb, s_qh, w, sa, sb);
             if (ra < R) {
-                s_key[ra] = desc_key(sa);
+                const uint32_t ka = desc_key(sa);
+                s_key[ra] = ka;
+                atomicAdd(&ts.hist[ka >> (32 - kRadixBits)], 1u);
                 if (exp_scores) exp_scores[ra] = sa;
             }
             if (rb < R) {
-                s_key[rb] = desc_key(sb);
+                const uint32_t kb = desc_key(sb);
+                s_key[rb] = kb;
+                atomicAdd(&ts.hist[kb >> (32 - kRadixBits)], 1u);
                 if (exp_scores) exp_scores[rb] = sb;
             }
         }
@@ -825,13 +829,15 @@ __global__ void __launch_bounds__(kFusedThreads) score_fused_kernel(ScoreParams 
             const float mysc = qd == 0 ? sc[0] : qd == 1 ? sc[1] : qd == 2 ? sc[2] : sc[3];
             const int r = r0 + qd * 64 + slot;
             if (r < R) {
-                s_key[r] = desc_key(mysc);
+                const uint32_t k = desc_key(mysc);
+                s_key[r] = k;
+                atomicAdd(&ts.hist[k >> (32 - kRadixBits)], 1u);
                 if (exp_scores) exp_scores[r] = mysc;
             }
         }
     }
     __syncthreads();
-    const int take = block_topk<kFusedThreads>(SmemKeys{s_key}, R, p.top_k, P2, s_sel, s_aux, ts, FROM_SCORES);
+    const int take = block_topk<kFusedThreads>(SmemKeys{s_key}, R, p.top_k, P2, s_sel, s_aux, ts, true);
     write_selection<kFusedThreads>(p, n, g, take, s_sel);
 }
 
