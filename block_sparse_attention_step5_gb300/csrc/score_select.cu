@@ -386,17 +386,19 @@ __device__ __forceinline__ void warp_append(bool act, uint64_t key, uint64_t* li
 // of ids 0..cnt-1 (all of them if cnt <= K) into s_sel[0..min(cnt, K)) in no particular
 // order, pads s_sel up to P2 (a power of two >= max(K, 32)) with ~0, returns min(cnt, K).
 // src(i) returns the 32-bit score key of id i and src.get4(j, cnt) those of ids 4j..4j+3
-// (entries past cnt undefined); s_aux holds sel_aux_slots(P2) keys of scratch.  Passes
-// over all keys, four per thread at a time: the range [smallest, largest] of the score
-// keys; then 11-bit digits below the bits that range fixes (scores of one row mostly
-// share sign and exponent), one pass each, until the K-th key's bin is taken whole,
-// holds at most kSelCands keys, or is one key value; then a pass counting each thread's
-// keys below the bin and in it, and one writing them (every key below the bin taken, the
-// bin's keys kept as candidates), with one slot reservation per thread in between.  The candidates descend by 8-bit
-// digits until their bin is taken whole or holds at most kSelRankMax keys, which are
-// ranked against each other by (key, id).  A single key value shared by more than
-// kSelCands keys is resolved by one warp taking the smallest ids in id order.  Must be
-// called by all NT threads of the block.
+// (entries past cnt undefined); s_aux holds sel_aux_slots(P2) keys of scratch.
+// A radix descent over 11-bit digits, one pass over all keys each (four per thread per
+// 16-byte shared load), until the K-th key's bin is taken whole, holds at most kSelCands
+// keys, or is one key value.  The first digit is either the keys' top bits, counted by
+// the caller as it wrote the keys (first_given: ts.hist holds those counts), or the 11
+// bits below those that the range [smallest, largest] of the keys fixes (a pass for the
+// range first: scores of one row mostly share sign and exponent).  Then a pass counts
+// each thread's keys below the bin and in it and one writes them (every key below the
+// bin taken, the bin's keys kept as candidates), with one slot reservation per thread in
+// between.  The candidates descend by 8-bit digits until their bin is taken whole or
+// holds at most kSelRankMax keys, which are ranked against each other by (key, id).  A
+// single key value shared by more than kSelCands keys is resolved by one warp taking the
+// smallest ids in id order.  Must be called by all NT threads of the block.
 template <int NT, class Src>
 __device__ int block_select_set(const Src& src, int cnt, int K, int P2, uint64_t* s_sel, uint64_t* s_aux,
                                 TopkSmem& ts, bool first_given = false) {
